@@ -1,0 +1,158 @@
+"""CPU oracle for the V:N:M format and SpMM (ctypes wrapper of vnm_oracle.c).
+
+TEST INFRASTRUCTURE ONLY: only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / ``--impl reference`` legs of ``bench.py`` may import this
+package. The product path (``structured_sparse_matmul_gb300``) never imports
+it, and the two share no code.
+
+The C source restates "VENOM: A Vectorized N:M Format for Unleashing the
+Power of Sparse Tensor Cores", section 3 (Figures 2 and 3) and section 4
+(Figure 4), with the 2:4 packing of the lecture notes "2:4 sparsity on sparse
+tensor cores" ("The compressed format", "Worked: compress a 2 x 8 matrix").
+Every function is pinned by tests/test_oracle.py.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Optional, Sequence, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "vnm_oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle_vnm.so")
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+OK, INVALID, NONFINITE, NOMEM = 0, 1, 4, 6
+
+
+class OracleError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"oracle {what} returned {code}")
+        self.code = code
+
+
+def build(src: str = _SRC, out: str = _LIB_PATH, defines: Sequence[str] = ()) -> str:
+    """Compile the oracle with gcc (plain C11, no fast-math, no FMA contraction)."""
+    os.makedirs(os.path.dirname(out), exist_ok=True)
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared",
+           *[f"-D{d}" for d in defines], src, "-o", out + ".tmp", "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(out + ".tmp", out)
+    return out
+
+
+def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
+    p, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+    lib.oracle_sizes.argtypes = [i64, i64, i32, i32, p, p, p]
+    lib.oracle_compress.argtypes = [p, i64, i64, i64, i32, i32, p, p, p]
+    lib.oracle_decompress.argtypes = [p, p, p, i64, i64, i32, i32, p, i64]
+    spmm_args = [p, p, p, i64, i64, i32, i32, p, i64, i64, p, i64, p]
+    lib.oracle_spmm_f32.argtypes = spmm_args
+    lib.oracle_spmm_f64.argtypes = spmm_args
+    for f in (lib.oracle_sizes, lib.oracle_compress, lib.oracle_decompress, lib.oracle_spmm_f32,
+              lib.oracle_spmm_f64):
+        f.restype = ctypes.c_int
+    return lib
+
+
+def load_from(path: str) -> ctypes.CDLL:
+    """Load an oracle shared library built from ``path`` (tests load variants)."""
+    return _declare(ctypes.CDLL(path))
+
+
+def lib() -> ctypes.CDLL:
+    """The oracle library, built on first use if missing or older than its source."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if (not os.path.exists(_LIB_PATH)
+                    or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)):
+                build()
+            _lib = load_from(_LIB_PATH)
+        return _lib
+
+
+def _ptr(a: Optional[np.ndarray]) -> Optional[int]:
+    return None if a is None else a.ctypes.data
+
+
+def sizes(R: int, K: int, V: int, M: int, L: Optional[ctypes.CDLL] = None) -> Tuple[int, int, int]:
+    """(number of fp16 values, bytes of m-indices, bytes of column-loc)."""
+    L = L or lib()
+    v, m, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    rc = L.oracle_sizes(R, K, V, M, ctypes.byref(v), ctypes.byref(m), ctypes.byref(c))
+    if rc != OK:
+        raise OracleError(rc, "sizes")
+    return v.value, m.value, c.value
+
+
+def meta_pitch(K: int, M: int) -> int:
+    """Bytes per row of m-indices (2 bits per stored value, rounded up)."""
+    return (2 * (K // M) + 3) // 4
+
+
+def compress(W: np.ndarray, V: int, M: int, L: Optional[ctypes.CDLL] = None):
+    """Magnitude V:N:M compress of an fp16 R x K matrix.
+
+    Returns ``(values, meta, colidx)``: values uint16 [R, 2K/M] (fp16 bit
+    patterns), meta uint8 [R, ceil(2K/M/4)], colidx uint8 [R/V, K/M, 4].
+    """
+    L = L or lib()
+    W = np.ascontiguousarray(W, dtype=np.float16)
+    R, K = W.shape
+    nv, nm, nc = sizes(R, K, V, M, L)
+    values = np.zeros((R, 2 * (K // M)), dtype=np.uint16)
+    meta = np.zeros((R, meta_pitch(K, M)), dtype=np.uint8)
+    colidx = np.zeros((R // V, K // M, 4), dtype=np.uint8)
+    assert values.size == nv and meta.size == nm and colidx.size == nc
+    rc = L.oracle_compress(_ptr(W), K, R, K, V, M, _ptr(values), _ptr(meta), _ptr(colidx))
+    if rc != OK:
+        raise OracleError(rc, "compress")
+    return values, meta, colidx
+
+
+def decompress(values: np.ndarray, meta: np.ndarray, colidx: np.ndarray, R: int, K: int, V: int,
+               M: int, L: Optional[ctypes.CDLL] = None) -> np.ndarray:
+    """Dense fp16 R x K from the compressed arrays (pruned positions +0.0)."""
+    L = L or lib()
+    values = np.ascontiguousarray(values, dtype=np.uint16)
+    meta = np.ascontiguousarray(meta, dtype=np.uint8)
+    colidx = np.ascontiguousarray(colidx, dtype=np.uint8)
+    W = np.empty((R, K), dtype=np.uint16)
+    rc = L.oracle_decompress(_ptr(values), _ptr(meta), _ptr(colidx), R, K, V, M, _ptr(W), K)
+    if rc != OK:
+        raise OracleError(rc, "decompress")
+    return W.view(np.float16)
+
+
+def spmm(values: np.ndarray, meta: np.ndarray, colidx: np.ndarray, R: int, K: int, V: int, M: int,
+         B: np.ndarray, rows: Optional[Sequence[int]] = None, acc: str = "f32",
+         L: Optional[ctypes.CDLL] = None) -> np.ndarray:
+    """C[rows, :] = A_vnm[rows, :] . B, accumulated in ``acc`` ("f32" or "f64").
+
+    B is fp16 K x N. Returns float32 (acc="f32") or float64 (acc="f64") of
+    shape [len(rows), N] (all R rows when ``rows`` is None).
+    """
+    L = L or lib()
+    values = np.ascontiguousarray(values, dtype=np.uint16)
+    meta = np.ascontiguousarray(meta, dtype=np.uint8)
+    colidx = np.ascontiguousarray(colidx, dtype=np.uint8)
+    B = np.ascontiguousarray(B, dtype=np.float16)
+    assert B.shape[0] == K
+    N = B.shape[1]
+    rows_arr = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    n_rows = R if rows_arr is None else rows_arr.size
+    dt = np.float32 if acc == "f32" else np.float64
+    C = np.zeros((n_rows, N), dtype=dt)
+    fn = L.oracle_spmm_f32 if acc == "f32" else L.oracle_spmm_f64
+    rc = fn(_ptr(values), _ptr(meta), _ptr(colidx), R, K, V, M, _ptr(B), N, N, _ptr(rows_arr),
+            n_rows, _ptr(C))
+    if rc != OK:
+        raise OracleError(rc, "spmm")
+    return C

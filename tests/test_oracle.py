@@ -1,0 +1,404 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each ``check_*`` function pins one part of the oracle against something other
+than the oracle itself: the worked example printed in the lecture notes "2:4
+sparsity on sparse tensor cores", the storage arithmetic printed there and in
+"VENOM" section 3, brute-force enumeration of every candidate subset, format
+invariants, round trips, and numpy's own fp64 matmul. ``test_mutants_are_caught``
+plants plausible mistakes in copies of the oracle source and checks that at
+least one pin fails for each.
+"""
+import itertools
+import os
+import re
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from conftest import read_fixture
+from structured_sparse_matmul_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _floats(s):
+    return [float(x) for x in s.split()]
+
+
+def _slots_of(meta_row, n):
+    """Decode n 2-bit slots of one m-index row under the LSB-first reading."""
+    return [(int(meta_row[t // 4]) >> (2 * (t % 4))) & 3 for t in range(n)]
+
+
+# ----------------------------------------------------------------------------
+# pins
+# ----------------------------------------------------------------------------
+
+def check_worked_example(L):
+    """The 2 x 8 matrix of "Worked: compress a 2 x 8 matrix and count bits"."""
+    fx = read_fixture(os.path.join(GOLDEN, "worked_2x8.txt"))
+    W = np.array([_floats(fx["dense_row0"]), _floats(fx["dense_row1"])], dtype=np.float16)
+    for V in (1, 2):
+        values, meta, colidx = oracle.compress(W, V, 4, L)
+        for r in range(2):
+            want_vals = np.array(_floats(fx[f"values_row{r}"]), dtype=np.float16)
+            assert values[r].tobytes() == want_vals.tobytes(), (V, r, values[r])
+            want_idx = [int(b, 2) for b in fx[f"indices_row{r}"].split()]
+            assert _slots_of(meta[r], 4) == want_idx, (V, r, meta[r])
+            # indices are the kept slots of each group, ascending
+            kept = [tuple(int(x) for x in g.split(",")) for g in fx[f"kept_row{r}"].split()]
+            assert [tuple(want_idx[0:2]), tuple(want_idx[2:4])] == kept
+            # the packed byte of the 4 printed 2-bit tags, LSB first
+            assert int(meta[r][0]) == sum(want_idx[t] << (2 * t) for t in range(4))
+        # M = 4: column-loc is the identity in every block
+        assert (colidx == np.array([0, 1, 2, 3], dtype=np.uint8)).all()
+    # the printed bytes of this packing: row 0 -> 0xD8, row 1 -> 0xC9
+    values, meta, colidx = oracle.compress(W, 1, 4, L)
+    assert meta[:, 0].tolist() == [0xD8, 0xC9]
+
+
+def check_worked_local_index(L):
+    """"slot 1 of the second group is column 4 + 1 = 5" (decompress position)."""
+    fx = read_fixture(os.path.join(GOLDEN, "worked_2x8.txt"))
+    W = np.array([_floats(fx["dense_row0"]), _floats(fx["dense_row1"])], dtype=np.float16)
+    values, meta, colidx = oracle.compress(W, 1, 4, L)
+    D = oracle.decompress(values, meta, colidx, 2, 8, 1, 4, L)
+    g = dict(kv.split("=") for kv in fx["local_index"].split())
+    col = int(g["column"])
+    assert col == 4 * int(g["group"]) + int(g["slot"])
+    assert D[0, col] == np.float16(0.7)
+    # kept positions hold the dense values, pruned ones are +0.0
+    kept0 = {0, 2, 5, 7}
+    for k in range(8):
+        if k in kept0:
+            assert D[0, k] == W[0, k]
+        else:
+            assert D[0, k].view(np.uint16) == 0
+
+
+def check_worked_product(L):
+    """Row 0 times B: 0.9*b0 - 0.4*b2 + 0.7*b5 - 1.2*b7 (with fp16 weights)."""
+    fx = read_fixture(os.path.join(GOLDEN, "worked_2x8.txt"))
+    W = np.array([_floats(fx["dense_row0"]), _floats(fx["dense_row1"])], dtype=np.float16)
+    values, meta, colidx = oracle.compress(W, 1, 4, L)
+    terms = []
+    for term in fx["product_row0"].split():
+        coef, b = term.split("*")
+        terms.append((float(np.float16(float(coef))), int(b[1:])))
+    B = np.zeros((8, 3), dtype=np.float16)
+    B[:, 0] = np.arange(1, 9)
+    B[:, 1] = np.array([0.5, -2, 3, 0.25, 7, -1, 1.5, 4])
+    B[:, 2] = 1
+    want = np.array([sum(c * float(B[k, n]) for c, k in terms) for n in range(3)])
+    got64 = oracle.spmm(values, meta, colidx, 2, 8, 1, 4, B, rows=[0], acc="f64", L=L)[0]
+    assert np.allclose(got64, want, rtol=1e-15, atol=0)
+    got32 = oracle.spmm(values, meta, colidx, 2, 8, 1, 4, B, rows=[0], acc="f32", L=L)[0]
+    assert np.allclose(got32, want, rtol=1e-6, atol=1e-7)
+
+
+def check_storage_arithmetic(L):
+    """Storage counts printed in the lecture notes and in VENOM section 3."""
+    fx = read_fixture(os.path.join(GOLDEN, "worked_2x8.txt"))
+    bits = dict(kv.split("=") for kv in fx["fp16_bits"].split())
+    nv, nm, nc = oracle.sizes(2, 8, 1, 4, L)
+    assert nv * 16 == int(bits["values"])
+    assert nm * 8 == int(bits["indices"])
+    assert nv * 16 + nm * 8 == int(bits["total"])
+    assert (nv * 16 + nm * 8) / (2 * 8 * 16) == float(bits["ratio"])
+    nv, nm, nc = oracle.sizes(512, 1024, 1, 4, L)
+    assert nm * 8 == int(fx["meta_bits_512x1024"])
+    assert nm == 64 * 1024
+    # VENOM Figure 3: values and m-indices R x K/M*2, column-loc R/V x K/M x 4
+    f3 = read_fixture(os.path.join(GOLDEN, "venom_fig3.txt"))
+    R, K, V, M = (int(f3[k]) for k in ("R", "K", "V", "M"))
+    nv, nm, nc = oracle.sizes(R, K, V, M, L)
+    assert nv == len(f3["m_indices"].split()) == R * K // M * 2
+    assert nc == len(f3["column_loc"].split()) == R // V * K // M * 4
+    # "For V = 128, the overhead is ~13.28%": (2-bit m-index per value + an
+    # 8-bit column-loc entry per 4 columns every V rows) over 16-bit values
+    nv, nm, nc = oracle.sizes(1024, 4096, 128, 8, L)
+    overhead = (nm * 8 + nc * 8) / (nv * 16)
+    assert round(100 * overhead, 2) == float(f3["overhead_v128_percent"])
+
+
+def _brute_force_compress(W, V, M):
+    """All-subset enumeration: the 4-column subset of largest total L1 per
+    block, then the 2-of-4 pair of largest |a|+|b| per row; on ties the
+    lexicographically smallest subset (itertools.combinations order)."""
+    R, K = W.shape
+    Wd = W.astype(np.float64)
+    sel = np.zeros((R // V, K // M, 4), dtype=np.int64)
+    pairs = np.zeros((R, K // M, 2), dtype=np.int64)
+    for i in range(R // V):
+        for j in range(K // M):
+            blk = np.abs(Wd[i * V:(i + 1) * V, j * M:(j + 1) * M])
+            l1 = [sum(blk[:, c].tolist()) for c in range(M)]  # exact for these dyadic values
+            best, best_s = None, None
+            for sub in itertools.combinations(range(M), 4):
+                s = sum(l1[c] for c in sub)
+                if best_s is None or s > best_s:
+                    best, best_s = sub, s
+            sel[i, j] = best
+            for r in range(V):
+                a = [abs(float(Wd[i * V + r, j * M + c])) for c in best]
+                bp, bs = None, None
+                for pr in itertools.combinations(range(4), 2):
+                    s = a[pr[0]] + a[pr[1]]
+                    if bs is None or s > bs:
+                        bp, bs = pr, s
+                pairs[i * V + r, j] = bp
+    return sel, pairs
+
+
+def _check_against_brute_force(L, W, V, M):
+    R, K = W.shape
+    values, meta, colidx = oracle.compress(W, V, M, L)
+    sel, pairs = _brute_force_compress(W, V, M)
+    assert (colidx.astype(np.int64) == sel).all(), "column-loc differs from brute force"
+    Wb = W.view(np.uint16)
+    for r in range(R):
+        slots = _slots_of(meta[r], 2 * (K // M))
+        for j in range(K // M):
+            assert (slots[2 * j], slots[2 * j + 1]) == tuple(pairs[r, j]), (r, j)
+            for t in range(2):
+                c = j * M + int(sel[r // V, j, pairs[r, j][t]])
+                assert values[r, 2 * j + t] == Wb[r, c], (r, j, t)
+
+
+def check_brute_force_ties(L):
+    """Tie-heavy inputs: values from {0, +-0.5, +-1}, many equal sums."""
+    k = 0
+    for M in (4, 5, 6, 8, 12):
+        for V in (1, 2, 4):
+            W = inputs.choice_f16((2 * V, 3 * M), 77, k, [0, 0.5, -0.5, 1, -1, 0.0])
+            k += 1
+            _check_against_brute_force(L, W, V, M)
+
+
+def check_brute_force_subnormals(L):
+    """Mixed subnormal / normal magnitudes, where the exact values decide."""
+    tiny = [1023 * 2.0 ** -24, -1023 * 2.0 ** -24, 1.5 * 2.0 ** -14, 2.0 ** -13, -(2.0 ** -13),
+            3 * 2.0 ** -24, 0.0, -0.0]
+    for k, (V, M) in enumerate(((1, 6), (2, 8), (3, 5))):
+        W = inputs.choice_f16((2 * V, 4 * M), 91, k, tiny)
+        _check_against_brute_force(L, W, V, M)
+
+
+def check_brute_force_normal(L):
+    """N(0, 0.02) inputs (the workloads' distribution), M up to 16."""
+    for k, (V, M) in enumerate(((4, 4), (2, 7), (4, 8), (1, 16))):
+        W = inputs.normal_f16((2 * V, 2 * M), 55, k, 0.02)
+        _check_against_brute_force(L, W, V, M)
+
+
+def check_invariants_and_round_trip(L):
+    """Format invariants and decompress(compress(W)) on random shapes."""
+    k = 0
+    for (R, K, V, M) in ((32, 64, 16, 4), (64, 128, 64, 8), (128, 96, 32, 12), (16, 512, 8, 32),
+                         (8, 256, 8, 256)):
+        W = inputs.normal_f16((R, K), 42, k, 0.02)
+        k += 1
+        values, meta, colidx = oracle.compress(W, V, M, L)
+        # column-loc: 4 distinct, strictly ascending indices < M per block
+        assert (np.diff(colidx.astype(np.int64), axis=2) > 0).all()
+        assert int(colidx.max()) < M
+        D = oracle.decompress(values, meta, colidx, R, K, V, M, L)
+        Wb, Db = W.view(np.uint16), D.view(np.uint16)
+        kept = np.zeros((R, K), dtype=bool)
+        for r in range(R):
+            slots = _slots_of(meta[r], 2 * (K // M))
+            for j in range(K // M):
+                s0, s1 = slots[2 * j], slots[2 * j + 1]
+                assert s0 < s1  # two distinct slots, ascending
+                for s in (s0, s1):
+                    kept[r, j * M + int(colidx[r // V, j, s])] = True
+        # exactly 2 kept per (row, block): density 2/M
+        assert kept.sum() == R * (K // M) * 2
+        assert (kept.reshape(R, K // M, M).sum(axis=2) == 2).all()
+        # kept positions are bit copies of W, pruned ones +0.0
+        assert (Db[kept] == Wb[kept]).all()
+        assert (Db[~kept] == 0).all()
+        # kept columns lie inside the block's column-loc
+        cols = kept.reshape(R // V, V, K // M, M).any(axis=1)
+        for i in range(R // V):
+            for j in range(K // M):
+                assert set(np.nonzero(cols[i, j])[0]) <= set(colidx[i, j].tolist())
+        # the 2 kept of each row are the 2 largest |w| of its 4 selected
+        for r in range(min(R, 8)):
+            for j in range(K // M):
+                sel = colidx[r // V, j].astype(np.int64) + j * M
+                mags = np.abs(W[r, sel].astype(np.float64))
+                kept_mags = np.abs(D[r, sel].astype(np.float64))[kept[r, sel]]
+                assert sorted(kept_mags) == sorted(mags)[2:]
+        # compress is idempotent on its own output (value-equal: +-0 may move)
+        v2, m2, c2 = oracle.compress(D, V, M, L)
+        D2 = oracle.decompress(v2, m2, c2, R, K, V, M, L)
+        assert (D2.astype(np.float64) == D.astype(np.float64)).all()
+
+
+def check_spmm_against_numpy(L):
+    """fp64 oracle SpMM equals numpy's fp64 matmul of the decompressed A."""
+    k = 0
+    for (R, K, N, V, M) in ((16, 32, 5, 8, 4), (32, 64, 17, 16, 8), (12, 60, 3, 4, 5),
+                            (8, 64, 9, 8, 16)):
+        A = inputs.normal_f16((R, K), 7, k, 0.02)
+        B = inputs.normal_f16((K, N), 7, k + 100, 1.0)
+        k += 1
+        values, meta, colidx = oracle.compress(A, V, M, L)
+        D = oracle.decompress(values, meta, colidx, R, K, V, M, L).astype(np.float64)
+        ref = D @ B.astype(np.float64)
+        got = oracle.spmm(values, meta, colidx, R, K, V, M, B, acc="f64", L=L)
+        assert np.allclose(got, ref, rtol=1e-12, atol=1e-14)
+        # fp32 accumulation: within the standard bound K * 2^-24 * sum |a||b|
+        got32 = oracle.spmm(values, meta, colidx, R, K, V, M, B, acc="f32", L=L).astype(np.float64)
+        bound = K * 2.0 ** -24 * (np.abs(D) @ np.abs(B.astype(np.float64))) + 1e-30
+        assert (np.abs(got32 - ref) <= bound).all()
+        # a row subset gives the same rows
+        rows = [R - 1, 0, R // 2]
+        sub = oracle.spmm(values, meta, colidx, R, K, V, M, B, rows=rows, acc="f64", L=L)
+        assert np.array_equal(sub, got[rows])
+    # subnormal and signed-zero operands: numpy converts fp16 exactly
+    tiny = [1023 * 2.0 ** -24, -3 * 2.0 ** -24, 2.0 ** -14, -0.0, 0.0, 1.0, -2.0]
+    A = inputs.choice_f16((8, 32), 3, 0, tiny)
+    B = inputs.choice_f16((32, 6), 3, 1, tiny)
+    values, meta, colidx = oracle.compress(A, 4, 8, L)
+    D = oracle.decompress(values, meta, colidx, 8, 32, 4, 8, L).astype(np.float64)
+    got = oracle.spmm(values, meta, colidx, 8, 32, 4, 8, B, acc="f64", L=L)
+    assert np.array_equal(got, D @ B.astype(np.float64))
+
+
+def check_fig3_fixture(L):
+    """VENOM Figure 3: ascending m-index pairs and column-loc decompress to
+    exactly 2 non-zeros per (row, block), inside the block's column-loc."""
+    f3 = read_fixture(os.path.join(GOLDEN, "venom_fig3.txt"))
+    R, K, V, M = (int(f3[k]) for k in ("R", "K", "V", "M"))
+    midx = [int(x) for x in f3["m_indices"].split()]
+    cl = np.array([int(x) for x in f3["column_loc"].split()], dtype=np.uint8).reshape(R // V, K // M, 4)
+    vpr = 2 * (K // M)
+    meta = np.zeros((R, (vpr + 3) // 4), dtype=np.uint8)
+    for r in range(R):
+        for t in range(vpr):
+            meta[r, t // 4] |= midx[r * vpr + t] << (2 * (t % 4))
+    labels = np.arange(1, R * vpr + 1, dtype=np.float16).reshape(R, vpr)  # label + 1: non-zero
+    D = oracle.decompress(labels.view(np.uint16), meta, cl, R, K, V, M, L).astype(np.float64)
+    for r in range(R):
+        for j in range(K // M):
+            blk = D[r, j * M:(j + 1) * M]
+            nz = np.nonzero(blk)[0]
+            assert len(nz) == 2
+            assert set(nz.tolist()) <= set(cl[r // V, j].tolist())
+            # row-major order: the two labels of a block increase left to right
+            assert blk[nz[0]] < blk[nz[1]]
+    for pair in zip(midx[0::2], midx[1::2]):
+        assert pair[0] < pair[1]
+    assert (np.diff(cl.astype(np.int64), axis=2) > 0).all()
+
+
+PINS = [check_worked_example, check_worked_local_index, check_worked_product,
+        check_storage_arithmetic, check_brute_force_ties, check_brute_force_subnormals,
+        check_brute_force_normal, check_invariants_and_round_trip, check_spmm_against_numpy,
+        check_fig3_fixture]
+
+
+# ----------------------------------------------------------------------------
+# tests
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("pin", PINS, ids=lambda f: f.__name__)
+def test_pin(pin):
+    pin(oracle.lib())
+
+
+def test_nonfinite_rejected():
+    L = oracle.lib()
+    for bad in (np.inf, -np.inf, np.nan):
+        W = inputs.normal_f16((8, 16), 1, 0, 0.02)
+        W[3, 5] = bad
+        with pytest.raises(oracle.OracleError) as e:
+            oracle.compress(W, 4, 8, L)
+        assert e.value.code == oracle.NONFINITE
+
+
+@pytest.mark.parametrize("R,K,V,M", [(10, 16, 4, 8), (8, 18, 4, 8), (8, 16, 4, 3), (8, 512, 4, 257),
+                                     (8192, 16, 8192, 8), (8, 16, 0, 8)])
+def test_invalid_shapes(R, K, V, M):
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.sizes(R, K, V, M)
+    assert e.value.code == oracle.INVALID
+
+
+def test_empty_inputs():
+    L = oracle.lib()
+    assert oracle.sizes(0, 64, 16, 8, L) == (0, 0, 0)
+    v, m, c = oracle.compress(np.zeros((0, 64), dtype=np.float16), 16, 8, L)
+    assert v.shape == (0, 16) and m.shape == (0, 4) and c.shape == (0, 8, 4)
+    v, m, c = oracle.compress(np.zeros((16, 0), dtype=np.float16), 16, 8, L)
+    assert v.shape == (16, 0) and c.shape == (1, 0, 4)
+    C = oracle.spmm(v, m, c, 16, 0, 16, 8, np.zeros((0, 5), dtype=np.float16), L=L)
+    assert C.shape == (16, 5) and not C.any()
+
+
+def test_generator_matches_its_definition():
+    """The shared input generator against a scalar restatement of SplitMix64."""
+    mask = (1 << 64) - 1
+
+    def mix(z):
+        z ^= z >> 30
+        z = (z * 0xBF58476D1CE4E5B9) & mask
+        z ^= z >> 27
+        z = (z * 0x94D049BB133111EB) & mask
+        return z ^ (z >> 31)
+
+    seed, stream = 1002, 3
+    key = mix((seed * 0x9E3779B97F4A7C15) & mask) ^ mix(((stream + 1) * 0xD1B54A32D192ED03) & mask)
+    want = [mix((key + (i + 1) * 0x9E3779B97F4A7C15) & mask) for i in range(8)]
+    assert inputs.raw_u64(seed, stream, 0, 8).tolist() == want
+    assert inputs.raw_u64(seed, stream, 5, 3).tolist() == want[5:]
+    x = inputs.normal_f16((1 << 16,), 1, 0, 0.02).astype(np.float64)
+    assert abs(x.mean()) < 3e-4 and abs(x.std() - 0.02) < 3e-4
+    # any chunk boundary gives the same stream
+    big = inputs.normal_range(0, 1000, 9, 2)
+    assert np.array_equal(inputs.normal_range(400, 1000, 9, 2), big[400:])
+
+
+# planted mistakes: (description, regex on the oracle source, replacement)
+MUTANTS = [
+    ("ties go to the higher index", r"score\[c\] > score\[best\]", "score[c] >= score[best]"),
+    ("keep the smallest instead of the largest", r"score\[c\] > score\[best\]", "score[c] < score[best]"),
+    ("m-index fields packed MSB first", r"\(uint8_t\)\(slot << \(2 \* \(t % 4\)\)\)",
+     "(uint8_t)(slot << (2 * (3 - t % 4)))"),
+    ("column-loc not sorted", r"out\[b - 1\] > out\[b\]", "0"),
+    ("signed instead of absolute column sums", r"s \+= fabs\(half_to_double", "s += (half_to_double"),
+    ("column-loc slot reversed on decompress", r"colidx\[\(i \* nblk \+ j\) \* 4 \+ slot\]",
+     "colidx[(i * nblk + j) * 4 + (3 - slot)]"),
+    ("SpMM drops the last k", r"for \(int64_t k = 0; k < K; \+\+k\) \{\n                const double ak",
+     "for (int64_t k = 0; k < K - 1; ++k) {\n                const double ak"),
+    ("subnormal scale off by one", r"ldexp\(\(double\)f, -24\)", "ldexp((double)f, -25)"),
+    ("values taken from the unselected column", r"W\[row \* ld_w \+ j \* M \+ sel\[keep\[t\]\]\]",
+     "W[row * ld_w + j * M + keep[t]]"),
+]
+
+
+def test_mutants_are_caught(tmp_path):
+    """Every planted mistake in a copy of the oracle fails at least one pin."""
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = open(os.path.join(os.path.dirname(oracle.__file__), "vnm_oracle.c")).read()
+    for k, (what, pat, rep) in enumerate(MUTANTS):
+        new, n = re.subn(pat, rep, src, count=1)
+        assert n == 1, f"mutant pattern not found: {what}"
+        path = tmp_path / f"mutant{k}.c"
+        path.write_text(new)
+        so = str(tmp_path / f"libmutant{k}.so")
+        oracle.build(str(path), so)
+        L = oracle.load_from(so)
+        failed = []
+        for pin in PINS:
+            try:
+                pin(L)
+            except (AssertionError, oracle.OracleError, IndexError, ValueError):
+                failed.append(pin.__name__)
+        assert failed, f"no pin caught the planted mistake: {what}"
