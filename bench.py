@@ -1,0 +1,465 @@
+#!/usr/bin/env python3
+"""Benchmark of the V:N:M hot path on GB300: magnitude prune-and-encode of a
+dense fp16 weight matrix (vnm_compress) followed by the SpMM C = A_vnm . B
+(vnm_spmm), through libvnm's C ABI.
+
+One step = one pass of the whole path over one batch of synthetic input:
+vnm_compress(W) then vnm_spmm(B) -> C, for the square compute-bound workload
+(A 4096 x 4096, V = 64, 2:8, B 4096 x 2048, fp16 C; --workload/--case pick
+another). Inputs are resident in HBM when the timed region starts; the steps
+rotate over enough distinct input/output sets that each set is evicted from
+L2 before it is used again. The K timed steps are captured once in a CUDA
+graph (with an event node around every kernel) and replayed.
+
+Output: one JSON line (rank 0). ``value`` is the dense-equivalent TFLOP/s of
+the whole step (2*R*N*K per step over the step time); ``e2e`` is the same
+metric through the public API with host buffers, copies included; the
+``roofline`` object covers the kernel that takes most of the step.
+
+``--impl reference`` times the CPU oracle (the only other implementation of
+this path here) on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "V:N:M SpMM TFLOP/s (dense-equiv & effective), % of sparse-TC/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["vnm", "reference"], default="vnm")
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--case", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target seconds of oracle work")
+    ap.add_argument("--clock-seconds", type=float, default=2.0, help="seconds of load around the timed region")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+
+
+def dist_max(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(world, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# --------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.gpu)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.rows.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = [p for (t, p) in self.rows if t0 <= t <= t1] or [p for (_, p) in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in rows if num(p[1]) is not None]
+        smax = [num(p[2]) for p in rows if num(p[2]) is not None]
+        reasons = set()
+        for p in rows:
+            for name, val in (("hw_slowdown", p[5]), ("hw_thermal_slowdown", p[6]), ("sw_thermal_slowdown", p[7]),
+                              ("sw_power_cap", p[8])):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        power = [num(p[3]) for p in rows if num(p[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(power) if power else None}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def time_oracle(case, seconds: float):
+    """Time the CPU oracle (compress + fp32-accumulate SpMM, as it stands) on
+    the first S V-block rows of the workload, S chosen for ~``seconds``."""
+    import numpy as np
+
+    import oracle
+    from structured_sparse_matmul_gb300 import inputs, workloads
+
+    V = case.V
+    # one V-block row first, to size the sample
+    def one(rows):
+        W = inputs.normal_f16((rows, case.K), case.seed, case.a_stream, workloads.A_SIGMA)
+        B = inputs.normal_f16((case.K, case.N), case.seed, case.b_stream, workloads.B_SIGMA)
+        t0 = time.perf_counter()
+        values, meta, colidx = oracle.compress(W, V, case.M)
+        oracle.spmm(values, meta, colidx, rows, case.K, V, case.M, B)
+        return time.perf_counter() - t0
+
+    rows = V
+    t1 = one(rows)
+    blocks = max(1, min(case.R // V, int(seconds / max(t1, 1e-6))))
+    rows = blocks * V
+    t = one(rows) if blocks > 1 else t1
+    flops = 2.0 * rows * case.N * case.K
+    return {"value": flops / t / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"compress + fp32 SpMM of rows 0..{rows - 1} ({blocks} of {case.R // V} V-block rows) of "
+                      f"{case.R}x{case.K}x{case.N}, {t:.2f} s single-threaded",
+            "seconds": t}
+
+
+# --------------------------------------------------------------------------- reference arm
+
+def run_reference(args, case):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cb = time_oracle(case, args.cpu_seconds)
+    step_s = cb["seconds"]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": config_of(case, None),
+        "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
+        "e2e": {"value": cb["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "note": "one bounded oracle sample per run (the oracle is a deliberately slow checker)",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(case, l2_note):
+    c = {"workload": (f"V:N:M magnitude compress + SpMM, A {case.R}x{case.K} fp16 N(0,0.02) {case.V}:2:{case.M} "
+                      f"({100 * (1 - 2 / case.M):.1f}% sparse), B {case.K}x{case.N} fp16 N(0,1), "
+                      f"{'fp32' if case.c_f32 else 'fp16'} C, fp32 accumulate"),
+         "R": case.R, "K": case.K, "N": case.N, "V": case.V, "M": case.M,
+         "c_dtype": "f32" if case.c_f32 else "f16"}
+    if l2_note:
+        c["l2"] = l2_note
+    return c
+
+
+# --------------------------------------------------------------------------- main arm
+
+def main():
+    args = parse_args()
+    from structured_sparse_matmul_gb300 import workloads
+    case = workloads.workload_cases(args.workload)[args.case]
+    if args.impl == "reference":
+        world, _, _ = dist_env()
+        dist_init(world, "gloo")
+        run_reference(args, case)
+        return
+
+    import numpy as np
+    import torch
+
+    from structured_sparse_matmul_gb300 import inputs, vnm
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    vnm.lib()  # fails loudly if libvnm is not built
+
+    peaks, peak_src = load_peaks()
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+
+    R, K, N, V, M = case.R, case.K, case.N, case.V, case.M
+    c_dtype = torch.float32 if case.c_f32 else torch.float16
+    W_h = inputs.normal_f16((R, K), case.seed, case.a_stream, workloads.A_SIGMA)
+    B_h = inputs.normal_f16((K, N), case.seed, case.b_stream, workloads.B_SIGMA)
+    vb, mb, cb = vnm.vnm_sizes(R, K, V, M)
+    c_bytes = R * N * (4 if case.c_f32 else 2)
+    set_bytes = 2 * R * K + 2 * K * N + c_bytes + vb + mb + cb
+    n_sets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+
+    W0 = torch.from_numpy(W_h).to(dev)
+    B0 = torch.from_numpy(B_h).to(dev)
+    sets = []
+    for _ in range(n_sets):
+        A = vnm.vnm_matrix_alloc(R, K, V, M, dev)
+        sets.append({"A": A, "W": W0.clone(), "B": B0.clone(), "C": torch.empty((R, N), dtype=c_dtype, device=dev),
+                     "ws": vnm.workspace_for(A, N, dev)})
+    del W0, B0
+    plan = vnm.vnm_spmm_plan_query(sets[0]["A"], sets[0]["B"], c_dtype,
+                                   0 if sets[0]["ws"] is None else sets[0]["ws"].numel() * 4)
+    splits = plan.splits if plan.path == vnm.VNM_PATH_TC else 1
+    kernels_per_step = 1 + (1 if plan.path != vnm.VNM_PATH_NONE else 0) + (1 if splits > 1 else 0)
+
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        s = sets[i % n_sets]
+        if ev is not None:
+            ev[0].record(stream)
+        vnm.vnm_compress(s["A"], s["W"], stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        vnm.vnm_spmm(s["A"], s["B"], s["C"], workspace=s["ws"], stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    # warm-up (eager), then check the status words
+    for i in range(max(args.warmup, 1)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    for s in sets:
+        st = vnm.vnm_get_status(s["A"])
+        if st != vnm.VNM_OK:
+            raise RuntimeError(f"kernel status {vnm.status_string(st)} during warm-up")
+
+    # capture the K timed steps (with event nodes) in one CUDA graph
+    steps = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    graph = torch.cuda.CUDAGraph()
+    cap_stream = torch.cuda.Stream(dev)
+    cap_stream.wait_stream(stream)
+    with torch.cuda.stream(cap_stream):
+        stream = cap_stream
+        with torch.cuda.graph(graph, stream=cap_stream):
+            for i in range(steps):
+                step(i, evs[i])
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    graph.replay()  # warm replay
+    torch.cuda.synchronize(dev)
+
+    # clocks: sample across a load phase that brackets the timed replay
+    sampler = ClockSampler(local)
+    sampler.start()
+    t_load0 = time.time()
+    reps = 0
+    while time.time() - t_load0 < args.clock_seconds / 2:
+        graph.replay()
+        torch.cuda.synchronize(dev)
+        reps += 1
+    g0 = torch.cuda.Event(enable_timing=True)
+    g1 = torch.cuda.Event(enable_timing=True)
+    dist_barrier(world, dev)
+    torch.cuda.synchronize(dev)
+    t_timed0 = time.time()
+    g0.record(stream)
+    graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_timed1 = time.time()
+    dist_barrier(world, dev)
+    elapsed_ms = g0.elapsed_time(g1)
+    comp_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    spmm_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    t_load1 = time.time()
+    while time.time() - t_load1 < args.clock_seconds / 2:
+        graph.replay()
+        torch.cuda.synchronize(dev)
+    sampler.stop()
+    clocks = sampler.summary(t_load0, time.time())
+    for s in sets:
+        st = vnm.vnm_get_status(s["A"])
+        if st != vnm.VNM_OK:
+            raise RuntimeError(f"kernel status {vnm.status_string(st)} during the timed region")
+
+    max_ms = dist_max(elapsed_ms, world, dev)
+    dense_flops = case.dense_flops()
+    eff_flops = case.effective_flops()
+    value = dense_flops * steps * world / (max_ms * 1e-3) / 1e12
+
+    # roofline of the kernel that takes most of the step
+    a_bytes = vb + mb + cb
+    spmm_bytes = a_bytes + 2 * K * N + c_bytes
+    comp_bytes = 2 * R * K + a_bytes
+    if spmm_ms >= comp_ms:
+        t_tc = eff_flops / (peaks["bf16_tflops"] * 1e12)
+        t_hbm = spmm_bytes / (peaks["hbm_gbs"] * 1e9)
+        if t_tc >= t_hbm:
+            achieved = eff_flops / (spmm_ms * 1e-3) / 1e12
+            roof = {"kernel": "vnm_spmm (tcgen05 sparse)" if plan.path == vnm.VNM_PATH_TC else "vnm_spmm (CUDA core)",
+                    "bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"],
+                    "per_launch": f"{eff_flops:.4g} effective flops (2 per kept non-zero per column of B)"}
+        else:
+            achieved = spmm_bytes / (spmm_ms * 1e-3) / 1e9
+            roof = {"kernel": "vnm_spmm", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "per_launch": f"{spmm_bytes} bytes (A values+meta+colidx, B, C once)"}
+    else:
+        achieved = comp_bytes / (comp_ms * 1e-3) / 1e9
+        roof = {"kernel": "vnm_compress", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "per_launch": f"{comp_bytes} bytes (dense W read, compressed arrays written)"}
+    roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
+    roof["traffic"] = None
+
+    # end to end: host buffers, copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        W_pin = torch.from_numpy(W_h).pin_memory()
+        B_pin = torch.from_numpy(B_h).pin_memory()
+        C_pin = torch.empty((R, N), dtype=c_dtype).pin_memory()
+        e_steps = max(3, min(steps, 50))
+        s0 = sets[0]
+        for _ in range(2):
+            s0["W"].copy_(W_pin, non_blocking=True)
+            s0["B"].copy_(B_pin, non_blocking=True)
+            vnm.vnm_compress(s0["A"], s0["W"])
+            vnm.vnm_spmm(s0["A"], s0["B"], s0["C"], workspace=s0["ws"])
+            C_pin.copy_(s0["C"], non_blocking=True)
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        dist_barrier(world, dev)
+        e0.record(stream)
+        for i in range(e_steps):
+            s = sets[i % n_sets]
+            s["W"].copy_(W_pin, non_blocking=True)
+            s["B"].copy_(B_pin, non_blocking=True)
+            vnm.vnm_compress(s["A"], s["W"])
+            vnm.vnm_spmm(s["A"], s["B"], s["C"], workspace=s["ws"])
+            C_pin.copy_(s["C"], non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = dist_max(e0.elapsed_time(e1), world, dev)
+        e2e = {"value": dense_flops * e_steps * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": int(W_h.nbytes + B_h.nbytes), "d2h_bytes_per_step": int(C_pin.numel() * C_pin.element_size()),
+               "steps": e_steps, "ms_per_step": e_ms / e_steps}
+
+    # context: dense torch.matmul on the same shape (fp16 in, fp32 accumulate)
+    ctx = {}
+    try:
+        Wd = sets[0]["W"]
+        Bd = sets[0]["B"]
+        for _ in range(3):
+            torch.matmul(Wd, Bd)
+        torch.cuda.synchronize(dev)
+        m0 = torch.cuda.Event(enable_timing=True)
+        m1 = torch.cuda.Event(enable_timing=True)
+        m0.record()
+        for _ in range(20):
+            torch.matmul(Wd, Bd)
+        m1.record()
+        torch.cuda.synchronize(dev)
+        ctx["torch_matmul_dense_tflops"] = dense_flops * 20 / (m0.elapsed_time(m1) * 1e-3) / 1e12
+    except Exception as exc:  # context only
+        ctx["torch_matmul_dense_tflops"] = f"unavailable: {exc}"
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        c = time_oracle(case, args.cpu_seconds)
+        cpu = {k: c[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": steps,
+            "warmup": args.warmup, "ms_per_step": max_ms / steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+            "config": config_of(case, f"{n_sets} rotating input/output sets of {set_bytes / 2**20:.1f} MiB "
+                                      f"(> 2x the {l2 / 2**20:.0f} MiB L2)"),
+            "effective_tflops": eff_flops * steps * world / (max_ms * 1e-3) / 1e12,
+            "kernels": {"vnm_compress_ms": comp_ms, "vnm_spmm_ms": spmm_ms,
+                        "spmm_dense_equiv_tflops": dense_flops / (spmm_ms * 1e-3) / 1e12,
+                        "spmm_effective_tflops": eff_flops / (spmm_ms * 1e-3) / 1e12,
+                        "compress_gbs": comp_bytes / (comp_ms * 1e-3) / 1e9,
+                        "plan": plan.as_dict()},
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": steps * kernels_per_step, "context": ctx,
+            "gpu": props.name, "sm_count": props.multi_processor_count,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,207 @@
+/*
+ * vnm.h - C ABI of libvnm: V:N:M structured-sparse weights on one NVIDIA
+ * GB300 GPU (sm_103a).
+ *
+ * The format is the one of "VENOM: A Vectorized N:M Format for Unleashing the
+ * Power of Sparse Tensor Cores" (Castro et al., SC'23), section 3 "The V:N:M
+ * format" (Figures 2 and 3): a dense R x K weight matrix A is cut into V x M
+ * blocks; each block keeps 4 of its M columns ("vector-wise" pruning), and
+ * every row keeps 2 of those 4 (2:4 pruning). Section 4 (Figure 4) maps the
+ * product C = A . B onto 2:4 sparse tensor cores: the 4 kept columns of each
+ * block select 4 of the M rows of B.
+ *
+ * Arrays (all row-major, caller-owned device memory, sizes from vnm_sizes):
+ *   values  fp16 [R][2K/M]          the kept weights, 2 per row and block, in
+ *                                   ascending slot order ("Non-zero values");
+ *   meta    uint8 [R][ceil(2K/M/4)] one 2-bit slot (0..3, position among the
+ *                                   block's 4 kept columns) per value; value t
+ *                                   of a row sits at bits 2*(t%4) of byte t/4
+ *                                   ("m-indices"; the 2-bit tags of the
+ *                                   lecture notes "2:4 sparsity on sparse
+ *                                   tensor cores", "The compressed format");
+ *   colidx  uint8 [R/V][K/M][4]     the 4 kept columns of each block, in-block
+ *                                   index 0..M-1, ascending ("column-loc").
+ *
+ * Conventions of every entry point:
+ *   - sizes are int64_t, element counts (leading dimensions in elements);
+ *   - pointers named W, B, C, values, meta, colidx, workspace are device
+ *     pointers on the GPU that was current when the matrix was created;
+ *   - work is enqueued on `stream` (a cudaStream_t; NULL is the legacy
+ *     default stream) and the call returns without waiting, except
+ *     vnm_get_status, which synchronises that stream;
+ *   - arguments are checked on the host before anything is enqueued; a
+ *     failed check returns an error and enqueues nothing;
+ *   - errors found by a kernel (non-finite weights, a bounded wait that ran
+ *     out) are written to the matrix's device status word and returned by
+ *     the next vnm_get_status;
+ *   - the library keeps no global state and allocates device memory only in
+ *     vnm_matrix_create (a 256-byte status block); one matrix handle may be
+ *     used by one host thread at a time.
+ */
+#ifndef VNM_H
+#define VNM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define VNM_VERSION 100 /* 1.0.0 */
+
+typedef enum vnm_status {
+    VNM_OK = 0,
+    VNM_ERR_INVALID_ARG = 1, /* a shape, pointer, alignment or handle check failed */
+    VNM_ERR_UNSUPPORTED = 2, /* a valid request that no kernel here serves */
+    VNM_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+    VNM_ERR_NONFINITE = 4,   /* the dense weights hold an Inf or NaN */
+    VNM_ERR_TIMEOUT = 5,     /* a kernel's bounded wait ran out; it returned early */
+    VNM_ERR_INTERNAL = 6     /* a kernel found an inconsistent internal state */
+} vnm_status;
+
+typedef enum vnm_dtype { VNM_F16 = 0, VNM_F32 = 1 } vnm_dtype;
+
+/* Which kernel family serves an SpMM. */
+typedef enum vnm_path {
+    VNM_PATH_NONE = 0, /* nothing to compute (an empty product) */
+    VNM_PATH_TC = 1,   /* tcgen05 2:4 sparse tensor-core MMA, TMEM accumulators */
+    VNM_PATH_SIMT = 2  /* CUDA-core kernel for small N (one warp per row) */
+} vnm_path;
+
+/* A launch plan for vnm_spmm. vnm_spmm_plan_query fills one; a caller may
+ * edit it and pass it to vnm_spmm_with_plan (tests and tuning sweeps do). */
+typedef struct vnm_spmm_plan {
+    int32_t path;      /* a vnm_path */
+    int32_t tile_m;    /* TC: rows per CTA tile = MMA M (64 or 128) */
+    int32_t tile_n;    /* TC: columns of C per CTA tile = MMA N (16..256, multiple of 16) */
+    int32_t stages;    /* TC: depth of the shared-memory pipeline */
+    int32_t splits;    /* split-K factor over the condensed K (1 = none) */
+    int32_t reserved[3];
+} vnm_spmm_plan;
+
+/* Opaque handle of one compressed matrix. It records R, K, V, M and the
+ * three array pointers; it does not own the arrays. */
+typedef struct vnm_matrix_s* vnm_matrix;
+
+/* A cudaStream_t (NULL = legacy default stream). */
+typedef struct CUstream_st* vnm_stream_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* vnm_status_string(vnm_status s);
+
+/* VNM_VERSION of the built library. */
+int32_t vnm_version(void);
+
+/*
+ * Byte sizes of the three compressed arrays of an R x K matrix (VENOM
+ * section 3: values and m-indices R x K/M*2, column-loc R/V x K/M x 4; the
+ * m-indices cost 2 bits per value as in the lecture notes' storage
+ * arithmetic). Host only; never touches the GPU.
+ * Valid shapes: R >= 0, K >= 0, 1 <= V <= 4096, 4 <= M <= 256, R % V == 0,
+ * K % M == 0 (no implicit padding). Any output pointer may be NULL.
+ * Errors: VNM_ERR_INVALID_ARG for an invalid shape.
+ */
+vnm_status vnm_sizes(int64_t R, int64_t K, int32_t V, int32_t M, size_t* values_bytes,
+                     size_t* meta_bytes, size_t* colidx_bytes);
+
+/*
+ * Create a handle for the compressed arrays of an R x K V:N:M matrix (shape
+ * rules as in vnm_sizes). values, meta and colidx must be 16-byte aligned
+ * device allocations of at least vnm_sizes' bytes (they may be NULL when
+ * that size is 0); they stay owned by the caller and must outlive the
+ * handle. The handle is bound to the current CUDA device and allocates its
+ * 256-byte device status block there (cleared to VNM_OK).
+ * Errors: VNM_ERR_INVALID_ARG (shape, NULL out, misaligned pointer),
+ *         VNM_ERR_CUDA (no device, allocation failed).
+ */
+vnm_status vnm_matrix_create(int64_t R, int64_t K, int32_t V, int32_t M, void* values, void* meta,
+                             void* colidx, vnm_matrix* out);
+
+/* Free the handle and its status block (not the arrays). NULL is a no-op.
+ * Synchronises the device first if work may still use the status block. */
+vnm_status vnm_matrix_destroy(vnm_matrix A);
+
+/*
+ * Magnitude prune-and-encode of a dense fp16 matrix W (R x K, row-major,
+ * leading dimension ld_w >= K) into the handle's values, meta and colidx
+ * (VENOM section 3, Figure 2): for each V x M block, the 4 columns of largest
+ * L1 norm over the block's V rows (computed exactly), ties to the lower
+ * column; for each row, the 2 of those 4 with the largest |w|, ties to the
+ * lower slot (the 2:4 step of the lecture notes' worked example: the row
+ * 0.9 0.1 -0.4 0.2 -0.05 0.7 0.3 -1.2 gives values 0.9 -0.4 0.7 -1.2 and
+ * slots 00 10 01 11). The result is unique and bit-exact.
+ * W must be 16-byte aligned with ld_w % 8 == 0. W is only read.
+ * Errors: VNM_ERR_INVALID_ARG (NULL/misaligned W, ld_w); kernel-detected
+ * Inf/NaN in W sets VNM_ERR_NONFINITE in the status word (outputs are then
+ * unspecified).
+ */
+vnm_status vnm_compress(vnm_matrix A, const void* W, int64_t ld_w, vnm_stream_t stream);
+
+/*
+ * Dense fp16 R x K copy of the compressed matrix into W_out (leading
+ * dimension ld_w >= K): kept positions get their stored value, pruned ones
+ * +0.0 (VENOM Figure 3 read backwards; for tests and checkpoints).
+ * W_out: 2-byte aligned device memory of at least (R-1)*ld_w + K elements.
+ * Errors: VNM_ERR_INVALID_ARG.
+ */
+vnm_status vnm_decompress(vnm_matrix A, void* W_out, int64_t ld_w, vnm_stream_t stream);
+
+/*
+ * C = A . B (VENOM section 4, Figure 4: sparse A times dense B is dense C;
+ * the column-loc of each block selects the 4 rows of B that its kept columns
+ * meet, and the m-indices select 2 of those 4 per row).
+ *   B: fp16 K x N, row-major, leading dimension ld_b >= N, 2-byte aligned;
+ *   C: R x N, row-major, leading dimension ld_c >= N, of type c_type
+ *      (VNM_F16: fp32 accumulation rounded once to fp16, round-to-nearest-
+ *      even; VNM_F32: the fp32 accumulator); C is overwritten, never read;
+ *   workspace: device scratch for split-K partial sums, at least
+ *      vnm_spmm_workspace_size bytes, 256-byte aligned; it may be NULL when
+ *      workspace_bytes is 0, and a smaller workspace only lowers the split
+ *      factor (the result stays within the same tolerance).
+ * The plan comes from vnm_spmm_plan_query. N = 0 or R = 0 is a no-op; K = 0
+ * writes zeros.
+ * Errors: VNM_ERR_INVALID_ARG (pointers, leading dimensions, c_type),
+ *         VNM_ERR_CUDA (a launch failed); kernel-detected errors go to the
+ *         status word.
+ */
+vnm_status vnm_spmm(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, void* C, int64_t ld_c,
+                    vnm_dtype c_type, void* workspace, size_t workspace_bytes, vnm_stream_t stream);
+
+/* Bytes of workspace that vnm_spmm's plan for this N wants (0 when it does
+ * not split K). Host only. Errors: VNM_ERR_INVALID_ARG. */
+vnm_status vnm_spmm_workspace_size(vnm_matrix A, int64_t N, size_t* bytes);
+
+/*
+ * The plan vnm_spmm would use for this product (host only; reads the current
+ * device's SM count). B and C alignment decide whether the tensor-core path
+ * is allowed: it needs B 16-byte aligned with ld_b % 8 == 0 and N >= 8, and
+ * a block geometry it serves (K/M % 32 == 0 and V % 128 == 0, V == 64, or
+ * M == 4); everything else takes the CUDA-core path.
+ * Errors: VNM_ERR_INVALID_ARG.
+ */
+vnm_status vnm_spmm_plan_query(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, vnm_dtype c_type,
+                               size_t workspace_bytes, vnm_spmm_plan* plan);
+
+/*
+ * vnm_spmm with an explicit plan (for example the CUDA-core path on a shape
+ * the tensor-core path would take, or another tile, depth or split).
+ * Errors: as vnm_spmm, plus VNM_ERR_UNSUPPORTED for a plan no kernel
+ * serves on this matrix (the plan is checked on the host first).
+ */
+vnm_status vnm_spmm_with_plan(vnm_matrix A, const vnm_spmm_plan* plan, const void* B, int64_t ld_b,
+                              int64_t N, void* C, int64_t ld_c, vnm_dtype c_type, void* workspace,
+                              size_t workspace_bytes, vnm_stream_t stream);
+
+/*
+ * Synchronise `stream`, then return and clear the first error any kernel
+ * of this matrix recorded since the last call (VNM_OK if none).
+ * Errors: VNM_ERR_CUDA if the synchronisation itself failed.
+ */
+vnm_status vnm_get_status(vnm_matrix A, vnm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VNM_H */

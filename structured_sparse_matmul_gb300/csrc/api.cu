@@ -1,0 +1,342 @@
+// Host side of the libvnm C ABI (include/vnm.h): argument checks, size
+// queries, launch planning, TMA descriptor encoding and kernel dispatch.
+// Every check runs before anything is enqueued; kernels report what they
+// find through the matrix's device status block.
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "vnm_internal.h"
+
+namespace vnm {
+int tc_default_stages(int tile_n);
+}
+
+namespace {
+
+using vnm::meta_pitch;
+using vnm::values_per_row;
+
+constexpr int32_t kMaxV = 4096;
+constexpr int32_t kMinM = 4;
+constexpr int32_t kMaxM = 256;
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool valid_shape(int64_t R, int64_t K, int32_t V, int32_t M) {
+    if (R < 0 || K < 0) return false;
+    if (V < 1 || V > kMaxV) return false;
+    if (M < kMinM || M > kMaxM) return false;
+    if (R % V != 0 || K % M != 0) return false;
+    if (R > (int64_t(1) << 31) || K > (int64_t(1) << 31)) return false;  // TMA coordinates are int32
+    return true;
+}
+
+bool valid_handle(vnm_matrix A) { return A != nullptr && A->magic == kVnmMagic; }
+
+vnm_status check_device(vnm_matrix A) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VNM_ERR_CUDA;
+    return dev == A->device ? VNM_OK : VNM_ERR_INVALID_ARG;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D row-major tensor: dim0 contiguous elements per row, dim1 rows,
+// row_bytes apart; box0 x box1 box.
+bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64_t dim0, uint64_t dim1,
+               uint64_t row_bytes, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
+    auto enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t gdim[2] = {dim0, dim1};
+    const cuuint64_t gstride[1] = {row_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estride[2] = {1, 1};
+    return enc(tm, dt, 2, const_cast<void*>(base), gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The tensor-core path serves: condensed K a whole number of 128-column
+// stages (K/M % 32 == 0), every 128-row tile inside one V-block row when
+// column-loc matters (M > 4 needs V % 128 == 0; M == 4 takes any V since
+// column-loc is then the identity), B rows 16-byte aligned, N >= 8.
+bool tc_geometry_ok(const vnm_matrix_s& A) {
+    if (A.K == 0 || (A.K / A.M) % 32 != 0) return false;
+    return A.M == 4 || A.V % 128 == 0;
+}
+
+bool tc_operands_ok(const void* B, int64_t ld_b, int64_t N) {
+    return N >= 8 && aligned(B, 16) && (ld_b % 8) == 0;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, size_t workspace_bytes) {
+    vnm_spmm_plan pl;
+    std::memset(&pl, 0, sizeof(pl));
+    pl.splits = 1;
+    if (A.R == 0 || N == 0 || A.K == 0) {
+        pl.path = VNM_PATH_NONE;
+        return pl;
+    }
+    if (!(tc_geometry_ok(A) && tc_operands_ok(B, ld_b, N))) {
+        pl.path = VNM_PATH_SIMT;
+        return pl;
+    }
+    pl.path = VNM_PATH_TC;
+    pl.tile_m = 128;
+    pl.tile_n = N >= 128 ? 128 : static_cast<int32_t>(ceil_div(N, 16) * 16);
+    if (pl.tile_n > 64 && pl.tile_n < 128) pl.tile_n = 128;
+    if (pl.tile_n > 32 && pl.tile_n < 64) pl.tile_n = 64;
+    if (pl.tile_n > 16 && pl.tile_n < 32) pl.tile_n = 32;
+    pl.stages = vnm::tc_default_stages(pl.tile_n);
+    // split K when the tiles alone cannot fill the GPU
+    const int64_t tiles = ceil_div(A.R, 128) * ceil_div(N, pl.tile_n);
+    const int64_t num_kt = (A.K / A.M) / 32;
+    int64_t splits = 1;
+    if (tiles < A.sm_count) splits = std::min<int64_t>(num_kt, std::max<int64_t>(1, A.sm_count / tiles));
+    const int64_t per_split = A.R * N * static_cast<int64_t>(sizeof(float));
+    if (splits > 1) splits = std::min<int64_t>(splits, static_cast<int64_t>(workspace_bytes) / per_split);
+    pl.splits = static_cast<int32_t>(std::max<int64_t>(1, splits));
+    return pl;
+}
+
+// The split the kernels will actually use (no empty split).
+int effective_splits(const vnm_matrix_s& A, int requested) {
+    const int num_kt = static_cast<int>((A.K / A.M) / 32);
+    const int req = std::max(1, std::min(requested, num_kt));
+    const int per = (num_kt + req - 1) / req;
+    return (num_kt + per - 1) / per;
+}
+
+vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void* B, int64_t ld_b, int64_t N,
+                      size_t workspace_bytes, const void* workspace) {
+    if (pl.path == VNM_PATH_SIMT) return VNM_OK;
+    if (pl.path != VNM_PATH_TC) return VNM_ERR_UNSUPPORTED;
+    if (!tc_geometry_ok(A) || !tc_operands_ok(B, ld_b, N)) return VNM_ERR_UNSUPPORTED;
+    if (pl.tile_m != 128) return VNM_ERR_UNSUPPORTED;
+    if (vnm::tc_default_stages(pl.tile_n) == 0 || pl.stages != vnm::tc_default_stages(pl.tile_n))
+        return VNM_ERR_UNSUPPORTED;
+    if (pl.splits < 1) return VNM_ERR_INVALID_ARG;
+    const int s = effective_splits(A, pl.splits);
+    if (s > 1) {
+        const size_t need = static_cast<size_t>(s) * A.R * N * sizeof(float);
+        if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)) return VNM_ERR_INVALID_ARG;
+    }
+    return VNM_OK;
+}
+
+vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_t ld_b, int64_t N, void* C,
+                    int64_t ld_c, vnm_dtype c_type, void* workspace, cudaStream_t stream) {
+    const bool c_f32 = c_type == VNM_F32;
+    cudaError_t e = cudaSuccess;
+    if (pl.path == VNM_PATH_SIMT) {
+        e = vnm::launch_spmm_simt(*A, B, ld_b, N, C, ld_c, c_f32, stream);
+    } else if (pl.path == VNM_PATH_TC) {
+        vnm::TcLaunch L;
+        std::memset(&L, 0, sizeof(L));
+        L.tile_m = pl.tile_m;
+        L.tile_n = pl.tile_n;
+        L.stages = pl.stages;
+        L.splits = effective_splits(*A, pl.splits);
+        L.gather = A->M > 4;
+        const uint64_t vpr = static_cast<uint64_t>(values_per_row(A->K, A->M));
+        const uint64_t mp = static_cast<uint64_t>(meta_pitch(A->K, A->M));
+        (void)mp;
+        bool ok = encode_2d(&L.tm_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A->values, vpr, A->R, vpr * 2, 16, 128,
+                            CU_TENSOR_MAP_SWIZZLE_32B);
+        ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, A->K, ld_b * 2, 64, L.gather ? 1 : 128,
+                             CU_TENSOR_MAP_SWIZZLE_128B);
+        if (!ok) return VNM_ERR_CUDA;
+        e = vnm::launch_spmm_tc(*A, L, N, C, ld_c, c_f32, static_cast<float*>(workspace), stream);
+    }
+    return e == cudaSuccess ? VNM_OK : VNM_ERR_CUDA;
+}
+
+vnm_status check_spmm_args(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, const void* C, int64_t ld_c,
+                           vnm_dtype c_type) {
+    if (!valid_handle(A)) return VNM_ERR_INVALID_ARG;
+    if (c_type != VNM_F16 && c_type != VNM_F32) return VNM_ERR_INVALID_ARG;
+    if (N < 0 || ld_b < std::max<int64_t>(N, 1) || ld_c < std::max<int64_t>(N, 1)) return VNM_ERR_INVALID_ARG;
+    if (N > (int64_t(1) << 31)) return VNM_ERR_INVALID_ARG;
+    const bool work = A->R > 0 && N > 0;
+    if (work && (C == nullptr || !aligned(C, c_type == VNM_F32 ? 4 : 2))) return VNM_ERR_INVALID_ARG;
+    if (work && A->K > 0 && (B == nullptr || !aligned(B, 2))) return VNM_ERR_INVALID_ARG;
+    return VNM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* vnm_status_string(vnm_status s) {
+    switch (s) {
+        case VNM_OK: return "VNM_OK";
+        case VNM_ERR_INVALID_ARG: return "VNM_ERR_INVALID_ARG";
+        case VNM_ERR_UNSUPPORTED: return "VNM_ERR_UNSUPPORTED";
+        case VNM_ERR_CUDA: return "VNM_ERR_CUDA";
+        case VNM_ERR_NONFINITE: return "VNM_ERR_NONFINITE";
+        case VNM_ERR_TIMEOUT: return "VNM_ERR_TIMEOUT";
+        case VNM_ERR_INTERNAL: return "VNM_ERR_INTERNAL";
+    }
+    return "VNM_ERR_UNKNOWN";
+}
+
+int32_t vnm_version(void) { return VNM_VERSION; }
+
+vnm_status vnm_sizes(int64_t R, int64_t K, int32_t V, int32_t M, size_t* values_bytes, size_t* meta_bytes,
+                     size_t* colidx_bytes) {
+    if (!valid_shape(R, K, V, M)) return VNM_ERR_INVALID_ARG;
+    if (values_bytes) *values_bytes = static_cast<size_t>(R * values_per_row(K, M)) * 2;
+    if (meta_bytes) *meta_bytes = static_cast<size_t>(R * meta_pitch(K, M));
+    if (colidx_bytes) *colidx_bytes = static_cast<size_t>((R / V) * (K / M) * 4);
+    return VNM_OK;
+}
+
+vnm_status vnm_matrix_create(int64_t R, int64_t K, int32_t V, int32_t M, void* values, void* meta, void* colidx,
+                             vnm_matrix* out) {
+    if (out == nullptr) return VNM_ERR_INVALID_ARG;
+    *out = nullptr;
+    size_t vb, mb, cb;
+    if (vnm_sizes(R, K, V, M, &vb, &mb, &cb) != VNM_OK) return VNM_ERR_INVALID_ARG;
+    if ((vb && (values == nullptr || !aligned(values, 16))) || (mb && (meta == nullptr || !aligned(meta, 16))) ||
+        (cb && (colidx == nullptr || !aligned(colidx, 16))))
+        return VNM_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VNM_ERR_CUDA;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return VNM_ERR_CUDA;
+    vnm_matrix A = new (std::nothrow) vnm_matrix_s;
+    if (A == nullptr) return VNM_ERR_INTERNAL;
+    A->magic = kVnmMagic;
+    A->R = R;
+    A->K = K;
+    A->V = V;
+    A->M = M;
+    A->values = values;
+    A->meta = meta;
+    A->colidx = colidx;
+    A->device = dev;
+    A->sm_count = prop.multiProcessorCount;
+    A->cc_major = prop.major;
+    A->cc_minor = prop.minor;
+    A->status = nullptr;
+    if (cudaMalloc(&A->status, kStatusBytes) != cudaSuccess || cudaMemset(A->status, 0, kStatusBytes) != cudaSuccess) {
+        if (A->status) cudaFree(A->status);
+        A->magic = 0;
+        delete A;
+        return VNM_ERR_CUDA;
+    }
+    *out = A;
+    return VNM_OK;
+}
+
+vnm_status vnm_matrix_destroy(vnm_matrix A) {
+    if (A == nullptr) return VNM_OK;
+    if (!valid_handle(A)) return VNM_ERR_INVALID_ARG;
+    A->magic = 0;
+    vnm_status st = VNM_OK;
+    if (A->status != nullptr && cudaFree(A->status) != cudaSuccess) st = VNM_ERR_CUDA;  // cudaFree synchronises
+    delete A;
+    return st;
+}
+
+vnm_status vnm_compress(vnm_matrix A, const void* W, int64_t ld_w, vnm_stream_t stream) {
+    if (!valid_handle(A)) return VNM_ERR_INVALID_ARG;
+    if (ld_w < std::max<int64_t>(A->K, 1)) return VNM_ERR_INVALID_ARG;
+    if (A->R == 0 || A->K == 0) return VNM_OK;
+    if (W == nullptr || !aligned(W, 16) || (ld_w % 8) != 0) return VNM_ERR_INVALID_ARG;
+    vnm_status st = check_device(A);
+    if (st != VNM_OK) return st;
+    return vnm::launch_compress(*A, W, ld_w, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? VNM_OK
+                                                                                                   : VNM_ERR_CUDA;
+}
+
+vnm_status vnm_decompress(vnm_matrix A, void* W_out, int64_t ld_w, vnm_stream_t stream) {
+    if (!valid_handle(A)) return VNM_ERR_INVALID_ARG;
+    if (ld_w < std::max<int64_t>(A->K, 1)) return VNM_ERR_INVALID_ARG;
+    if (A->R == 0 || A->K == 0) return VNM_OK;
+    if (W_out == nullptr || !aligned(W_out, 2)) return VNM_ERR_INVALID_ARG;
+    vnm_status st = check_device(A);
+    if (st != VNM_OK) return st;
+    return vnm::launch_decompress(*A, W_out, ld_w, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? VNM_OK
+               : VNM_ERR_CUDA;
+}
+
+vnm_status vnm_spmm_plan_query(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, vnm_dtype c_type,
+                               size_t workspace_bytes, vnm_spmm_plan* plan) {
+    if (!valid_handle(A) || plan == nullptr) return VNM_ERR_INVALID_ARG;
+    if (c_type != VNM_F16 && c_type != VNM_F32) return VNM_ERR_INVALID_ARG;
+    if (N < 0 || ld_b < std::max<int64_t>(N, 1)) return VNM_ERR_INVALID_ARG;
+    *plan = make_plan(*A, B, ld_b, N, workspace_bytes);
+    return VNM_OK;
+}
+
+vnm_status vnm_spmm_workspace_size(vnm_matrix A, int64_t N, size_t* bytes) {
+    if (!valid_handle(A) || bytes == nullptr || N < 0) return VNM_ERR_INVALID_ARG;
+    // assume a B that the tensor-core path accepts; an unlimited workspace
+    const void* aligned_b = reinterpret_cast<const void*>(uintptr_t(256));
+    vnm_spmm_plan pl = make_plan(*A, aligned_b, ((std::max<int64_t>(N, 1) + 7) / 8) * 8, N, SIZE_MAX / 2);
+    *bytes = 0;
+    if (pl.path == VNM_PATH_TC) {
+        const int s = effective_splits(*A, pl.splits);
+        if (s > 1) *bytes = static_cast<size_t>(s) * A->R * N * sizeof(float);
+    }
+    return VNM_OK;
+}
+
+vnm_status vnm_spmm_with_plan(vnm_matrix A, const vnm_spmm_plan* plan, const void* B, int64_t ld_b, int64_t N,
+                              void* C, int64_t ld_c, vnm_dtype c_type, void* workspace, size_t workspace_bytes,
+                              vnm_stream_t stream) {
+    vnm_status st = check_spmm_args(A, B, ld_b, N, C, ld_c, c_type);
+    if (st != VNM_OK) return st;
+    if (plan == nullptr) return VNM_ERR_INVALID_ARG;
+    if (A->R == 0 || N == 0) return VNM_OK;
+    st = check_device(A);
+    if (st != VNM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (A->K == 0) {
+        const size_t esz = c_type == VNM_F32 ? 4 : 2;
+        return cudaMemset2DAsync(C, ld_c * esz, 0, N * esz, A->R, s) == cudaSuccess ? VNM_OK : VNM_ERR_CUDA;
+    }
+    st = check_plan(*A, *plan, B, ld_b, N, workspace_bytes, workspace);
+    if (st != VNM_OK) return st;
+    return run_spmm(A, *plan, B, ld_b, N, C, ld_c, c_type, workspace, s);
+}
+
+vnm_status vnm_spmm(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, void* C, int64_t ld_c, vnm_dtype c_type,
+                    void* workspace, size_t workspace_bytes, vnm_stream_t stream) {
+    vnm_status st = check_spmm_args(A, B, ld_b, N, C, ld_c, c_type);
+    if (st != VNM_OK) return st;
+    if (workspace == nullptr) workspace_bytes = 0;
+    vnm_spmm_plan pl = make_plan(*A, B, ld_b, N, workspace_bytes);
+    return vnm_spmm_with_plan(A, &pl, B, ld_b, N, C, ld_c, c_type, workspace, workspace_bytes, stream);
+}
+
+vnm_status vnm_get_status(vnm_matrix A, vnm_stream_t stream) {
+    if (!valid_handle(A)) return VNM_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return VNM_ERR_CUDA;
+    int words[3] = {0, 0, 0};
+    if (cudaMemcpy(words, A->status, sizeof(words), cudaMemcpyDeviceToHost) != cudaSuccess) return VNM_ERR_CUDA;
+    if (words[kStatusCode] != 0 && cudaMemset(A->status, 0, sizeof(words)) != cudaSuccess) return VNM_ERR_CUDA;
+    return static_cast<vnm_status>(words[kStatusCode]);
+}
+
+}  // extern "C"

@@ -1,0 +1,167 @@
+// CUDA-core V:N:M SpMM for small N (decode-like products, where the weight
+// bytes dominate), and the split-K reduction used by the tensor-core path.
+//
+// VENOM section 4, Figure 4: each stored value of row r in block j meets the
+// row j*M + colidx[r/V][j][slot] of B; the 2-bit m-index picks the slot
+// among the block's 4 kept columns (lecture notes "2:4 sparsity on sparse
+// tensor cores": the tags act on the activations, selecting K/2 of K).
+// One warp owns one row of A: lanes stream the row's values, m-indices and
+// the block-row's column-loc with coalesced loads, gather the matching B
+// rows (small, cache-resident), accumulate in fp32 and reduce across lanes.
+#include <cuda_fp16.h>
+
+#include <algorithm>
+
+#include "vnm_internal.h"
+
+namespace vnm {
+namespace {
+
+constexpr int kSimtWarps = 8;
+
+struct SimtArgs {
+    const uint32_t* values;  // [R][nblk] words: the 2 fp16 values of one block
+    const uint8_t* meta;     // [R][mpitch]
+    const uint32_t* colidx;  // [R/V][nblk] words: 4 column bytes
+    const __half* B;
+    int64_t ld_b;
+    void* C;
+    int64_t ld_c;
+    int64_t R, N;
+    int V, M;
+    int64_t nblk, mpitch;
+    bool c_f32;
+};
+
+template <int NB>
+__device__ __forceinline__ void accumulate_block(const SimtArgs& p, int64_t row, int64_t j, int64_t n0,
+                                                 uint32_t vv, uint32_t code, uint32_t sel, float (&acc)[NB]) {
+    const int64_t k0 = j * p.M + ((sel >> (8u * (code & 3u))) & 0xFFu);
+    const int64_t k1 = j * p.M + ((sel >> (8u * (code >> 2))) & 0xFFu);
+    const float a0 = __half2float(__ushort_as_half(static_cast<unsigned short>(vv & 0xFFFFu)));
+    const float a1 = __half2float(__ushort_as_half(static_cast<unsigned short>(vv >> 16)));
+    const __half* b0 = p.B + k0 * p.ld_b + n0;
+    const __half* b1 = p.B + k1 * p.ld_b + n0;
+#pragma unroll
+    for (int q = 0; q < NB; ++q) {
+        if (n0 + q < p.N) {
+            acc[q] = fmaf(a0, __half2float(b0[q]), acc[q]);
+            acc[q] = fmaf(a1, __half2float(b1[q]), acc[q]);
+        }
+    }
+}
+
+template <int NB>
+__global__ void __launch_bounds__(32 * kSimtWarps) spmm_simt_kernel(const SimtArgs p) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kSimtWarps + warp;
+    if (row >= p.R) return;
+    const uint32_t* vrow = p.values + row * p.nblk;
+    const uint8_t* mrow = p.meta + row * p.mpitch;
+    const uint32_t* crow = p.colidx + (row / p.V) * p.nblk;
+    for (int64_t n0 = 0; n0 < p.N; n0 += NB) {
+        float acc[NB];
+#pragma unroll
+        for (int q = 0; q < NB; ++q) acc[q] = 0.f;
+        int64_t j = lane;
+        // four blocks per lane in flight
+        for (; j + 96 < p.nblk; j += 128) {
+            uint32_t vv[4], mb[4], sel[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t jj = j + 32 * u;
+                vv[u] = __ldg(vrow + jj);
+                mb[u] = __ldg(mrow + (jj >> 1));
+                sel[u] = __ldg(crow + jj);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int64_t jj = j + 32 * u;
+                accumulate_block<NB>(p, row, jj, n0, vv[u], (mb[u] >> (4 * (jj & 1))) & 0xFu, sel[u], acc);
+            }
+        }
+        for (; j < p.nblk; j += 32) {
+            const uint32_t vv = __ldg(vrow + j);
+            const uint32_t code = (__ldg(mrow + (j >> 1)) >> (4 * (j & 1))) & 0xFu;
+            accumulate_block<NB>(p, row, j, n0, vv, code, __ldg(crow + j), acc);
+        }
+#pragma unroll
+        for (int q = 0; q < NB; ++q) {
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc[q] += __shfl_xor_sync(0xFFFFFFFFu, acc[q], off);
+        }
+        if (lane < NB && n0 + lane < p.N) {
+            float v = acc[0];
+#pragma unroll
+            for (int q = 1; q < NB; ++q)
+                if (lane == q) v = acc[q];
+            if (p.c_f32)
+                static_cast<float*>(p.C)[row * p.ld_c + n0 + lane] = v;
+            else
+                static_cast<__half*>(p.C)[row * p.ld_c + n0 + lane] = __float2half_rn(v);
+        }
+    }
+}
+
+// C[r][n] = sum over s = 0 .. splits-1 (in order) of partial[s][r][n].
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, int64_t R, int64_t N, void* C,
+                                     int64_t ld_c, bool c_f32) {
+    const int64_t total = R * N;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < total;
+         q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = q / N, n = q % N;
+        float s = 0.f;
+        for (int z = 0; z < splits; ++z) s += __ldg(partial + z * total + q);
+        if (c_f32)
+            static_cast<float*>(C)[r * ld_c + n] = s;
+        else
+            static_cast<__half*>(C)[r * ld_c + n] = __float2half_rn(s);
+    }
+}
+
+template <int NB>
+cudaError_t launch_nb(const SimtArgs& p, cudaStream_t stream) {
+    const unsigned grid = static_cast<unsigned>((p.R + kSimtWarps - 1) / kSimtWarps);
+    spmm_simt_kernel<NB><<<grid, 32 * kSimtWarps, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
+                             int64_t ld_c, bool c_f32, cudaStream_t stream) {
+    SimtArgs p;
+    p.values = static_cast<const uint32_t*>(A.values);
+    p.meta = static_cast<const uint8_t*>(A.meta);
+    p.colidx = static_cast<const uint32_t*>(A.colidx);
+    p.B = static_cast<const __half*>(B);
+    p.ld_b = ld_b;
+    p.C = C;
+    p.ld_c = ld_c;
+    p.R = A.R;
+    p.N = N;
+    p.V = A.V;
+    p.M = A.M;
+    p.nblk = A.K / A.M;
+    p.mpitch = meta_pitch(A.K, A.M);
+    p.c_f32 = c_f32;
+    if (A.R == 0 || N == 0) return cudaSuccess;
+    if (N <= 1) return launch_nb<1>(p, stream);
+    if (N <= 2) return launch_nb<2>(p, stream);
+    if (N <= 4) return launch_nb<4>(p, stream);
+    if (N <= 8) return launch_nb<8>(p, stream);
+    return launch_nb<16>(p, stream);
+}
+
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, void* C, int64_t ld_c,
+                                 bool c_f32, cudaStream_t stream) {
+    const int64_t total = R * N;
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, 148 * 16);
+    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(partial, splits, R, N, C, ld_c,
+                                                                              c_f32);
+    return cudaGetLastError();
+}
+
+}  // namespace vnm

@@ -1,0 +1,387 @@
+// V:N:M SpMM on Blackwell's 2:4 sparse tensor cores (tcgen05.mma.sp).
+//
+// VENOM: A Vectorized N:M Format for Unleashing the Power of Sparse Tensor
+// Cores, section 4 (Figure 4): the V:N:M matrix is run on 2:4 sparse tensor
+// cores as an R x (K/M*4) operand, each block's column-loc selecting 4 of
+// its M rows of B; section 4.1 (Figures 5-8): a thread-block tile spans V
+// rows (BSr = V), column-loc is fetched ahead of the B rows it selects, and
+// the output tile is written back with wide, coalesced stores.
+//
+// GB300 design (one CTA = one 128-row x tile_n tile of C, over a range of
+// the condensed K):
+//   warp 0    TMA producer: per 128-column stage of the condensed K, four
+//             tiled loads of the A values (one per MMA k-step: 128 rows x 16
+//             values, 32B swizzle, each in its own aligned buffer) and the B
+//             rows: M == 4 -> a plain tiled load (column-loc is the
+//             identity); M > 4 -> each lane reads one block's column-loc word
+//             and issues a 4-row TMA gather of exactly the selected B rows.
+//   warp 1    TMEM owner and MMA issuer (one thread): 4 sparse MMAs of
+//             M=128, N=tile_n, K=32 per stage into an fp32 accumulator in
+//             TMEM; tcgen05.commit releases the stage.
+//   warps 2-5 during the main loop: the m-indices of their 32 rows, read
+//             from global memory and written to TMEM with tcgen05.st, one
+//             32-bit word per lane and MMA (rows i and i+8 of each 16-row
+//             group share their 16-bit halves between lanes i and i+8),
+//             each MMA's word in its own 8-column-aligned slot; after the
+//             main loop, the epilogue: TMEM ->
+//             registers (tcgen05.ld) -> fp16 (RNE) or fp32 -> global, each
+//             thread writing whole 32-byte sectors of its row; with split-K,
+//             fp32 partials to the workspace.
+// Every mbarrier wait is bounded: on time-out the CTA records
+// VNM_ERR_TIMEOUT, drains what it already issued, frees TMEM and returns.
+#include <cuda_fp16.h>
+
+#include "vnm_internal.h"
+#include "vnm_ptx.cuh"
+
+namespace vnm {
+namespace {
+
+constexpr int kTcThreads = 192;
+constexpr int kKTile = 128;        // condensed K per stage = 4 MMAs of K = 32
+constexpr int kValsPerKTile = 64;  // stored values per row per stage (128 bytes)
+constexpr int kTileM = 128;
+constexpr int kMetaSlotCols = 8;   // TMEM columns between consecutive MMAs' m-index words
+constexpr int kMetaStageCols = 4 * kMetaSlotCols;
+// m-index word of a row that lies beyond R: slots (0, 1) in all 8 groups
+constexpr uint32_t kPadMeta = 0x44444444u;
+
+struct TcArgs {
+    const uint32_t* colidx;  // [R/V][nblk] words of 4 column bytes
+    const uint8_t* meta;     // [R][mpitch] m-indices
+    void* C;
+    int64_t ld_c;
+    float* partial;          // [splits][R][N] fp32, or null
+    int64_t R, N;
+    int V, M;
+    int64_t nblk, mpitch;
+    int num_kt;              // condensed K / kKTile
+    int kt_per_split;
+    int c_f32;
+    int vec_store;           // C row starts 16-byte aligned
+    int* status;
+};
+
+__host__ __device__ constexpr int pow2_at_least(int x) {
+    int p = 32;
+    while (p < x) p *= 2;
+    return p;
+}
+
+template <int BN, int STAGES>
+struct TcCfg {
+    static constexpr int kAtoms = (BN + 63) / 64;            // 64-column swizzle atoms of B
+    static constexpr int kAStepBytes = kTileM * 32;          // one MMA's A: 128 rows x 16 values
+    static constexpr int kABytes = 4 * kAStepBytes;
+    static constexpr int kBBytes = kAtoms * kKTile * 128;    // per atom: 128 rows x 128 B
+    static constexpr int kStageTx = kABytes + kBBytes;
+    static constexpr int kTmemCols = pow2_at_least(BN + STAGES * kMetaStageCols);
+    static constexpr int kSmemBytes = STAGES * kStageTx + 1024;  // + alignment slack
+    static_assert(BN + STAGES * kMetaStageCols <= 512, "TMEM budget");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+};
+
+template <int BN, int STAGES, bool GATHER>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const TcArgs p) {
+    using Cfg = TcCfg<BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];   // TMA bytes landed
+    __shared__ __align__(8) uint64_t meta_bar[STAGES];   // m-indices written to TMEM (4 warps)
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];  // MMAs done with the stage
+    __shared__ __align__(8) uint64_t acc_bar;            // accumulator complete
+    __shared__ uint32_t tmem_slot;
+    __shared__ int abort_flag;
+
+    // B stages first: a B descriptor read stays inside this CTA's allocation
+    // even if its two strides were interpreted the other way round.
+    const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t sB0 = smem_base;
+    const uint32_t sA0 = sB0 + STAGES * Cfg::kBBytes;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * BN;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTileM;
+    const int split = blockIdx.z;
+    const int kt0 = split * p.kt_per_split;
+    const int nkt = min(p.num_kt, kt0 + p.kt_per_split) - kt0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&meta_bar[s]), 4);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        mbar_init(smem_u32(&acc_bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (threadIdx.x == 32) {
+        tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), Cfg::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem_acc = tmem_slot;        // columns [0, BN): fp32 accumulator, lane = row
+    const uint32_t tmem_e = tmem_slot + BN;     // columns [BN, BN + STAGES*32): m-index words
+    volatile int* abort = &abort_flag;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        int last_it[STAGES];
+#pragma unroll
+        for (int s = 0; s < STAGES; ++s) last_it[s] = -1;
+        const uint32_t* crow = p.colidx + (m0 / p.V) * p.nblk;
+        for (int it = 0; it < nkt; ++it) {
+            const int slot = it % STAGES;
+            const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            const int kt = kt0 + it;
+            const uint32_t fb = smem_u32(&full_bar[slot]);
+            const uint32_t sA = sA0 + slot * Cfg::kABytes;
+            const uint32_t sB = sB0 + slot * Cfg::kBBytes;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(fb, Cfg::kStageTx);
+#pragma unroll
+                for (int s = 0; s < 4; ++s)
+                    tma_load_2d(sA + s * Cfg::kAStepBytes, &tm_a, kt * kValsPerKTile + 16 * s,
+                                static_cast<int32_t>(m0), fb);
+                if (!GATHER) {
+#pragma unroll
+                    for (int a = 0; a < Cfg::kAtoms; ++a)
+                        tma_load_2d(sB + a * kKTile * 128, &tm_b, static_cast<int32_t>(n0 + 64 * a), kt * kKTile,
+                                    fb);
+                }
+                last_it[slot] = it;
+            }
+            if (GATHER) {
+                __syncwarp();
+                // 32 blocks per stage: lane l gathers the 4 selected B rows of block kt*32 + l
+                const int64_t j = static_cast<int64_t>(kt) * 32 + lane;
+                const uint32_t sel = __ldg(crow + j);
+                const int32_t rb = static_cast<int32_t>(j * p.M);
+                const int32_t r0 = rb + static_cast<int32_t>(sel & 0xFFu);
+                const int32_t r1 = rb + static_cast<int32_t>((sel >> 8) & 0xFFu);
+                const int32_t r2 = rb + static_cast<int32_t>((sel >> 16) & 0xFFu);
+                const int32_t r3 = rb + static_cast<int32_t>(sel >> 24);
+#pragma unroll
+                for (int a = 0; a < Cfg::kAtoms; ++a)
+                    tma_gather4(sB + a * kKTile * 128 + lane * 4 * 128, &tm_b, static_cast<int32_t>(n0 + 64 * a), r0,
+                                r1, r2, r3, fb);
+            }
+        }
+        if (lane == 0 && *abort) {
+            // let every copy already issued land before the CTA exits
+            for (int s = 0; s < STAGES; ++s)
+                if (last_it[s] >= 0) mbar_drain(smem_u32(&full_bar[s]), static_cast<uint32_t>(last_it[s] / STAGES) & 1u);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc_f16_f32(kTileM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/true);
+            for (int it = 0; it < nkt; ++it) {
+                const int slot = it % STAGES;
+                const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
+                if (!mbar_wait(smem_u32(&full_bar[slot]), ph, abort)) break;
+                if (!mbar_wait(smem_u32(&meta_bar[slot]), ph, abort)) break;
+                tc_fence_after_sync();
+                const uint32_t sA = sA0 + slot * Cfg::kABytes;
+                const uint32_t sB = sB0 + slot * Cfg::kBBytes;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    // A: K-major, 32B swizzle, 32-byte rows, 8-row groups 256 bytes apart
+                    const uint64_t ad = make_smem_desc(sA + s * Cfg::kAStepBytes, 16, 256, kLayoutSw32);
+                    // B: N-major, 128B swizzle; 64-column atoms kKTile*128 bytes apart (leading
+                    // dimension), 8-row groups of K 1024 bytes apart (stride dimension)
+                    const uint64_t bd =
+                        make_smem_desc(sB + s * 32 * 128, Cfg::kAtoms > 1 ? kKTile * 128 : 1024, 1024, kLayoutSw128);
+                    const uint32_t te = tmem_e + slot * kMetaStageCols + s * kMetaSlotCols;
+                    tc_mma_sp_f16(tmem_acc, ad, bd, te, idesc, (it > 0 || s > 0) ? 1u : 0u);
+                }
+                tc_commit(smem_u32(&empty_bar[slot]));
+            }
+            tc_commit(smem_u32(&acc_bar));
+            // all issued MMAs must finish before TMEM is released
+            mbar_drain(smem_u32(&acc_bar), 0);
+        }
+        __syncwarp();
+    } else {
+        const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
+        const int64_t row = m0 + 32 * q + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+        // ------------------------------------------------ m-indices -> TMEM
+        for (int it = 0; it < nkt; ++it) {
+            const int slot = it % STAGES;
+            const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            const int kt = kt0 + it;
+            uint4 w = make_uint4(kPadMeta, kPadMeta, kPadMeta, kPadMeta);
+            if (row < p.R) w = __ldg(reinterpret_cast<const uint4*>(p.meta + row * p.mpitch) + kt);
+            const uint32_t own[4] = {w.x, w.y, w.z, w.w};
+            uint32_t v[32];
+#pragma unroll
+            for (int u = 0; u < 32; ++u) v[u] = 0u;
+#pragma unroll
+            for (int s = 0; s < 4; ++s) {
+                // The sparse MMA reads the m-indices of rows i and i+8 of each
+                // 16-row group in pairs: lane i holds both rows' first 16 bits
+                // (K 0..15 of the k-step), lane i+8 both rows' last 16 bits.
+                const uint32_t mine = own[s];
+                const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 8);
+                v[s * kMetaSlotCols] = (lane & 8) ? ((other >> 16) | (mine & 0xFFFF0000u))
+                                                  : ((mine & 0xFFFFu) | (other << 16));
+            }
+            tmem_st_32x32b_x32(tmem_e + slot * kMetaStageCols + lane_addr, v);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&meta_bar[slot]));
+        }
+        // ------------------------------------------------ epilogue
+        int ok = 1;
+        if (lane == 0) ok = mbar_wait(smem_u32(&acc_bar), 0, abort) && !*abort;
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        tc_fence_after_sync();
+        if (ok) {
+#pragma unroll 1
+            for (int c = 0; c < BN; c += 16) {
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(tmem_acc + lane_addr + c, v);
+                tmem_wait_ld();
+                const int64_t col = n0 + c;
+                if (row >= p.R || col >= p.N) continue;
+                const bool full = col + 16 <= p.N;
+                if (p.partial != nullptr) {
+                    float* dst = p.partial + (static_cast<int64_t>(split) * p.R + row) * p.N + col;
+                    if (full && (p.N % 4) == 0) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            reinterpret_cast<uint4*>(dst)[u] = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                    } else {
+                        for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u] = __uint_as_float(v[u]);
+                    }
+                } else if (p.c_f32) {
+                    float* dst = static_cast<float*>(p.C) + row * p.ld_c + col;
+                    if (full && p.vec_store) {
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            reinterpret_cast<uint4*>(dst)[u] = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+                    } else {
+                        for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u] = __uint_as_float(v[u]);
+                    }
+                } else {
+                    __half* dst = static_cast<__half*>(p.C) + row * p.ld_c + col;
+                    uint32_t h[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const __half2 t = __floats2half2_rn(__uint_as_float(v[2 * u]), __uint_as_float(v[2 * u + 1]));
+                        h[u] = *reinterpret_cast<const uint32_t*>(&t);
+                    }
+                    if (full && p.vec_store) {
+                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                    } else {
+                        for (int u = 0; u < 16 && col + u < p.N; ++u)
+                            dst[u] = __float2half_rn(__uint_as_float(v[u]));
+                    }
+                }
+            }
+        }
+    }
+
+    // ---------------------------------------------------- teardown
+    tc_fence_before_sync();
+    __syncthreads();
+    if (threadIdx.x == 0 && abort_flag) record_error(p.status, VNM_ERR_TIMEOUT, 10 + blockIdx.z);
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_acc, Cfg::kTmemCols);
+    }
+}
+
+template <int BN, int STAGES, bool GATHER>
+cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, dim3 grid, cudaStream_t stream) {
+    using Cfg = TcCfg<BN, STAGES>;
+    auto kern = spmm_tc_kernel<BN, STAGES, GATHER>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kTcThreads, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_b, p);
+    return cudaGetLastError();
+}
+
+template <bool GATHER>
+cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, dim3 grid, cudaStream_t stream) {
+    switch (L.tile_n) {
+        case 16: return launch_variant<16, 6, GATHER>(L, p, grid, stream);
+        case 32: return launch_variant<32, 6, GATHER>(L, p, grid, stream);
+        case 64: return launch_variant<64, 6, GATHER>(L, p, grid, stream);
+        case 128: return launch_variant<128, 4, GATHER>(L, p, grid, stream);
+        case 256: return launch_variant<256, 2, GATHER>(L, p, grid, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+int tc_default_stages(int tile_n) {
+    switch (tile_n) {
+        case 16:
+        case 32:
+        case 64: return 6;
+        case 128: return 4;
+        case 256: return 2;
+        default: return 0;
+    }
+}
+
+int tc_smem_bytes(int tile_m, int tile_n, int stages) {
+    (void)tile_m;
+    const int atoms = (tile_n + 63) / 64;
+    return stages * (kTileM * 128 + atoms * kKTile * 128) + 1024;
+}
+
+cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, int64_t N, void* C, int64_t ld_c, bool c_f32,
+                           float* partial, cudaStream_t stream) {
+    if (L.tile_m != kTileM || L.stages != tc_default_stages(L.tile_n)) return cudaErrorInvalidValue;
+    TcArgs p;
+    p.colidx = static_cast<const uint32_t*>(A.colidx);
+    p.meta = static_cast<const uint8_t*>(A.meta);
+    p.mpitch = meta_pitch(A.K, A.M);
+    p.C = C;
+    p.ld_c = ld_c;
+    p.R = A.R;
+    p.N = N;
+    p.V = A.V;
+    p.M = A.M;
+    p.nblk = A.K / A.M;
+    p.num_kt = static_cast<int>(p.nblk / 32);
+    const int splits_req = max(1, min(L.splits, p.num_kt));
+    p.kt_per_split = (p.num_kt + splits_req - 1) / splits_req;
+    const int splits = (p.num_kt + p.kt_per_split - 1) / p.kt_per_split;
+    p.partial = splits > 1 ? partial : nullptr;
+    p.c_f32 = c_f32 ? 1 : 0;
+    const int64_t esz = c_f32 ? 4 : 2;
+    p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ld_c * esz) % 16 == 0);
+    p.status = A.status;
+    if (splits > 1 && partial == nullptr) return cudaErrorInvalidValue;
+    dim3 grid(static_cast<unsigned>((N + L.tile_n - 1) / L.tile_n), static_cast<unsigned>((A.R + kTileM - 1) / kTileM),
+              static_cast<unsigned>(splits));
+    cudaError_t e = L.gather ? dispatch_bn<true>(L, p, grid, stream) : dispatch_bn<false>(L, p, grid, stream);
+    if (e != cudaSuccess) return e;
+    if (splits > 1) return launch_splitk_reduce(partial, splits, A.R, N, C, ld_c, c_f32, stream);
+    return cudaSuccess;
+}
+
+}  // namespace vnm

@@ -1,0 +1,71 @@
+// Internal declarations shared by the host API (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/vnm.h"
+
+constexpr uint32_t kVnmMagic = 0x564E4D31u;  // "VNM1"
+constexpr int kStatusBytes = 256;
+
+// Layout of the device status block (int32 words).
+enum StatusWord : int {
+    kStatusCode = 0,     // first error recorded (0 = none)
+    kStatusWhere = 1,    // kernel-specific detail of that error
+    kStatusCount = 2,    // number of errors recorded
+};
+
+struct vnm_matrix_s {
+    uint32_t magic;
+    int64_t R, K;
+    int32_t V, M;
+    void* values;   // fp16 [R][2K/M]
+    void* meta;     // uint8 [R][ceil(2K/M/4)]
+    void* colidx;   // uint8 [R/V][K/M][4]
+    int device;
+    int sm_count;
+    int cc_major, cc_minor;
+    int* status;    // device, kStatusBytes
+};
+
+namespace vnm {
+
+inline int64_t values_per_row(int64_t K, int32_t M) { return 2 * (K / M); }
+inline int64_t meta_pitch(int64_t K, int32_t M) { return (values_per_row(K, M) + 3) / 4; }
+
+// Kernel-side error recording: keep the first code, count all.
+__device__ __forceinline__ void record_error(int* status, int code, int where) {
+    if (atomicCAS(status + kStatusCode, 0, code) == 0) status[kStatusWhere] = where;
+    atomicAdd(status + kStatusCount, 1);
+}
+
+// ---- launchers (each returns the launch's cudaError_t) ----
+
+cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, cudaStream_t stream);
+cudaError_t launch_decompress(const vnm_matrix_s& A, void* W, int64_t ld_w, cudaStream_t stream);
+
+// CUDA-core SpMM; writes C directly (fp16 or fp32).
+cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
+                             int64_t ld_c, bool c_f32, cudaStream_t stream);
+
+struct TcLaunch {
+    CUtensorMap tm_a;   // values, box {16, tile_m}: one MMA k-step, 32B swizzle
+    CUtensorMap tm_b;   // B, box {64, 128} (tile) or {64, 1} (gather4), 128B swizzle
+    int tile_m, tile_n, stages, splits;
+    bool gather;        // M > 4: rows of B selected through colidx
+};
+
+// tcgen05 sparse SpMM; with splits > 1 it writes fp32 partials to
+// `partial` ([splits][R][N]) and a second kernel reduces them into C.
+cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, int64_t N, void* C, int64_t ld_c,
+                           bool c_f32, float* partial, cudaStream_t stream);
+
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, void* C,
+                                 int64_t ld_c, bool c_f32, cudaStream_t stream);
+
+// Shared-memory bytes one TC CTA needs for a (tile_m, tile_n, stages) plan.
+int tc_smem_bytes(int tile_m, int tile_n, int stages);
+
+}  // namespace vnm

@@ -1,0 +1,249 @@
+"""Thin Python binding of libvnm's C ABI (include/vnm.h), same names.
+
+Argument marshalling only: PyTorch provides device memory and streams, and
+every step of the computation runs in libvnm's CUDA kernels. There is no CPU
+or PyTorch fallback: if libvnm.so is missing, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+from typing import Optional, Tuple
+
+import torch
+
+from . import build as _build
+
+VNM_OK = 0
+VNM_ERR_INVALID_ARG = 1
+VNM_ERR_UNSUPPORTED = 2
+VNM_ERR_CUDA = 3
+VNM_ERR_NONFINITE = 4
+VNM_ERR_TIMEOUT = 5
+VNM_ERR_INTERNAL = 6
+
+VNM_F16 = 0
+VNM_F32 = 1
+
+VNM_PATH_NONE = 0
+VNM_PATH_TC = 1
+VNM_PATH_SIMT = 2
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class VnmError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {status_string(code)} ({code})")
+        self.code = code
+
+
+class vnm_spmm_plan(ctypes.Structure):
+    _fields_ = [("path", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
+                ("stages", ctypes.c_int32), ("splits", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k in ("path", "tile_m", "tile_n", "stages", "splits")}
+
+
+def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
+    p, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_size_t
+    L.vnm_status_string.argtypes = [ctypes.c_int]
+    L.vnm_status_string.restype = ctypes.c_char_p
+    L.vnm_version.argtypes = []
+    L.vnm_version.restype = i32
+    L.vnm_sizes.argtypes = [i64, i64, i32, i32, p, p, p]
+    L.vnm_matrix_create.argtypes = [i64, i64, i32, i32, p, p, p, p]
+    L.vnm_matrix_destroy.argtypes = [p]
+    L.vnm_compress.argtypes = [p, p, i64, p]
+    L.vnm_decompress.argtypes = [p, p, i64, p]
+    L.vnm_spmm.argtypes = [p, p, i64, i64, p, i64, ctypes.c_int, p, sz, p]
+    L.vnm_spmm_workspace_size.argtypes = [p, i64, p]
+    L.vnm_spmm_plan_query.argtypes = [p, p, i64, i64, ctypes.c_int, sz, ctypes.POINTER(vnm_spmm_plan)]
+    L.vnm_spmm_with_plan.argtypes = [p, ctypes.POINTER(vnm_spmm_plan), p, i64, i64, p, i64, ctypes.c_int, p, sz, p]
+    L.vnm_get_status.argtypes = [p, p]
+    for name in ("vnm_sizes", "vnm_matrix_create", "vnm_matrix_destroy", "vnm_compress", "vnm_decompress",
+                 "vnm_spmm", "vnm_spmm_workspace_size", "vnm_spmm_plan_query", "vnm_spmm_with_plan",
+                 "vnm_get_status"):
+        getattr(L, name).restype = ctypes.c_int
+    return L
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """libvnm, loaded once. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_build.LIB_PATH):
+                raise RuntimeError(
+                    f"libvnm is not built ({_build.LIB_PATH} missing); run "
+                    "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            _lib = _declare(ctypes.CDLL(_build.LIB_PATH))
+        return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().vnm_status_string(code).decode()
+
+
+def _check(code: int, what: str) -> None:
+    if code != VNM_OK:
+        raise VnmError(code, what)
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _rowmajor(t: torch.Tensor, name: str) -> int:
+    """Leading dimension (elements) of a row-major 2-D tensor."""
+    if t.dim() != 2 or t.stride(1) != 1:
+        raise ValueError(f"{name} must be a 2-D row-major tensor (stride(1) == 1)")
+    return max(int(t.stride(0)), int(t.shape[1]), 1)
+
+
+def vnm_version() -> int:
+    return int(lib().vnm_version())
+
+
+def vnm_sizes(R: int, K: int, V: int, M: int) -> Tuple[int, int, int]:
+    """Byte sizes (values, meta, colidx) of the compressed arrays."""
+    v, m, c = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().vnm_sizes(R, K, V, M, ctypes.byref(v), ctypes.byref(m), ctypes.byref(c)), "vnm_sizes")
+    return v.value, m.value, c.value
+
+
+@dataclass
+class VnmMatrix:
+    """A handle plus the caller-owned compressed arrays it describes."""
+
+    handle: int
+    R: int
+    K: int
+    V: int
+    M: int
+    values: torch.Tensor  # fp16 [R, 2K/M]
+    meta: torch.Tensor    # uint8 [R, ceil(2K/M/4)]
+    colidx: torch.Tensor  # uint8 [R/V, K/M, 4]
+
+    def __del__(self):
+        try:
+            if self.handle:
+                vnm_matrix_destroy(self)
+        except Exception:
+            pass
+
+
+def vnm_matrix_create(R: int, K: int, V: int, M: int, values: torch.Tensor, meta: torch.Tensor,
+                      colidx: torch.Tensor) -> VnmMatrix:
+    h = ctypes.c_void_p()
+    _check(lib().vnm_matrix_create(R, K, V, M, values.data_ptr() or None, meta.data_ptr() or None,
+                                   colidx.data_ptr() or None, ctypes.byref(h)), "vnm_matrix_create")
+    return VnmMatrix(int(h.value), R, K, V, M, values, meta, colidx)
+
+
+def vnm_matrix_alloc(R: int, K: int, V: int, M: int, device=None) -> VnmMatrix:
+    """Allocate the three arrays with torch on ``device`` and create a handle."""
+    vb, mb, cb = vnm_sizes(R, K, V, M)
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    values = torch.empty((R, 2 * (K // M)), dtype=torch.float16, device=dev)
+    meta = torch.empty((R, (2 * (K // M) + 3) // 4), dtype=torch.uint8, device=dev)
+    colidx = torch.empty((R // V, K // M, 4), dtype=torch.uint8, device=dev)
+    assert values.numel() * 2 == vb and meta.numel() == mb and colidx.numel() == cb
+    with torch.cuda.device(dev):
+        return vnm_matrix_create(R, K, V, M, values, meta, colidx)
+
+
+def vnm_matrix_destroy(A: VnmMatrix) -> None:
+    h, A.handle = A.handle, 0
+    if h:
+        _check(lib().vnm_matrix_destroy(h), "vnm_matrix_destroy")
+
+
+def vnm_compress(A: VnmMatrix, W: torch.Tensor, stream=None) -> None:
+    if W.dtype != torch.float16 or not W.is_cuda or tuple(W.shape) != (A.R, A.K):
+        raise ValueError("W must be a CUDA fp16 tensor of shape (R, K)")
+    _check(lib().vnm_compress(A.handle, W.data_ptr() or None, _rowmajor(W, "W"), _stream_ptr(stream)),
+           "vnm_compress")
+
+
+def vnm_decompress(A: VnmMatrix, W_out: torch.Tensor, stream=None) -> None:
+    if W_out.dtype != torch.float16 or not W_out.is_cuda or tuple(W_out.shape) != (A.R, A.K):
+        raise ValueError("W_out must be a CUDA fp16 tensor of shape (R, K)")
+    _check(lib().vnm_decompress(A.handle, W_out.data_ptr() or None, _rowmajor(W_out, "W_out"), _stream_ptr(stream)),
+           "vnm_decompress")
+
+
+def _c_type(C: torch.Tensor) -> int:
+    if C.dtype == torch.float16:
+        return VNM_F16
+    if C.dtype == torch.float32:
+        return VNM_F32
+    raise ValueError("C must be fp16 or fp32")
+
+
+def _spmm_operands(A: VnmMatrix, B: torch.Tensor, C: torch.Tensor):
+    if B.dtype != torch.float16 or not B.is_cuda or B.dim() != 2 or B.shape[0] != A.K:
+        raise ValueError("B must be a CUDA fp16 tensor of shape (K, N)")
+    N = int(B.shape[1])
+    if not C.is_cuda or tuple(C.shape) != (A.R, N):
+        raise ValueError("C must be a CUDA tensor of shape (R, N)")
+    return N, _rowmajor(B, "B"), _rowmajor(C, "C"), _c_type(C)
+
+
+def vnm_spmm_workspace_size(A: VnmMatrix, N: int) -> int:
+    b = ctypes.c_size_t()
+    _check(lib().vnm_spmm_workspace_size(A.handle, N, ctypes.byref(b)), "vnm_spmm_workspace_size")
+    return b.value
+
+
+def vnm_spmm_plan_query(A: VnmMatrix, B: torch.Tensor, c_dtype=torch.float16, workspace_bytes: int = 0
+                        ) -> vnm_spmm_plan:
+    plan = vnm_spmm_plan()
+    N = int(B.shape[1])
+    ct = VNM_F16 if c_dtype == torch.float16 else VNM_F32
+    _check(lib().vnm_spmm_plan_query(A.handle, B.data_ptr() or None, _rowmajor(B, "B"), N, ct, workspace_bytes,
+                                     ctypes.byref(plan)), "vnm_spmm_plan_query")
+    return plan
+
+
+def vnm_spmm(A: VnmMatrix, B: torch.Tensor, C: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+             stream=None) -> None:
+    """C = A . B on ``stream`` (default: torch's current stream)."""
+    N, ld_b, ld_c, ct = _spmm_operands(A, B, C)
+    wp = workspace.data_ptr() if workspace is not None and workspace.numel() else None
+    wb = workspace.numel() * workspace.element_size() if wp else 0
+    _check(lib().vnm_spmm(A.handle, B.data_ptr() or None, ld_b, N, C.data_ptr() or None, ld_c, ct, wp, wb,
+                          _stream_ptr(stream)), "vnm_spmm")
+
+
+def vnm_spmm_with_plan(A: VnmMatrix, plan: vnm_spmm_plan, B: torch.Tensor, C: torch.Tensor,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    N, ld_b, ld_c, ct = _spmm_operands(A, B, C)
+    wp = workspace.data_ptr() if workspace is not None and workspace.numel() else None
+    wb = workspace.numel() * workspace.element_size() if wp else 0
+    _check(lib().vnm_spmm_with_plan(A.handle, ctypes.byref(plan), B.data_ptr() or None, ld_b, N,
+                                    C.data_ptr() or None, ld_c, ct, wp, wb, _stream_ptr(stream)),
+           "vnm_spmm_with_plan")
+
+
+def vnm_get_status(A: VnmMatrix, stream=None) -> int:
+    """Synchronise the stream and return (and clear) the kernels' first error code."""
+    return int(lib().vnm_get_status(A.handle, _stream_ptr(stream)))
+
+
+def workspace_for(A: VnmMatrix, N: int, device=None) -> Optional[torch.Tensor]:
+    """A torch-allocated workspace of the size vnm_spmm's plan wants (None if 0)."""
+    nbytes = vnm_spmm_workspace_size(A, N)
+    if nbytes == 0:
+        return None
+    dev = device if device is not None else A.values.device
+    return torch.empty(nbytes // 4 + 64, dtype=torch.float32, device=dev)

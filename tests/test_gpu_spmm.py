@@ -1,0 +1,160 @@
+"""vnm_spmm on the GPU against the CPU oracle: C within 1e-2 * (1 + |C_oracle|)
+(fp16 inputs, fp32 accumulation; VENOM section 4, Figure 4), on the
+tensor-core path and on the CUDA-core path, with multi-tile and ragged
+shapes, split-K, both C types, and the workload shapes."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import read_fixture
+from structured_sparse_matmul_gb300 import inputs, vnm, workloads
+
+pytestmark = pytest.mark.gpu
+
+from gpu_util import (assert_compress_bitexact, check_close, device, gpu_compress, run_spmm,  # noqa: E402
+                      sample_rows, to_dev)
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _setup(R, K, N, V, M, seed=21, a_sigma=0.02):
+    W = inputs.normal_f16((R, K), seed, 0, a_sigma)
+    B = inputs.normal_f16((K, N), seed, 1, 1.0)
+    A, st = gpu_compress(W, V, M)
+    assert st == vnm.VNM_OK
+    values, meta, colidx = assert_compress_bitexact(A, W, V, M)
+    return A, B, (values, meta, colidx)
+
+
+def _ref(comp, R, K, V, M, B, rows=None):
+    values, meta, colidx = comp
+    return oracle.spmm(values, meta, colidx, R, K, V, M, B, rows=rows)
+
+
+def test_worked_example_product():
+    """Row 0 of the 2 x 8 worked example times B = 0.9*b0 - 0.4*b2 + 0.7*b5 - 1.2*b7."""
+    fx = read_fixture(os.path.join(GOLDEN, "worked_2x8.txt"))
+    W = np.array([[float(x) for x in fx["dense_row0"].split()], [float(x) for x in fx["dense_row1"].split()]],
+                 dtype=np.float16)
+    B = np.zeros((8, 3), dtype=np.float16)
+    B[:, 0] = np.arange(1, 9)
+    B[:, 1] = [0.5, -2, 3, 0.25, 7, -1, 1.5, 4]
+    B[:, 2] = 1
+    A, st = gpu_compress(W, 1, 4)
+    got, _ = run_spmm(A, B, torch.float32)
+    f = lambda x: float(np.float16(x))  # noqa: E731
+    want0 = [f(0.9) * float(B[0, n]) + f(-0.4) * float(B[2, n]) + f(0.7) * float(B[5, n]) + f(-1.2) * float(B[7, n])
+             for n in range(3)]
+    assert np.allclose(got[0], want0, rtol=1e-6, atol=1e-6)
+
+
+TC_SHAPES = [
+    # R, K, N, V, M
+    (384, 512, 64, 128, 4),
+    (384, 512, 128, 128, 4),
+    (256, 1024, 200, 128, 8),
+    (384, 1536, 256, 128, 8),
+    (256, 2048, 48, 128, 16),
+    (128, 4096, 16, 128, 32),
+    (272, 256, 72, 16, 4),     # ragged rows (R % 128 != 0), plain 2:4
+    (256, 1024, 24, 256, 8),   # V = 256: two tiles per block row
+    (128, 512, 8, 128, 4),     # N = 8: one MMA of N = 16 with zero-filled columns
+]
+
+
+@pytest.mark.parametrize("R,K,N,V,M", TC_SHAPES)
+@pytest.mark.parametrize("c_dtype", [torch.float16, torch.float32], ids=["f16", "f32"])
+def test_tensor_core_path(R, K, N, V, M, c_dtype):
+    A, B, comp = _setup(R, K, N, V, M)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B), c_dtype)
+    assert plan.path == vnm.VNM_PATH_TC, plan.as_dict()
+    got, _ = run_spmm(A, B, c_dtype)
+    check_close(got, _ref(comp, R, K, V, M, B), f"tc {R}x{K}x{N} {V}:2:{M}")
+
+
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 256])
+def test_tensor_core_tiles(tile_n):
+    R, K, N, V, M = 256, 1024, 300, 128, 8
+    A, B, comp = _setup(R, K, N, V, M, seed=22)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    plan.tile_n = tile_n
+    plan.stages = {16: 6, 32: 6, 64: 6, 128: 4, 256: 2}[tile_n]
+    plan.splits = 1
+    got, _ = run_spmm(A, B, plan=plan)
+    check_close(got, _ref(comp, R, K, V, M, B), f"tile_n {tile_n}")
+
+
+@pytest.mark.parametrize("splits", [2, 3, 5])
+def test_tensor_core_split_k(splits):
+    R, K, N, V, M = 256, 2560, 40, 128, 4
+    A, B, comp = _setup(R, K, N, V, M, seed=23)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    assert plan.path == vnm.VNM_PATH_TC
+    plan.splits = splits
+    for c_dtype in (torch.float16, torch.float32):
+        got, _ = run_spmm(A, B, c_dtype, plan=plan)
+        check_close(got, _ref(comp, R, K, V, M, B), f"splits {splits}")
+
+
+@pytest.mark.parametrize("R,K,N,V,M", [(256, 1024, 200, 128, 8), (272, 256, 72, 16, 4), (96, 600, 33, 8, 5),
+                                       (128, 512, 40, 64, 8), (64, 4096, 17, 64, 4)])
+def test_cuda_core_path(R, K, N, V, M):
+    A, B, comp = _setup(R, K, N, V, M, seed=24)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    plan.path = vnm.VNM_PATH_SIMT
+    for c_dtype in (torch.float16, torch.float32):
+        got, _ = run_spmm(A, B, c_dtype, plan=plan)
+        check_close(got, _ref(comp, R, K, V, M, B), f"simt {R}x{K}x{N}")
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 5, 7])
+def test_small_n(N):
+    R, K, V, M = 256, 2048, 64, 8
+    A, B, comp = _setup(R, K, N, V, M, seed=25)
+    got, _ = run_spmm(A, B)
+    check_close(got, _ref(comp, R, K, V, M, B), f"N={N}")
+
+
+def test_unaligned_and_strided_operands():
+    R, K, N, V, M = 256, 1024, 37, 128, 8
+    A, B, comp = _setup(R, K, N, V, M, seed=26)
+    ref = _ref(comp, R, K, V, M, B)
+    got, _ = run_spmm(A, B, ld_b=N)            # ld_b % 8 != 0: CUDA-core path
+    check_close(got, ref, "ld_b = N")
+    got, _ = run_spmm(A, B, ld_b=48, ld_c=41)  # aligned B, padded C rows
+    check_close(got, ref, "ld_b = 48, ld_c = 41")
+
+
+def test_empty_products():
+    R, K, V, M = 128, 512, 128, 4
+    A, B, comp = _setup(R, K, 8, V, M)
+    C = torch.full((R, 0), 1.0, dtype=torch.float16, device=device())
+    vnm.vnm_spmm(A, torch.zeros((K, 0), dtype=torch.float16, device=device()), C)
+    Z = vnm.vnm_matrix_alloc(64, 0, 16, 8, device())
+    C = torch.full((64, 5), 7.0, dtype=torch.float32, device=device())
+    vnm.vnm_spmm(Z, torch.zeros((0, 5), dtype=torch.float16, device=device()), C)
+    assert vnm.vnm_get_status(Z) == vnm.VNM_OK
+    assert not C.any().item()
+
+
+def _workload_case(case: workloads.Case, max_rows: int):
+    W = inputs.normal_f16((case.R, case.K), case.seed, case.a_stream, workloads.A_SIGMA)
+    B = inputs.normal_f16((case.K, case.N), case.seed, case.b_stream, workloads.B_SIGMA)
+    A, st = gpu_compress(W, case.V, case.M)
+    assert st == vnm.VNM_OK
+    comp = assert_compress_bitexact(A, W, case.V, case.M)
+    c_dtype = torch.float32 if case.c_f32 else torch.float16
+    got, Bd = run_spmm(A, B, c_dtype)
+    rows = None if case.R <= max_rows else sample_rows(case.R, case.V, max_rows // 2)
+    ref = _ref(comp, case.R, case.K, case.V, case.M, B, rows=rows)
+    check_close(got if rows is None else got[rows], ref, case.name)
+    return A, Bd
+
+
+@pytest.mark.parametrize("case", [c for w in (1, 2, 3, 4) for c in workloads.workload_cases(w)],
+                         ids=lambda c: c.name)
+def test_workloads(case):
+    _workload_case(case, max_rows=256 if case.N >= 2048 else 1024)
