@@ -51,6 +51,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target seconds of oracle work")
     ap.add_argument("--clock-seconds", type=float, default=2.0, help="seconds of load around the timed region")
+    ap.add_argument("--no-context", action="store_true", help="skip the dense torch.matmul context timing")
     return ap.parse_args()
 
 
@@ -302,7 +303,10 @@ def main():
 
     # capture the K timed steps (with event nodes) in one CUDA graph
     steps = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    try:  # event record nodes inside the graph (external events)
+        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] for _ in range(steps)]
+    except TypeError:
+        evs = None
     graph = torch.cuda.CUDAGraph()
     cap_stream = torch.cuda.Stream(dev)
     cap_stream.wait_stream(stream)
@@ -310,7 +314,7 @@ def main():
         stream = cap_stream
         with torch.cuda.graph(graph, stream=cap_stream):
             for i in range(steps):
-                step(i, evs[i])
+                step(i, evs[i] if evs is not None else None)
     stream = torch.cuda.current_stream(dev)
     torch.cuda.synchronize(dev)
     graph.replay()  # warm replay
@@ -337,8 +341,16 @@ def main():
     t_timed1 = time.time()
     dist_barrier(world, dev)
     elapsed_ms = g0.elapsed_time(g1)
-    comp_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
-    spmm_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    if evs is not None:
+        comp_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+        spmm_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    else:  # per-kernel events on an eager replay of the same steps
+        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+        for i in range(steps):
+            step(i, ev2[i])
+        torch.cuda.synchronize(dev)
+        comp_ms = sum(e[0].elapsed_time(e[1]) for e in ev2) / steps
+        spmm_ms = sum(e[1].elapsed_time(e[2]) for e in ev2) / steps
     t_load1 = time.time()
     while time.time() - t_load1 < args.clock_seconds / 2:
         graph.replay()
@@ -417,6 +429,8 @@ def main():
     # context: dense torch.matmul on the same shape (fp16 in, fp32 accumulate)
     ctx = {}
     try:
+        if args.no_context:
+            raise RuntimeError("skipped (--no-context)")
         Wd = sets[0]["W"]
         Bd = sets[0]["B"]
         for _ in range(3):

@@ -73,9 +73,10 @@ typedef enum vnm_path {
  * edit it and pass it to vnm_spmm_with_plan (tests and tuning sweeps do). */
 typedef struct vnm_spmm_plan {
     int32_t path;      /* a vnm_path */
-    int32_t tile_m;    /* TC: rows per CTA tile = MMA M (64 or 128) */
+    int32_t tile_m;    /* TC: rows per CTA tile = MMA M (128; 64 when column-loc changes every 64 rows) */
     int32_t tile_n;    /* TC: columns of C per CTA tile = MMA N (16..256, multiple of 16) */
-    int32_t stages;    /* TC: depth of the shared-memory pipeline */
+    int32_t stages;    /* TC: depth of the shared-memory pipeline (one depth is built per tile;
+                          0 in a plan passed to vnm_spmm_with_plan means that depth) */
     int32_t splits;    /* split-K factor over the condensed K (1 = none) */
     int32_t reserved[3];
 } vnm_spmm_plan;
@@ -176,8 +177,8 @@ vnm_status vnm_spmm_workspace_size(vnm_matrix A, int64_t N, size_t* bytes);
  * The plan vnm_spmm would use for this product (host only; reads the current
  * device's SM count). B and C alignment decide whether the tensor-core path
  * is allowed: it needs B 16-byte aligned with ld_b % 8 == 0 and N >= 8, and
- * a block geometry it serves (K/M % 32 == 0 and V % 128 == 0, V == 64, or
- * M == 4); everything else takes the CUDA-core path.
+ * a block geometry it serves (K/M % 32 == 0, and V % 64 == 0 or M == 4);
+ * everything else takes the CUDA-core path.
  * Errors: VNM_ERR_INVALID_ARG.
  */
 vnm_status vnm_spmm_plan_query(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, vnm_dtype c_type,

@@ -12,10 +12,6 @@
 
 #include "vnm_internal.h"
 
-namespace vnm {
-int tc_default_stages(int tile_n);
-}
-
 namespace {
 
 using vnm::meta_pitch;
@@ -73,12 +69,19 @@ bool encode_2d(CUtensorMap* tm, CUtensorMapDataType dt, const void* base, uint64
 }
 
 // The tensor-core path serves: condensed K a whole number of 128-column
-// stages (K/M % 32 == 0), every 128-row tile inside one V-block row when
-// column-loc matters (M > 4 needs V % 128 == 0; M == 4 takes any V since
-// column-loc is then the identity), B rows 16-byte aligned, N >= 8.
+// stages (K/M % 32 == 0), every row tile inside one V-block row when
+// column-loc matters (M > 4 needs V % 64 == 0: 128-row tiles when
+// V % 128 == 0, else 64-row tiles; M == 4 takes any V since column-loc is
+// then the identity), B rows 16-byte aligned, N >= 8.
 bool tc_geometry_ok(const vnm_matrix_s& A) {
     if (A.K == 0 || (A.K / A.M) % 32 != 0) return false;
-    return A.M == 4 || A.V % 128 == 0;
+    return A.M == 4 || A.V % 64 == 0;
+}
+
+bool tc_tile_m_ok(const vnm_matrix_s& A, int tile_m) {
+    if (tile_m == 128) return A.M == 4 || A.V % 128 == 0;
+    if (tile_m == 64) return A.M == 4 || A.V % 64 == 0;
+    return false;
 }
 
 bool tc_operands_ok(const void* B, int64_t ld_b, int64_t N) {
@@ -100,14 +103,14 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
         return pl;
     }
     pl.path = VNM_PATH_TC;
-    pl.tile_m = 128;
+    pl.tile_m = tc_tile_m_ok(A, 128) ? 128 : 64;
     pl.tile_n = N >= 128 ? 128 : static_cast<int32_t>(ceil_div(N, 16) * 16);
     if (pl.tile_n > 64 && pl.tile_n < 128) pl.tile_n = 128;
     if (pl.tile_n > 32 && pl.tile_n < 64) pl.tile_n = 64;
     if (pl.tile_n > 16 && pl.tile_n < 32) pl.tile_n = 32;
-    pl.stages = vnm::tc_default_stages(pl.tile_n);
+    pl.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n);
     // split K when the tiles alone cannot fill the GPU
-    const int64_t tiles = ceil_div(A.R, 128) * ceil_div(N, pl.tile_n);
+    const int64_t tiles = ceil_div(A.R, pl.tile_m) * ceil_div(N, pl.tile_n);
     const int64_t num_kt = (A.K / A.M) / 32;
     int64_t splits = 1;
     if (tiles < A.sm_count) splits = std::min<int64_t>(num_kt, std::max<int64_t>(1, A.sm_count / tiles));
@@ -130,9 +133,9 @@ vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void
     if (pl.path == VNM_PATH_SIMT) return VNM_OK;
     if (pl.path != VNM_PATH_TC) return VNM_ERR_UNSUPPORTED;
     if (!tc_geometry_ok(A) || !tc_operands_ok(B, ld_b, N)) return VNM_ERR_UNSUPPORTED;
-    if (pl.tile_m != 128) return VNM_ERR_UNSUPPORTED;
-    if (vnm::tc_default_stages(pl.tile_n) == 0 || pl.stages != vnm::tc_default_stages(pl.tile_n))
-        return VNM_ERR_UNSUPPORTED;
+    if (!tc_tile_m_ok(A, pl.tile_m)) return VNM_ERR_UNSUPPORTED;
+    const int depth = vnm::tc_default_stages(pl.tile_m, pl.tile_n);
+    if (depth == 0 || (pl.stages != 0 && pl.stages != depth)) return VNM_ERR_UNSUPPORTED;
     if (pl.splits < 1) return VNM_ERR_INVALID_ARG;
     const int s = effective_splits(A, pl.splits);
     if (s > 1) {
@@ -153,14 +156,15 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         std::memset(&L, 0, sizeof(L));
         L.tile_m = pl.tile_m;
         L.tile_n = pl.tile_n;
-        L.stages = pl.stages;
+        L.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n);
         L.splits = effective_splits(*A, pl.splits);
         L.gather = A->M > 4;
         const uint64_t vpr = static_cast<uint64_t>(values_per_row(A->K, A->M));
         const uint64_t mp = static_cast<uint64_t>(meta_pitch(A->K, A->M));
-        (void)mp;
-        bool ok = encode_2d(&L.tm_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A->values, vpr, A->R, vpr * 2, 16, 128,
-                            CU_TENSOR_MAP_SWIZZLE_32B);
+        bool ok = encode_2d(&L.tm_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A->values, vpr, A->R, vpr * 2, 16,
+                            static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_32B);
+        ok = ok && encode_2d(&L.tm_e, CU_TENSOR_MAP_DATA_TYPE_UINT32, A->meta, mp / 4, A->R, mp, 4,
+                             static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_NONE);
         ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, A->K, ld_b * 2, 64, L.gather ? 1 : 128,
                              CU_TENSOR_MAP_SWIZZLE_128B);
         if (!ok) return VNM_ERR_CUDA;

@@ -303,9 +303,13 @@ cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, 
         p.vec_load = (reinterpret_cast<uintptr_t>(W) % 16 == 0) && (ld_w % 8 == 0) && (p.tk % 8 == 0);
         const size_t smem = tile_bytes_aligned(A.V, p.tk) + sizeof(uint64_t) * p.tk +
                             sizeof(uint32_t) * (p.tk / A.M);
-        cudaError_t e = cudaFuncSetAttribute(compress_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
+        static size_t configured = 0;  // largest dynamic shared memory size set so far
+        if (smem > 48 * 1024 && smem > configured) {
+            cudaError_t e = cudaFuncSetAttribute(compress_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 static_cast<int>(smem));
+            if (e != cudaSuccess) return e;
+            configured = smem;
+        }
         dim3 grid(static_cast<unsigned>((A.K + p.tk - 1) / p.tk), static_cast<unsigned>(A.R / A.V));
         compress_tiled_kernel<<<grid, kCompressThreads, smem, stream>>>(p);
     } else {

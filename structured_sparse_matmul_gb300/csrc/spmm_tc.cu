@@ -7,26 +7,31 @@
 // rows (BSr = V), column-loc is fetched ahead of the B rows it selects, and
 // the output tile is written back with wide, coalesced stores.
 //
-// GB300 design (one CTA = one 128-row x tile_n tile of C, over a range of
-// the condensed K):
-//   warp 0    TMA producer: per 128-column stage of the condensed K, four
-//             tiled loads of the A values (one per MMA k-step: 128 rows x 16
-//             values, 32B swizzle, each in its own aligned buffer) and the B
-//             rows: M == 4 -> a plain tiled load (column-loc is the
-//             identity); M > 4 -> each lane reads one block's column-loc word
-//             and issues a 4-row TMA gather of exactly the selected B rows.
+// GB300 design (one CTA = one tile_m x tile_n tile of C, over a range of the
+// condensed K; tile_m = 128, or 64 when V = 64 and column-loc differs per
+// 64-row block). Per 128-column stage of the condensed K (4 MMA k-steps):
+//   warp 0    TMA producer. Up front (and every kCidxChunk stages) it copies
+//             the column-loc words of its k-range into shared memory, so no
+//             global load sits on a stage's critical path. Per stage: four
+//             tiled loads of the A values (one per MMA k-step: tile_m rows x
+//             16 values, 32B swizzle, each in its own aligned buffer), one of
+//             the m-indices (tile_m rows x 16 bytes) and the B rows:
+//             M == 4 -> a plain tiled load (column-loc is the identity);
+//             M > 4 -> lane l issues the 4-row TMA gather of the B rows that
+//             block 32*stage + l selects.
+//   warps 2-5 per stage: read their rows' m-index words from shared memory,
+//             pair them the way the sparse MMA reads them (rows i and i+8 of
+//             each 16-row group share their 16-bit halves between TMEM lanes
+//             i and i+8) and write them to TMEM (tcgen05.st), each MMA's word
+//             in its own 8-column-aligned slot; after the main loop they are
+//             the epilogue: TMEM -> registers (tcgen05.ld) -> fp16 (RNE) or
+//             fp32 -> global, each thread writing whole 32-byte sectors of its
+//             row (fp32 partials to the workspace under split-K).
 //   warp 1    TMEM owner and MMA issuer (one thread): 4 sparse MMAs of
-//             M=128, N=tile_n, K=32 per stage into an fp32 accumulator in
-//             TMEM; tcgen05.commit releases the stage.
-//   warps 2-5 during the main loop: the m-indices of their 32 rows, read
-//             from global memory and written to TMEM with tcgen05.st, one
-//             32-bit word per lane and MMA (rows i and i+8 of each 16-row
-//             group share their 16-bit halves between lanes i and i+8),
-//             each MMA's word in its own 8-column-aligned slot; after the
-//             main loop, the epilogue: TMEM ->
-//             registers (tcgen05.ld) -> fp16 (RNE) or fp32 -> global, each
-//             thread writing whole 32-byte sectors of its row; with split-K,
-//             fp32 partials to the workspace.
+//             M=tile_m, N=tile_n, K=32 per stage into an fp32 accumulator in
+//             TMEM; tcgen05.commit releases the stage. With M=128 row r of
+//             the tile lives in TMEM lane r; with M=64 in lane
+//             32*(r/16) + r%16 (lanes 16..31 of each quarter stay unused).
 // Every mbarrier wait is bounded: on time-out the CTA records
 // VNM_ERR_TIMEOUT, drains what it already issued, frees TMEM and returns.
 #include <cuda_fp16.h>
@@ -40,21 +45,20 @@ namespace {
 constexpr int kTcThreads = 192;
 constexpr int kKTile = 128;        // condensed K per stage = 4 MMAs of K = 32
 constexpr int kValsPerKTile = 64;  // stored values per row per stage (128 bytes)
-constexpr int kTileM = 128;
 constexpr int kMetaSlotCols = 8;   // TMEM columns between consecutive MMAs' m-index words
 constexpr int kMetaStageCols = 4 * kMetaSlotCols;
+constexpr int kCidxChunk = 64;     // stages of column-loc words staged in shared memory at a time
 // m-index word of a row that lies beyond R: slots (0, 1) in all 8 groups
 constexpr uint32_t kPadMeta = 0x44444444u;
 
 struct TcArgs {
     const uint32_t* colidx;  // [R/V][nblk] words of 4 column bytes
-    const uint8_t* meta;     // [R][mpitch] m-indices
     void* C;
     int64_t ld_c;
     float* partial;          // [splits][R][N] fp32, or null
     int64_t R, N;
     int V, M;
-    int64_t nblk, mpitch;
+    int64_t nblk;
     int num_kt;              // condensed K / kKTile
     int kt_per_split;
     int c_f32;
@@ -68,24 +72,36 @@ __host__ __device__ constexpr int pow2_at_least(int x) {
     return p;
 }
 
-template <int BN, int STAGES>
+template <int TM, int BN>
 struct TcCfg {
     static constexpr int kAtoms = (BN + 63) / 64;            // 64-column swizzle atoms of B
-    static constexpr int kAStepBytes = kTileM * 32;          // one MMA's A: 128 rows x 16 values
+    static constexpr int kAStepBytes = TM * 32;              // one MMA's A: TM rows x 16 values
     static constexpr int kABytes = 4 * kAStepBytes;
     static constexpr int kBBytes = kAtoms * kKTile * 128;    // per atom: 128 rows x 128 B
-    static constexpr int kStageTx = kABytes + kBBytes;
-    static constexpr int kTmemCols = pow2_at_least(BN + STAGES * kMetaStageCols);
-    static constexpr int kSmemBytes = STAGES * kStageTx + 1024;  // + alignment slack
-    static_assert(BN + STAGES * kMetaStageCols <= 512, "TMEM budget");
-    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+    static constexpr int kEBytes = TM * 16;                  // 4 m-index words per row
+    static constexpr int kStageTx = kABytes + kBBytes + kEBytes;
+    static constexpr int kStages = tc_stages_for(TM, BN);
+    static constexpr int kTmemCols = pow2_at_least(BN + kStages * kMetaStageCols);
+    static constexpr int kSmemBytes = kStages * kStageTx + 1024;  // + alignment slack
+    static_assert(kStages >= 2, "pipeline depth");
+    static_assert(BN + kStages * kMetaStageCols <= 512, "TMEM budget");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
+    static_assert(TM == 64 || TM == 128, "MMA M");
 };
 
-template <int BN, int STAGES, bool GATHER>
+// TMEM lane quarter q (warp % 4), lane l -> row of the tile (or -1).
+template <int TM>
+__device__ __forceinline__ int tile_row_of_lane(int q, int l) {
+    if (TM == 128) return 32 * q + l;
+    return l < 16 ? 16 * q + l : -1;
+}
+
+template <int TM, int BN, bool GATHER>
 __global__ void __launch_bounds__(kTcThreads, 1)
-    spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const TcArgs p) {
-    using Cfg = TcCfg<BN, STAGES>;
+    spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_e,
+                   const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
+    using Cfg = TcCfg<TM, BN>;
+    constexpr int STAGES = Cfg::kStages;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];   // TMA bytes landed
     __shared__ __align__(8) uint64_t meta_bar[STAGES];   // m-indices written to TMEM (4 warps)
@@ -93,16 +109,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t acc_bar;            // accumulator complete
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
+    __shared__ __align__(16) uint32_t s_cidx[GATHER ? kCidxChunk * 32 : 1];
 
     // B stages first: a B descriptor read stays inside this CTA's allocation
     // even if its two strides were interpreted the other way round.
     const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sB0 = smem_base;
     const uint32_t sA0 = sB0 + STAGES * Cfg::kBBytes;
+    const uint32_t sE0 = sA0 + STAGES * Cfg::kABytes;
+    const uint8_t* sE_generic = smem_raw + (sE0 - smem_u32(smem_raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t n0 = static_cast<int64_t>(blockIdx.x) * BN;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * kTileM;
+    const int64_t m0 = static_cast<int64_t>(blockIdx.y) * TM;
     const int split = blockIdx.z;
     const int kt0 = split * p.kt_per_split;
     const int nkt = min(p.num_kt, kt0 + p.kt_per_split) - kt0;
@@ -119,6 +138,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     if (threadIdx.x == 32) {
         tma_prefetch_desc(&tm_a);
+        tma_prefetch_desc(&tm_e);
         tma_prefetch_desc(&tm_b);
     }
     if (warp == 1) {
@@ -128,7 +148,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tmem_acc = tmem_slot;        // columns [0, BN): fp32 accumulator, lane = row
+    const uint32_t tmem_acc = tmem_slot;        // columns [0, BN): fp32 accumulator
     const uint32_t tmem_e = tmem_slot + BN;     // columns [BN, BN + STAGES*32): m-index words
     volatile int* abort = &abort_flag;
 
@@ -137,8 +157,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int last_it[STAGES];
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) last_it[s] = -1;
-        const uint32_t* crow = p.colidx + (m0 / p.V) * p.nblk;
+        const uint32_t* crow = p.colidx + (m0 / p.V) * p.nblk + static_cast<int64_t>(kt0) * 32;
         for (int it = 0; it < nkt; ++it) {
+            if (GATHER && (it % kCidxChunk) == 0) {
+                // stage the column-loc words of the next kCidxChunk stages (only this warp reads them)
+                const int n = min(kCidxChunk, nkt - it) * 32;
+                __syncwarp();
+                for (int u = lane; u < n; u += 32) s_cidx[u] = __ldg(crow + static_cast<int64_t>(it) * 32 + u);
+                __syncwarp();
+            }
             const int slot = it % STAGES;
             const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
             int ok = 1;
@@ -149,12 +176,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t fb = smem_u32(&full_bar[slot]);
             const uint32_t sA = sA0 + slot * Cfg::kABytes;
             const uint32_t sB = sB0 + slot * Cfg::kBBytes;
+            const uint32_t sE = sE0 + slot * Cfg::kEBytes;
             if (lane == 0) {
                 mbar_arrive_expect_tx(fb, Cfg::kStageTx);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     tma_load_2d(sA + s * Cfg::kAStepBytes, &tm_a, kt * kValsPerKTile + 16 * s,
                                 static_cast<int32_t>(m0), fb);
+                tma_load_2d(sE, &tm_e, kt * 4, static_cast<int32_t>(m0), fb);
                 if (!GATHER) {
 #pragma unroll
                     for (int a = 0; a < Cfg::kAtoms; ++a)
@@ -165,9 +194,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             }
             if (GATHER) {
                 __syncwarp();
-                // 32 blocks per stage: lane l gathers the 4 selected B rows of block kt*32 + l
+                // lane l gathers the 4 selected B rows of block 32*kt + l
                 const int64_t j = static_cast<int64_t>(kt) * 32 + lane;
-                const uint32_t sel = __ldg(crow + j);
+                const uint32_t sel = s_cidx[(it % kCidxChunk) * 32 + lane];
                 const int32_t rb = static_cast<int32_t>(j * p.M);
                 const int32_t r0 = rb + static_cast<int32_t>(sel & 0xFFu);
                 const int32_t r1 = rb + static_cast<int32_t>((sel >> 8) & 0xFFu);
@@ -187,11 +216,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc_f16_f32(kTileM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/true);
+            constexpr uint32_t idesc = make_idesc_f16_f32(TM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/true);
             for (int it = 0; it < nkt; ++it) {
                 const int slot = it % STAGES;
                 const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
-                if (!mbar_wait(smem_u32(&full_bar[slot]), ph, abort)) break;
+                // the m-index warps arrive only after this stage's TMA bytes landed
                 if (!mbar_wait(smem_u32(&meta_bar[slot]), ph, abort)) break;
                 tc_fence_after_sync();
                 const uint32_t sA = sA0 + slot * Cfg::kABytes;
@@ -216,28 +245,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else {
         const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
-        const int64_t row = m0 + 32 * q + lane;
+        const int trow = tile_row_of_lane<TM>(q, lane);
+        const int64_t row = trow >= 0 ? m0 + trow : p.R;  // lanes with no row act as padding
+        const int srow = trow >= 0 ? trow : tile_row_of_lane<TM>(q, lane & 15);  // an in-tile row to read
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         // ------------------------------------------------ m-indices -> TMEM
         for (int it = 0; it < nkt; ++it) {
             const int slot = it % STAGES;
             const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
             int ok = 1;
-            if (lane == 0) ok = mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort);
+            if (lane == 0) ok = mbar_wait(smem_u32(&full_bar[slot]), ph, abort);
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             if (!ok) break;
-            const int kt = kt0 + it;
-            uint4 w = make_uint4(kPadMeta, kPadMeta, kPadMeta, kPadMeta);
-            if (row < p.R) w = __ldg(reinterpret_cast<const uint4*>(p.meta + row * p.mpitch) + kt);
+            uint4 w = *reinterpret_cast<const uint4*>(sE_generic + slot * Cfg::kEBytes + srow * 16);
+            if (row >= p.R) w = make_uint4(kPadMeta, kPadMeta, kPadMeta, kPadMeta);
             const uint32_t own[4] = {w.x, w.y, w.z, w.w};
             uint32_t v[32];
 #pragma unroll
             for (int u = 0; u < 32; ++u) v[u] = 0u;
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                // The sparse MMA reads the m-indices of rows i and i+8 of each
-                // 16-row group in pairs: lane i holds both rows' first 16 bits
-                // (K 0..15 of the k-step), lane i+8 both rows' last 16 bits.
                 const uint32_t mine = own[s];
                 const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, mine, 8);
                 v[s * kMetaSlotCols] = (lane & 8) ? ((other >> 16) | (mine & 0xFFFF0000u))
@@ -311,54 +338,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
 }
 
-template <int BN, int STAGES, bool GATHER>
+template <int TM, int BN, bool GATHER>
 cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, dim3 grid, cudaStream_t stream) {
-    using Cfg = TcCfg<BN, STAGES>;
-    auto kern = spmm_tc_kernel<BN, STAGES, GATHER>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    kern<<<grid, kTcThreads, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_b, p);
+    using Cfg = TcCfg<TM, BN>;
+    auto kern = spmm_tc_kernel<TM, BN, GATHER>;
+    static bool configured = false;  // once per process (the attribute is per function)
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    kern<<<grid, kTcThreads, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_e, L.tm_b, p);
     return cudaGetLastError();
 }
 
-template <bool GATHER>
+template <int TM, bool GATHER>
 cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, dim3 grid, cudaStream_t stream) {
     switch (L.tile_n) {
-        case 16: return launch_variant<16, 6, GATHER>(L, p, grid, stream);
-        case 32: return launch_variant<32, 6, GATHER>(L, p, grid, stream);
-        case 64: return launch_variant<64, 6, GATHER>(L, p, grid, stream);
-        case 128: return launch_variant<128, 4, GATHER>(L, p, grid, stream);
-        case 256: return launch_variant<256, 2, GATHER>(L, p, grid, stream);
+        case 16: return launch_variant<TM, 16, GATHER>(L, p, grid, stream);
+        case 32: return launch_variant<TM, 32, GATHER>(L, p, grid, stream);
+        case 64: return launch_variant<TM, 64, GATHER>(L, p, grid, stream);
+        case 128: return launch_variant<TM, 128, GATHER>(L, p, grid, stream);
+        case 256: return launch_variant<TM, 256, GATHER>(L, p, grid, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-int tc_default_stages(int tile_n) {
-    switch (tile_n) {
-        case 16:
-        case 32:
-        case 64: return 6;
-        case 128: return 4;
-        case 256: return 2;
-        default: return 0;
-    }
-}
-
-int tc_smem_bytes(int tile_m, int tile_n, int stages) {
-    (void)tile_m;
-    const int atoms = (tile_n + 63) / 64;
-    return stages * (kTileM * 128 + atoms * kKTile * 128) + 1024;
+int tc_default_stages(int tile_m, int tile_n) {
+    if (tile_m != 64 && tile_m != 128) return 0;
+    if (tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 && tile_n != 256) return 0;
+    return tc_stages_for(tile_m, tile_n);
 }
 
 cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, int64_t N, void* C, int64_t ld_c, bool c_f32,
                            float* partial, cudaStream_t stream) {
-    if (L.tile_m != kTileM || L.stages != tc_default_stages(L.tile_n)) return cudaErrorInvalidValue;
+    if (tc_default_stages(L.tile_m, L.tile_n) == 0 || L.stages != tc_default_stages(L.tile_m, L.tile_n))
+        return cudaErrorInvalidValue;
     TcArgs p;
     p.colidx = static_cast<const uint32_t*>(A.colidx);
-    p.meta = static_cast<const uint8_t*>(A.meta);
-    p.mpitch = meta_pitch(A.K, A.M);
     p.C = C;
     p.ld_c = ld_c;
     p.R = A.R;
@@ -376,9 +395,13 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, int64_t N, 
     p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ld_c * esz) % 16 == 0);
     p.status = A.status;
     if (splits > 1 && partial == nullptr) return cudaErrorInvalidValue;
-    dim3 grid(static_cast<unsigned>((N + L.tile_n - 1) / L.tile_n), static_cast<unsigned>((A.R + kTileM - 1) / kTileM),
-              static_cast<unsigned>(splits));
-    cudaError_t e = L.gather ? dispatch_bn<true>(L, p, grid, stream) : dispatch_bn<false>(L, p, grid, stream);
+    dim3 grid(static_cast<unsigned>((N + L.tile_n - 1) / L.tile_n),
+              static_cast<unsigned>((A.R + L.tile_m - 1) / L.tile_m), static_cast<unsigned>(splits));
+    cudaError_t e;
+    if (L.tile_m == 128)
+        e = L.gather ? dispatch_bn<128, true>(L, p, grid, stream) : dispatch_bn<128, false>(L, p, grid, stream);
+    else
+        e = L.gather ? dispatch_bn<64, true>(L, p, grid, stream) : dispatch_bn<64, false>(L, p, grid, stream);
     if (e != cudaSuccess) return e;
     if (splits > 1) return launch_splitk_reduce(partial, splits, A.R, N, C, ld_c, c_f32, stream);
     return cudaSuccess;

@@ -50,8 +50,19 @@ cudaError_t launch_decompress(const vnm_matrix_s& A, void* W, int64_t ld_w, cuda
 cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
                              int64_t ld_c, bool c_f32, cudaStream_t stream);
 
+// Shared-memory pipeline depth of the tensor-core kernel for a tile: as many
+// 128-column stages (B rows, A values, m-indices) as fit next to the staged
+// column-loc words, at most 8.
+__host__ __device__ constexpr int tc_stages_for(int tile_m, int tile_n) {
+    const int stage = ((tile_n + 63) / 64) * 128 * 128 + tile_m * 128 + tile_m * 16;
+    const int budget = 227 * 1024 - 8 * 1024 - 2 * 1024;  // minus column-loc words, barriers, alignment
+    const int s = budget / stage;
+    return s > 8 ? 8 : s;
+}
+
 struct TcLaunch {
     CUtensorMap tm_a;   // values, box {16, tile_m}: one MMA k-step, 32B swizzle
+    CUtensorMap tm_e;   // m-indices as u32 words, box {4, tile_m}, no swizzle
     CUtensorMap tm_b;   // B, box {64, 128} (tile) or {64, 1} (gather4), 128B swizzle
     int tile_m, tile_n, stages, splits;
     bool gather;        // M > 4: rows of B selected through colidx
@@ -65,7 +76,7 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, int64_t N, 
 cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, void* C,
                                  int64_t ld_c, bool c_f32, cudaStream_t stream);
 
-// Shared-memory bytes one TC CTA needs for a (tile_m, tile_n, stages) plan.
-int tc_smem_bytes(int tile_m, int tile_n, int stages);
+// Pipeline depth the tensor-core kernel is built with for a tile (0: no such tile).
+int tc_default_stages(int tile_m, int tile_n);
 
 }  // namespace vnm

@@ -62,6 +62,10 @@ TC_SHAPES = [
     (272, 256, 72, 16, 4),     # ragged rows (R % 128 != 0), plain 2:4
     (256, 1024, 24, 256, 8),   # V = 256: two tiles per block row
     (128, 512, 8, 128, 4),     # N = 8: one MMA of N = 16 with zero-filled columns
+    (256, 1024, 128, 64, 8),   # V = 64: 64-row tiles (M = 64 MMA)
+    (192, 2048, 40, 64, 16),
+    (64, 4096, 256, 64, 32),
+    (320, 512, 72, 64, 4),     # V = 64 with M = 4: 128-row tiles, ragged rows
 ]
 
 
@@ -76,12 +80,15 @@ def test_tensor_core_path(R, K, N, V, M, c_dtype):
 
 
 @pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 256])
-def test_tensor_core_tiles(tile_n):
-    R, K, N, V, M = 256, 1024, 300, 128, 8
+@pytest.mark.parametrize("V,tile_m", [(128, 128), (64, 64), (128, 64)])
+def test_tensor_core_tiles(tile_n, V, tile_m):
+    R, K, N, M = 256, 1024, 296, 8  # N % 8 == 0 (TMA rows), ragged against every tile_n
     A, B, comp = _setup(R, K, N, V, M, seed=22)
     plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    assert plan.path == vnm.VNM_PATH_TC
+    plan.tile_m = tile_m
     plan.tile_n = tile_n
-    plan.stages = {16: 6, 32: 6, 64: 6, 128: 4, 256: 2}[tile_n]
+    plan.stages = 0  # the default depth for this tile
     plan.splits = 1
     got, _ = run_spmm(A, B, plan=plan)
     check_close(got, _ref(comp, R, K, V, M, B), f"tile_n {tile_n}")
@@ -126,6 +133,17 @@ def test_unaligned_and_strided_operands():
     check_close(got, ref, "ld_b = N")
     got, _ = run_spmm(A, B, ld_b=48, ld_c=41)  # aligned B, padded C rows
     check_close(got, ref, "ld_b = 48, ld_c = 41")
+
+
+def test_unservable_plan_rejected():
+    R, K, N, V, M = 128, 512, 64, 64, 8
+    A, B, comp = _setup(R, K, N, V, M, seed=27)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    assert plan.path == vnm.VNM_PATH_TC and plan.tile_m == 64
+    plan.tile_m = 128  # a 128-row tile would span two column-loc blocks
+    with pytest.raises(vnm.VnmError) as e:
+        run_spmm(A, B, plan=plan)
+    assert e.value.code == vnm.VNM_ERR_UNSUPPORTED
 
 
 def test_empty_products():
