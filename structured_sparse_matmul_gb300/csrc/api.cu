@@ -116,6 +116,18 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     if (tiles < A.sm_count) splits = std::min<int64_t>(num_kt, std::max<int64_t>(1, A.sm_count / tiles));
     const int64_t per_split = A.R * N * static_cast<int64_t>(sizeof(float));
     if (splits > 1) splits = std::min<int64_t>(splits, static_cast<int64_t>(workspace_bytes) / per_split);
+    // a gathering CTA covers at most tc_gather_max_stages() stages
+    const int64_t min_splits = A.M > 4 ? ceil_div(num_kt, vnm::tc_gather_max_stages()) : 1;
+    splits = std::max<int64_t>(1, splits);
+    if (splits < min_splits) {
+        if (min_splits * per_split > static_cast<int64_t>(workspace_bytes)) {
+            pl.path = VNM_PATH_SIMT;  // such a long K needs split-K partials; no workspace for them
+            pl.tile_m = pl.tile_n = pl.stages = 0;
+            pl.splits = 1;
+            return pl;
+        }
+        splits = min_splits;
+    }
     pl.splits = static_cast<int32_t>(std::max<int64_t>(1, splits));
     return pl;
 }
@@ -138,6 +150,8 @@ vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void
     if (depth == 0 || (pl.stages != 0 && pl.stages != depth)) return VNM_ERR_UNSUPPORTED;
     if (pl.splits < 1) return VNM_ERR_INVALID_ARG;
     const int s = effective_splits(A, pl.splits);
+    const int num_kt = static_cast<int>((A.K / A.M) / 32);
+    if (A.M > 4 && ceil_div(num_kt, s) > vnm::tc_gather_max_stages()) return VNM_ERR_UNSUPPORTED;
     if (s > 1) {
         const size_t need = static_cast<size_t>(s) * A.R * N * sizeof(float);
         if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)) return VNM_ERR_INVALID_ARG;
@@ -168,7 +182,7 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, A->K, ld_b * 2, 64, L.gather ? 1 : 128,
                              CU_TENSOR_MAP_SWIZZLE_128B);
         if (!ok) return VNM_ERR_CUDA;
-        e = vnm::launch_spmm_tc(*A, L, N, C, ld_c, c_f32, static_cast<float*>(workspace), stream);
+        e = vnm::launch_spmm_tc(*A, L, B, ld_b, N, C, ld_c, c_f32, static_cast<float*>(workspace), stream);
     }
     return e == cudaSuccess ? VNM_OK : VNM_ERR_CUDA;
 }

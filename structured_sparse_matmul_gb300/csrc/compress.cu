@@ -17,6 +17,7 @@
 #include <algorithm>
 
 #include "vnm_internal.h"
+#include "vnm_ptx.cuh"
 
 namespace vnm {
 namespace {
@@ -64,24 +65,23 @@ __device__ __forceinline__ uint32_t top4_ascending(const uint64_t* score, int n)
 
 // 2 of the 4 values a[0..3] with the largest |a| (lower slot on ties), in
 // ascending slot order. Returns the 4-bit code s0 | s1 << 2 and the two
-// fp16 bit patterns.
+// fp16 bit patterns. Branch-free: slot i is kept when fewer than two slots
+// beat it, slot j < i beating i when |a_j| >= |a_i| and slot j > i when
+// |a_j| > |a_i| (finite fp16 magnitudes order like their integer bits).
 __device__ __forceinline__ uint32_t keep2of4(const uint16_t a[4], uint16_t& v0, uint16_t& v1) {
-    uint32_t m[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) m[s] = a[s] & 0x7FFFu;  // finite fp16 magnitudes order like integers
-    int first = 0;
-#pragma unroll
-    for (int s = 1; s < 4; ++s)
-        if (m[s] > m[first]) first = s;
-    int second = first == 0 ? 1 : 0;
-#pragma unroll
-    for (int s = 0; s < 4; ++s)
-        if (s != first && m[s] > m[second]) second = s;
-    const int s0 = first < second ? first : second;
-    const int s1 = first < second ? second : first;
-    v0 = a[s0];
-    v1 = a[s1];
-    return static_cast<uint32_t>(s0) | (static_cast<uint32_t>(s1) << 2);
+    const uint32_t m0 = a[0] & 0x7FFFu, m1 = a[1] & 0x7FFFu, m2 = a[2] & 0x7FFFu, m3 = a[3] & 0x7FFFu;
+    const uint32_t g01 = m0 >= m1, g02 = m0 >= m2, g03 = m0 >= m3;
+    const uint32_t g12 = m1 >= m2, g13 = m1 >= m3, g23 = m2 >= m3;
+    const uint32_t r0 = (1u - g01) + (1u - g02) + (1u - g03);
+    const uint32_t r1 = g01 + (1u - g12) + (1u - g13);
+    const uint32_t r2 = g02 + g12 + (1u - g23);
+    const uint32_t r3 = g03 + g13 + g23;
+    const uint32_t keep = (r0 < 2u) | ((r1 < 2u) << 1) | ((r2 < 2u) << 2) | ((r3 < 2u) << 3);
+    const uint32_t s0 = __ffs(keep) - 1u;  // exactly two bits are set
+    const uint32_t s1 = 31u - __clz(keep);
+    v0 = s0 == 0u ? a[0] : (s0 == 1u ? a[1] : a[2]);
+    v1 = s1 == 3u ? a[3] : (s1 == 2u ? a[2] : a[1]);
+    return s0 | (s1 << 2);
 }
 
 // Bytes of the staged W tile, rounded up so the column sums that follow
@@ -253,6 +253,275 @@ __global__ void __launch_bounds__(kCompressThreads) compress_block_kernel(const 
     }
 }
 
+// Streaming compress: a persistent grid walks the V x tk tiles; each CTA
+// double-buffers its tiles in shared memory with 16-byte cp.async, so the
+// next tile loads while this one is processed.
+//   M == 4: column-loc is the identity; only the 2:4 step runs.
+//   M > 4:  columns are ranked by fp32 sums of |w| (rows added in order);
+//           when the gap between the 4th and 5th largest is not wider than
+//           the fp32 error bound of such a sum (V * 2^-24 relative), the
+//           block's columns are re-summed exactly as integers (units of
+//           2^-24) and ranked on those. Either way the result is the exact
+//           ranking, ties to the lower column.
+constexpr int kStreamCtasPerSm = 3;
+
+__device__ __forceinline__ float half_abs_to_float(uint16_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0x7FFFu)));
+}
+
+// Rank the M columns of one block (one warp): keep the 4 largest sums,
+// lower column first on ties; return them ascending, one per byte. Lanes
+// own columns lane, lane + 32, ...; `score` is either the fp32 or the exact
+// sums (compared as given). `sRank` is per-block scratch of M bytes.
+template <typename T>
+__device__ __forceinline__ void rank_columns(const T* score, int M, uint8_t* sRank, int lane) {
+    for (int c = lane; c < M; c += 32) {
+        const T v = score[c];
+        int rank = 0;
+        for (int d = 0; d < M; ++d) {
+            const T w = score[d];
+            rank += (w > v) || (w == v && d < c);
+        }
+        sRank[c] = static_cast<uint8_t>(rank < 255 ? rank : 255);
+    }
+    __syncwarp();
+}
+
+// The 4 columns of rank < 4, ascending, packed one per byte.
+__device__ __forceinline__ uint32_t selected_columns(const uint8_t* sRank, int M, int lane) {
+    uint32_t word = 0;
+    for (int c0 = 0; c0 < M; c0 += 32) {
+        const int c = c0 + lane;
+        const bool sel = c < M && sRank[c] < 4;
+        const uint32_t mask = __ballot_sync(0xFFFFFFFFu, sel);
+        if (sel) {
+            // position among the selected columns = selected columns before c
+            int pos = __popc(mask & ((1u << lane) - 1u));
+            for (int d = 0; d < c0; ++d) pos += sRank[d] < 4;
+            word |= static_cast<uint32_t>(c) << (8 * pos);
+        }
+    }
+    // OR the partial words of all lanes
+    for (int off = 16; off > 0; off >>= 1) word |= __shfl_xor_sync(0xFFFFFFFFu, word, off);
+    return word;
+}
+
+// Value of the column of rank r (0-based) among `score`, via sRank.
+template <typename T>
+__device__ __forceinline__ T value_of_rank(const T* score, const uint8_t* sRank, int M, int r, int lane) {
+    T v = T(0);
+    int found = 0;
+    for (int c0 = 0; c0 < M; c0 += 32) {
+        const int c = c0 + lane;
+        const bool hit = c < M && sRank[c] == r;
+        const uint32_t mask = __ballot_sync(0xFFFFFFFFu, hit);
+        if (!found && mask) {
+            const int src = __ffs(mask) - 1;
+            v = __shfl_sync(0xFFFFFFFFu, hit ? score[c] : T(0), src);
+            found = 1;
+        }
+    }
+    return v;
+}
+
+// Warp-wide: the 4 selected columns of the block whose columns start at
+// col0 of the staged tile. fp32 sums decide unless the 4th/5th gap is inside
+// the fp32 error bound (relative 2.5 * V * 2^-24); then exact integer sums.
+__device__ uint32_t rank_block_warp(const uint16_t* sW, int TK, int V, int M, int col0, const float* sF,
+                                    uint64_t* sExact, uint8_t* sRank, int lane) {
+    rank_columns(sF + col0, M, sRank, lane);
+    const float v4 = value_of_rank(sF + col0, sRank, M, 3, lane);
+    const float v5 = value_of_rank(sF + col0, sRank, M, 4, lane);
+    if (v4 - v5 > 2.5f * static_cast<float>(V) * 5.9604645e-8f * v4) return selected_columns(sRank, M, lane);
+    for (int c = lane; c < M; c += 32) {
+        uint64_t e = 0;
+        for (int r = 0; r < V; ++r) e += mag_units(sW[r * TK + col0 + c]);
+        sExact[col0 + c] = e;
+    }
+    __syncwarp();
+    rank_columns(sExact + col0, M, sRank, lane);
+    return selected_columns(sRank, M, lane);
+}
+
+__global__ void __launch_bounds__(kCompressThreads) compress_stream_kernel(const CompressArgs p) {
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int V = p.V, M = p.M, TK = p.tk;
+    const size_t tile_bytes = tile_bytes_aligned(V, TK);
+    uint16_t* sBuf[2] = {reinterpret_cast<uint16_t*>(smem), reinterpret_cast<uint16_t*>(smem + tile_bytes)};
+    float* sF = reinterpret_cast<float*>(smem + 2 * tile_bytes);                    // [TK]
+    uint64_t* sExact = reinterpret_cast<uint64_t*>(sF + TK + (TK & 1));            // [TK]
+    uint32_t* sSel = reinterpret_cast<uint32_t*>(sExact + TK);                      // [TK / M]
+    float* sPart = reinterpret_cast<float*>(sSel + TK / M + 4);                     // [kCompressThreads * 8]
+    uint8_t* sRankAll = reinterpret_cast<uint8_t*>(sPart + kCompressThreads * 8);    // [8 warps][256]
+    __shared__ int bad;
+    const int64_t tiles_x = (p.K + TK - 1) / TK;
+    const int64_t n_tiles = (p.R / V) * tiles_x;
+    const int cpr = TK / 8;  // 16-byte chunks per tile row
+    const bool cpr_pow2 = (cpr & (cpr - 1)) == 0;
+    const int cpr_log2 = 31 - __clz(cpr);
+
+    auto issue = [&](int64_t t, uint16_t* dst) {
+        const int64_t i = t / tiles_x, k0 = (t % tiles_x) * TK;
+        const int tk = static_cast<int>(p.K - k0 < TK ? p.K - k0 : TK);
+        const uint16_t* Wt = p.W + i * V * p.ld_w + k0;
+        for (int q = threadIdx.x; q < V * cpr; q += kCompressThreads) {
+            const int r = cpr_pow2 ? (q >> cpr_log2) : q / cpr;
+            const int c8 = q - r * cpr;
+            const int left = tk - 8 * c8;
+            const uint32_t bytes = left >= 8 ? 16u : (left > 0 ? 2u * left : 0u);
+            cp_async_16(smem_u32(dst + r * TK + 8 * c8), Wt + r * p.ld_w + (bytes ? 8 * c8 : 0), bytes);
+        }
+        cp_async_commit();
+    };
+
+    if (threadIdx.x == 0) bad = 0;
+    int64_t t = blockIdx.x;
+    if (t < n_tiles) issue(t, sBuf[0]);
+    for (int n = 0; t < n_tiles; ++n, t += gridDim.x) {
+        const int64_t tn = t + gridDim.x;
+        if (tn < n_tiles) {
+            issue(tn, sBuf[(n + 1) & 1]);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncthreads();
+        const uint16_t* sW = sBuf[n & 1];
+        const int64_t i = t / tiles_x, k0 = (t % tiles_x) * TK;
+        const int tk = static_cast<int>(p.K - k0 < TK ? p.K - k0 : TK);
+        const int nb = tk / M;
+        const int64_t jt = k0 / M;
+        int nonfinite = 0;
+        if (M == 4) {
+            for (int b = threadIdx.x; b < nb; b += kCompressThreads) sSel[b] = 0x03020100u;
+        } else {
+            // fp32 column sums: thread = (8-column chunk, row group); partials per row group
+            const int cpr = TK / 8;
+            if (kCompressThreads % cpr == 0) {
+                const int rgs = kCompressThreads / cpr;
+                const int cc = threadIdx.x % cpr, rg = threadIdx.x / cpr;
+                float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+                for (int r = rg; r < V; r += rgs) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(sW + r * TK + 8 * cc);
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int h = 0; h < 4; ++h) {
+                        acc[2 * h] += half_abs_to_float(static_cast<uint16_t>(w[h] & 0xFFFFu));
+                        acc[2 * h + 1] += half_abs_to_float(static_cast<uint16_t>(w[h] >> 16));
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < 8; ++h) sPart[rg * TK + 8 * cc + h] = acc[h];
+                __syncthreads();
+                for (int c = threadIdx.x; c < tk; c += kCompressThreads) {
+                    float sum = 0.f;
+                    for (int g = 0; g < rgs; ++g) sum += sPart[g * TK + c];
+                    sF[c] = sum;
+                    nonfinite |= !(sum <= 3.4e38f);  // Inf or NaN in the column
+                }
+            } else {
+                for (int c = threadIdx.x; c < tk; c += kCompressThreads) {
+                    float sum = 0.f;
+                    for (int r = 0; r < V; ++r) sum += half_abs_to_float(sW[r * TK + c]);
+                    sF[c] = sum;
+                    nonfinite |= !(sum <= 3.4e38f);
+                }
+            }
+            __syncthreads();
+            const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+            for (int b = warp; b < nb; b += kCompressThreads / 32) {
+                const uint32_t sel = rank_block_warp(sW, TK, V, M, b * M, sF, sExact, sRankAll + 256 * warp, lane);
+                if (lane == 0) sSel[b] = sel;
+            }
+        }
+        __syncthreads();
+        for (int b = threadIdx.x; b < nb; b += kCompressThreads) p.colidx[i * p.nblk + jt + b] = sSel[b];
+
+        // 2 of 4 per row; one item = one row x 4 consecutive blocks
+        const int ngroups = (nb + 3) / 4;
+        const bool vec_store = (p.nblk % 4 == 0) && (jt % 4 == 0);
+        for (int q = threadIdx.x; q < V * ngroups; q += kCompressThreads) {
+            const int r = q / ngroups, g = q % ngroups;
+            const int64_t row = i * V + r;
+            uint16_t out[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+            uint32_t code = 0;
+            const int nblk_here = min(4, nb - 4 * g);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (u < nblk_here) {
+                    const int b = 4 * g + u;
+                    const uint32_t sel = sSel[b];
+                    const uint16_t* wr = sW + r * TK + b * M;
+                    const uint16_t a[4] = {wr[sel & 0xFFu], wr[(sel >> 8) & 0xFFu], wr[(sel >> 16) & 0xFFu],
+                                           wr[sel >> 24]};
+                    if (M == 4) nonfinite |= half_nonfinite(a[0]) | half_nonfinite(a[1]) | half_nonfinite(a[2]) |
+                                             half_nonfinite(a[3]);
+                    code |= keep2of4(a, out[2 * u], out[2 * u + 1]) << (4 * u);
+                }
+            }
+            uint16_t* vrow = p.values + row * (2 * p.nblk) + 2 * (jt + 4 * g);
+            uint8_t* mrow = p.meta + row * p.mpitch + (jt + 4 * g) / 2;
+            if (vec_store && nblk_here == 4) {
+                uint4 v;
+                v.x = out[0] | (static_cast<uint32_t>(out[1]) << 16);
+                v.y = out[2] | (static_cast<uint32_t>(out[3]) << 16);
+                v.z = out[4] | (static_cast<uint32_t>(out[5]) << 16);
+                v.w = out[6] | (static_cast<uint32_t>(out[7]) << 16);
+                *reinterpret_cast<uint4*>(vrow) = v;
+                *reinterpret_cast<uint16_t*>(mrow) = static_cast<uint16_t>(code);
+            } else {
+                for (int u = 0; u < 2 * nblk_here; ++u) vrow[u] = out[u];
+                for (int u = 0; u < nblk_here; u += 2) mrow[u / 2] = static_cast<uint8_t>(code >> (4 * u));
+            }
+        }
+        if (nonfinite) bad = 1;
+        __syncthreads();  // this tile's buffer is refilled two tiles from now
+    }
+    if (threadIdx.x == 0 && bad) record_error(p.status, VNM_ERR_NONFINITE, 3);
+}
+
+// M == 4: column-loc is the identity, so prune-and-encode is the 2:4 step
+// alone, on each group of 4 consecutive weights of a row. One thread turns
+// 16 consecutive weights (32 bytes) into 8 values (16 bytes) and 4 nibbles
+// of m-indices (2 bytes); consecutive threads take consecutive chunks of a
+// row, so loads and stores are fully coalesced and no shared memory is used.
+constexpr int kM4Threads = 256;
+
+__global__ void __launch_bounds__(kM4Threads) compress_m4_kernel(const CompressArgs p) {
+    const int64_t cpr = p.K / 16;  // 16-weight chunks per row
+    const int64_t total = p.R * cpr;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kM4Threads;
+    int nonfinite = 0;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kM4Threads + threadIdx.x; q < total; q += stride) {
+        const int64_t r = q / cpr, x = q % cpr;
+        const uint4* src = reinterpret_cast<const uint4*>(p.W + r * p.ld_w + 16 * x);
+        const uint4 a = __ldg(src), b = __ldg(src + 1);
+        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+        uint16_t out[8];
+        uint32_t code = 0;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint16_t e[4] = {static_cast<uint16_t>(w[2 * g] & 0xFFFFu), static_cast<uint16_t>(w[2 * g] >> 16),
+                                   static_cast<uint16_t>(w[2 * g + 1] & 0xFFFFu),
+                                   static_cast<uint16_t>(w[2 * g + 1] >> 16)};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) nonfinite |= half_nonfinite(e[u]);
+            code |= keep2of4(e, out[2 * g], out[2 * g + 1]) << (4 * g);
+        }
+        uint4 v;
+        v.x = out[0] | (static_cast<uint32_t>(out[1]) << 16);
+        v.y = out[2] | (static_cast<uint32_t>(out[3]) << 16);
+        v.z = out[4] | (static_cast<uint32_t>(out[5]) << 16);
+        v.w = out[6] | (static_cast<uint32_t>(out[7]) << 16);
+        *reinterpret_cast<uint4*>(p.values + r * (p.K / 2) + 8 * x) = v;
+        *reinterpret_cast<uint16_t*>(p.meta + r * p.mpitch + 2 * x) = static_cast<uint16_t>(code);
+    }
+    const int64_t ncw = (p.R / p.V) * p.nblk;  // column-loc words: always 0, 1, 2, 3
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kM4Threads + threadIdx.x; q < ncw; q += stride)
+        p.colidx[q] = 0x03020100u;
+    if (__any_sync(0xFFFFFFFFu, nonfinite) && (threadIdx.x & 31) == 0) record_error(p.status, VNM_ERR_NONFINITE, 4);
+}
+
 struct DecompressArgs {
     const uint16_t* values;
     const uint8_t* meta;
@@ -295,6 +564,13 @@ cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, 
     p.mpitch = meta_pitch(A.K, A.M);
     p.status = A.status;
     if (A.R == 0 || A.K == 0) return cudaSuccess;
+    if (A.M == 4 && A.K % 16 == 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0 && ld_w % 8 == 0) {
+        const int64_t chunks = A.R * (A.K / 16);
+        const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((chunks + kM4Threads - 1) / kM4Threads,
+                                                                      static_cast<int64_t>(A.sm_count) * 8));
+        compress_m4_kernel<<<static_cast<unsigned>(blocks), kM4Threads, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
     // tile width: an even number of blocks, as many as fit the budget
     int64_t pairs = kTileElems / (static_cast<int64_t>(A.V) * 2 * A.M);
     pairs = std::min<int64_t>(pairs, kTileMaxCols / (2 * A.M));
@@ -309,6 +585,25 @@ cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, 
                                                  static_cast<int>(smem));
             if (e != cudaSuccess) return e;
             configured = smem;
+        }
+        if (p.vec_load) {
+            // persistent, double-buffered: two tiles + column sums + exact sums + selections
+            const size_t ssmem = 2 * tile_bytes_aligned(A.V, p.tk) + sizeof(float) * (p.tk + 1) +
+                                 sizeof(uint64_t) * p.tk + sizeof(uint32_t) * (p.tk / A.M + 4) +
+                                 sizeof(float) * kCompressThreads * 8 + 8 * 256 + 16;
+            static size_t sconfigured = 0;
+            if (ssmem > 48 * 1024 && ssmem > sconfigured) {
+                cudaError_t e = cudaFuncSetAttribute(compress_stream_kernel,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     static_cast<int>(ssmem));
+                if (e != cudaSuccess) return e;
+                sconfigured = ssmem;
+            }
+            const int64_t n_tiles = (A.R / A.V) * ((A.K + p.tk - 1) / p.tk);
+            const int64_t fit = std::max<int64_t>(1, std::min<int64_t>(kStreamCtasPerSm, (220 * 1024) / ssmem));
+            const int64_t ctas = std::min<int64_t>(n_tiles, static_cast<int64_t>(A.sm_count) * fit);
+            compress_stream_kernel<<<static_cast<unsigned>(ctas), kCompressThreads, ssmem, stream>>>(p);
+            return cudaGetLastError();
         }
         dim3 grid(static_cast<unsigned>((A.K + p.tk - 1) / p.tk), static_cast<unsigned>(A.R / A.V));
         compress_tiled_kernel<<<grid, kCompressThreads, smem, stream>>>(p);

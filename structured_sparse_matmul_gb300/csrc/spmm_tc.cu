@@ -10,15 +10,22 @@
 // GB300 design (one CTA = one tile_m x tile_n tile of C, over a range of the
 // condensed K; tile_m = 128, or 64 when V = 64 and column-loc differs per
 // 64-row block). Per 128-column stage of the condensed K (4 MMA k-steps):
-//   warp 0    TMA producer. Up front (and every kCidxChunk stages) it copies
-//             the column-loc words of its k-range into shared memory, so no
-//             global load sits on a stage's critical path. Per stage: four
-//             tiled loads of the A values (one per MMA k-step: tile_m rows x
-//             16 values, 32B swizzle, each in its own aligned buffer), one of
-//             the m-indices (tile_m rows x 16 bytes) and the B rows:
-//             M == 4 -> a plain tiled load (column-loc is the identity);
-//             M > 4 -> lane l issues the 4-row TMA gather of the B rows that
-//             block 32*stage + l selects.
+//   warp 0    TMA producer. Per stage: four tiled loads of the A values
+//             (one per MMA k-step: tile_m rows x 16 values, 32B swizzle, each
+//             in its own aligned buffer), one of the m-indices (tile_m rows x
+//             16 bytes) and, when M == 4 (column-loc is the identity), the B
+//             rows as plain tiled loads.
+//   warps 6-9 (M > 4) the B gather: the column-loc words of the CTA's
+//             k-range (at most kCidxStages stages; the planner splits K to
+//             keep it so) are staged in shared memory before the main loop;
+//             per stage these warps copy the 128 selected B rows (4 per
+//             block, tile_n columns each) with 16-byte cp.async, coalesced
+//             along each row, straight into the 128B-swizzled operand layout
+//             (zero-filled past N); each thread's copies arrive on the
+//             stage's barrier by themselves when they land
+//             (cp.async.mbarrier.arrive), so every pipeline stage can be in
+//             flight; the MMA thread fences the generic-proxy writes into the
+//             async proxy after acquiring the barrier.
 //   warps 2-5 per stage: read their rows' m-index words from shared memory,
 //             pair them the way the sparse MMA reads them (rows i and i+8 of
 //             each 16-row group share their 16-bit halves between TMEM lanes
@@ -42,17 +49,21 @@
 namespace vnm {
 namespace {
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreadsTile = 192;    // warps 0-5
+constexpr int kTcThreadsGather = 320;  // warps 0-5 plus 4 gather warps
+constexpr int kGatherThreads = 128;
 constexpr int kKTile = 128;        // condensed K per stage = 4 MMAs of K = 32
 constexpr int kValsPerKTile = 64;  // stored values per row per stage (128 bytes)
 constexpr int kMetaSlotCols = 8;   // TMEM columns between consecutive MMAs' m-index words
 constexpr int kMetaStageCols = 4 * kMetaSlotCols;
-constexpr int kCidxChunk = 64;     // stages of column-loc words staged in shared memory at a time
+constexpr int kCidxStages = 64;    // most stages one gathering CTA covers (column-loc words in shared memory)
 // m-index word of a row that lies beyond R: slots (0, 1) in all 8 groups
 constexpr uint32_t kPadMeta = 0x44444444u;
 
 struct TcArgs {
     const uint32_t* colidx;  // [R/V][nblk] words of 4 column bytes
+    const uint16_t* B;       // K x N fp16 (ld_b), read by the gather warps
+    int64_t ld_b;
     void* C;
     int64_t ld_c;
     float* partial;          // [splits][R][N] fp32, or null
@@ -97,7 +108,7 @@ __device__ __forceinline__ int tile_row_of_lane(int q, int l) {
 }
 
 template <int TM, int BN, bool GATHER>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(GATHER ? kTcThreadsGather : kTcThreadsTile, 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_e,
                    const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
     using Cfg = TcCfg<TM, BN>;
@@ -109,7 +120,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     __shared__ __align__(8) uint64_t acc_bar;            // accumulator complete
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
-    __shared__ __align__(16) uint32_t s_cidx[GATHER ? kCidxChunk * 32 : 1];
+    __shared__ __align__(16) uint32_t s_cidx[GATHER ? kCidxStages * 32 : 1];
 
     // B stages first: a B descriptor read stays inside this CTA's allocation
     // even if its two strides were interpreted the other way round.
@@ -128,7 +139,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&full_bar[s]), GATHER ? 1 + kGatherThreads : 1);
             mbar_init(smem_u32(&meta_bar[s]), 4);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
@@ -140,6 +151,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_e);
         tma_prefetch_desc(&tm_b);
+    }
+    if (GATHER) {
+        if (nkt > kCidxStages) {  // the host never launches this; refuse rather than overrun
+            if (threadIdx.x == 0) record_error(p.status, VNM_ERR_INTERNAL, 20);
+            return;
+        }
+        // column-loc words of this CTA's k-range, for the gather warps
+        const uint32_t* crow = p.colidx + (m0 / p.V) * p.nblk + static_cast<int64_t>(kt0) * 32;
+        for (int u = threadIdx.x; u < nkt * 32; u += blockDim.x) s_cidx[u] = __ldg(crow + u);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&tmem_slot), Cfg::kTmemCols);
@@ -157,15 +177,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int last_it[STAGES];
 #pragma unroll
         for (int s = 0; s < STAGES; ++s) last_it[s] = -1;
-        const uint32_t* crow = p.colidx + (m0 / p.V) * p.nblk + static_cast<int64_t>(kt0) * 32;
         for (int it = 0; it < nkt; ++it) {
-            if (GATHER && (it % kCidxChunk) == 0) {
-                // stage the column-loc words of the next kCidxChunk stages (only this warp reads them)
-                const int n = min(kCidxChunk, nkt - it) * 32;
-                __syncwarp();
-                for (int u = lane; u < n; u += 32) s_cidx[u] = __ldg(crow + static_cast<int64_t>(it) * 32 + u);
-                __syncwarp();
-            }
             const int slot = it % STAGES;
             const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
             int ok = 1;
@@ -178,7 +190,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const uint32_t sB = sB0 + slot * Cfg::kBBytes;
             const uint32_t sE = sE0 + slot * Cfg::kEBytes;
             if (lane == 0) {
-                mbar_arrive_expect_tx(fb, Cfg::kStageTx);
+                mbar_arrive_expect_tx(fb, GATHER ? Cfg::kABytes + Cfg::kEBytes : Cfg::kStageTx);
 #pragma unroll
                 for (int s = 0; s < 4; ++s)
                     tma_load_2d(sA + s * Cfg::kAStepBytes, &tm_a, kt * kValsPerKTile + 16 * s,
@@ -191,21 +203,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                                     fb);
                 }
                 last_it[slot] = it;
-            }
-            if (GATHER) {
-                __syncwarp();
-                // lane l gathers the 4 selected B rows of block 32*kt + l
-                const int64_t j = static_cast<int64_t>(kt) * 32 + lane;
-                const uint32_t sel = s_cidx[(it % kCidxChunk) * 32 + lane];
-                const int32_t rb = static_cast<int32_t>(j * p.M);
-                const int32_t r0 = rb + static_cast<int32_t>(sel & 0xFFu);
-                const int32_t r1 = rb + static_cast<int32_t>((sel >> 8) & 0xFFu);
-                const int32_t r2 = rb + static_cast<int32_t>((sel >> 16) & 0xFFu);
-                const int32_t r3 = rb + static_cast<int32_t>(sel >> 24);
-#pragma unroll
-                for (int a = 0; a < Cfg::kAtoms; ++a)
-                    tma_gather4(sB + a * kKTile * 128 + lane * 4 * 128, &tm_b, static_cast<int32_t>(n0 + 64 * a), r0,
-                                r1, r2, r3, fb);
             }
         }
         if (lane == 0 && *abort) {
@@ -222,6 +219,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
                 // the m-index warps arrive only after this stage's TMA bytes landed
                 if (!mbar_wait(smem_u32(&meta_bar[slot]), ph, abort)) break;
+                if (GATHER) fence_proxy_async_smem();  // gathered B rows were written by cp.async
                 tc_fence_after_sync();
                 const uint32_t sA = sA0 + slot * Cfg::kABytes;
                 const uint32_t sB = sB0 + slot * Cfg::kBBytes;
@@ -243,6 +241,47 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             mbar_drain(smem_u32(&acc_bar), 0);
         }
         __syncwarp();
+    } else if (GATHER && warp >= 6) {
+        // ------------------------------------------------ B gather (cp.async)
+        constexpr int kChunksPerRow = BN / 8;                       // 16-byte chunks of a gathered row
+        constexpr int kChunks = kKTile * kChunksPerRow;             // per stage
+        static_assert(kChunks % kGatherThreads == 0, "gather split");
+        const int gt = threadIdx.x - 6 * 32;
+        // Fixed thread -> (chunk, row) map: thread gt copies chunk c of rows
+        // q = u * kRowsPerPass + q0, u = 0 .. kPasses-1; consecutive threads
+        // cover consecutive 16-byte chunks of one row (coalesced reads).
+        constexpr int kRowsPerPass = kGatherThreads / kChunksPerRow;
+        constexpr int kPasses = kChunks / kGatherThreads;
+        const int c = gt % kChunksPerRow;
+        const int q0 = gt / kChunksPerRow;
+        const int64_t col = n0 + 8 * c;
+        const int64_t left = p.N - col;
+        const uint32_t bytes = left >= 8 ? 16u : (left > 0 ? static_cast<uint32_t>(2 * left) : 0u);
+        const uint16_t* bcol = p.B + (bytes ? col : 0);
+        const uint32_t dst_atom = (c >> 3) * (kKTile * 128);  // 64-column atom of chunk c
+        const int cx = c & 7;                                  // chunk within the atom's 128-byte row
+        for (int it = 0; it < nkt; ++it) {
+            const int slot = it % STAGES;
+            const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(smem_u32(&empty_bar[slot]), ph ^ 1u, abort);
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            if (!ok) break;
+            const int kt = kt0 + it;
+            const uint32_t sB = sB0 + slot * Cfg::kBBytes + dst_atom;
+            const uint32_t* sel_row = s_cidx + it * 32;
+            const int32_t kbase = kt * 32 * p.M;
+#pragma unroll
+            for (int u = 0; u < kPasses; ++u) {
+                const int q = u * kRowsPerPass + q0;  // row of the gathered tile: block q/4, slot q%4
+                const uint32_t sel = sel_row[q >> 2];
+                const int32_t kr = kbase + (q >> 2) * p.M + static_cast<int32_t>((sel >> (8 * (q & 3))) & 0xFFu);
+                // 128B swizzle: chunk cx of row q sits at chunk cx ^ (q % 8)
+                cp_async_16(sB + q * 128 + ((cx ^ (q & 7)) << 4), bcol + static_cast<int64_t>(kr) * p.ld_b, bytes);
+            }
+            cp_async_arrive_noinc(smem_u32(&full_bar[slot]));
+        }
+        cp_async_wait_all();  // nothing may still be landing when the CTA exits
     } else {
         const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
         const int trow = tile_row_of_lane<TM>(q, lane);
@@ -348,7 +387,7 @@ cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, dim3 grid, cudaSt
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<grid, kTcThreads, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_e, L.tm_b, p);
+    kern<<<grid, GATHER ? kTcThreadsGather : kTcThreadsTile, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_e, L.tm_b, p);
     return cudaGetLastError();
 }
 
@@ -366,18 +405,22 @@ cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, dim3 grid, cudaStrea
 
 }  // namespace
 
+int tc_gather_max_stages() { return kCidxStages; }
+
 int tc_default_stages(int tile_m, int tile_n) {
     if (tile_m != 64 && tile_m != 128) return 0;
     if (tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 && tile_n != 256) return 0;
     return tc_stages_for(tile_m, tile_n);
 }
 
-cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, int64_t N, void* C, int64_t ld_c, bool c_f32,
-                           float* partial, cudaStream_t stream) {
+cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void* B, int64_t ld_b, int64_t N, void* C,
+                           int64_t ld_c, bool c_f32, float* partial, cudaStream_t stream) {
     if (tc_default_stages(L.tile_m, L.tile_n) == 0 || L.stages != tc_default_stages(L.tile_m, L.tile_n))
         return cudaErrorInvalidValue;
     TcArgs p;
     p.colidx = static_cast<const uint32_t*>(A.colidx);
+    p.B = static_cast<const uint16_t*>(B);
+    p.ld_b = ld_b;
     p.C = C;
     p.ld_c = ld_c;
     p.R = A.R;

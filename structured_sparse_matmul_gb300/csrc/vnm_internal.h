@@ -70,13 +70,17 @@ struct TcLaunch {
 
 // tcgen05 sparse SpMM; with splits > 1 it writes fp32 partials to
 // `partial` ([splits][R][N]) and a second kernel reduces them into C.
-cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, int64_t N, void* C, int64_t ld_c,
-                           bool c_f32, float* partial, cudaStream_t stream);
+cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void* B, int64_t ld_b, int64_t N,
+                           void* C, int64_t ld_c, bool c_f32, float* partial, cudaStream_t stream);
 
 cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, void* C,
                                  int64_t ld_c, bool c_f32, cudaStream_t stream);
 
 // Pipeline depth the tensor-core kernel is built with for a tile (0: no such tile).
 int tc_default_stages(int tile_m, int tile_n);
+
+// Most 128-column stages of the condensed K one CTA covers when it gathers B
+// rows (M > 4); a longer K is split across CTAs.
+int tc_gather_max_stages();
 
 }  // namespace vnm
