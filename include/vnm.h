@@ -195,6 +195,35 @@ vnm_status vnm_spmm_with_plan(vnm_matrix A, const vnm_spmm_plan* plan, const voi
                               size_t workspace_bytes, vnm_stream_t stream);
 
 /*
+ * vnm_spmm for callers that cannot allocate device memory. The paper has no
+ * counterpart: it is a deployment variant of vnm_spmm. Some callers cannot
+ * call cudaMalloc where they need this product (a serving loop whose device
+ * memory is held in full by another caching allocator, or a latency-critical
+ * path that must not take the implicit device synchronisation of
+ * cudaMalloc/cudaFree), and so cannot create a vnm_matrix either. This entry
+ * point takes the compressed arrays of an R x K V:N:M matrix directly (shape
+ * rules and layouts as in vnm_sizes; 16-byte aligned) and computes
+ * C = A . B exactly as vnm_spmm would with an unlimited workspace, allocating
+ * nothing: its split-K partial sums live in a static device array of this
+ * library (8 MiB, plus a 256-byte status region), which every GPU that loads
+ * the library holds until the process exits.
+ *   B, ld_b, N, C, ld_c, c_type: as in vnm_spmm;
+ *   status: optional device pointer to 3 int32 words (first error code,
+ *     detail, error count) that the caller zeroed; kernel-detected errors are
+ *     recorded there. NULL records them in the static status region instead,
+ *     which each call clears first and the caller cannot read.
+ * The first call on a device resolves the static array's address on that
+ * device (cudaGetSymbolAddress); make that first call before any stream
+ * capture. Every call shares the array: calls that overlap on the GPU (for
+ * example on two streams) race on it; stream-ordered calls do not.
+ * Errors: VNM_ERR_INVALID_ARG (shapes, pointers, leading dimensions, or
+ * split-K partials larger than the 8 MiB scratch), VNM_ERR_CUDA.
+ */
+vnm_status vnm_spmm_noalloc(int64_t R, int64_t K, int32_t V, int32_t M, const void* values, const void* meta,
+                            const void* colidx, const void* B, int64_t ld_b, int64_t N, void* C, int64_t ld_c,
+                            vnm_dtype c_type, int32_t* status, vnm_stream_t stream);
+
+/*
  * Synchronise `stream`, then return and clear the first error any kernel
  * of this matrix recorded since the last call (VNM_OK if none).
  * Errors: VNM_ERR_CUDA if the synchronisation itself failed.

@@ -1,0 +1,102 @@
+// vnm_spmm_noalloc: the SpMM for callers that cannot allocate device memory.
+//
+// Some callers cannot call cudaMalloc where they need this product: a
+// serving loop whose device memory is already held in full by another
+// caching allocator, or a latency-critical path that must not take the
+// implicit device synchronisation that cudaMalloc and cudaFree can cause.
+// Such a caller cannot create a vnm_matrix either (vnm_matrix_create
+// allocates a status block), so this entry point takes the compressed
+// arrays directly and keeps its split-K scratch, and its internal status
+// words, in a fixed static device array of this library.
+//
+// The array is resolved with cudaGetSymbolAddress once per device, on the
+// first call made with that device current; that first call should come
+// before any stream capture. In host code the array's name is only a host
+// stand-in, so the kernels are given the resolved device address.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "vnm_internal.h"
+
+namespace {
+
+constexpr size_t kStatusRegionBytes = 256;             // status words (first kStatusBytes of it used)
+constexpr size_t kScratchBytes = size_t(8) << 20;      // 8 MiB of fp32 split-K partial sums
+constexpr int kMaxDevices = 64;
+
+// Holds the status region followed by the split-K scratch. Every call shares
+// it and it keeps the last call's contents; calls that overlap on the GPU
+// (for example on two streams) race on it.
+static __device__ __align__(256) unsigned char g_noalloc_area[kStatusRegionBytes + kScratchBytes];
+
+std::mutex g_mutex;
+unsigned char* g_area_on_device[kMaxDevices] = {};
+
+// Device address of g_noalloc_area on the current device `dev` (null on failure).
+unsigned char* area_address(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_area_on_device[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_area) != cudaSuccess) return nullptr;
+        g_area_on_device[dev] = static_cast<unsigned char*>(p);
+    }
+    return g_area_on_device[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" vnm_status vnm_spmm_noalloc(int64_t R, int64_t K, int32_t V, int32_t M, const void* values,
+                                       const void* meta, const void* colidx, const void* B, int64_t ld_b,
+                                       int64_t N, void* C, int64_t ld_c, vnm_dtype c_type, int32_t* status,
+                                       vnm_stream_t stream) {
+    size_t vb = 0, mb = 0, cb = 0;
+    if (vnm_sizes(R, K, V, M, &vb, &mb, &cb) != VNM_OK) return VNM_ERR_INVALID_ARG;
+    if ((vb && (values == nullptr || !aligned16(values))) || (mb && (meta == nullptr || !aligned16(meta))) ||
+        (cb && (colidx == nullptr || !aligned16(colidx))))
+        return VNM_ERR_INVALID_ARG;
+    if (status != nullptr && (reinterpret_cast<uintptr_t>(status) & 3u) != 0) return VNM_ERR_INVALID_ARG;
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return VNM_ERR_CUDA;
+    unsigned char* area = area_address(dev);
+    if (area == nullptr) return VNM_ERR_CUDA;
+    int sms = 0, major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return VNM_ERR_CUDA;
+
+    // a handle on the stack: it describes the caller's arrays and owns nothing
+    vnm_matrix_s A;
+    A.magic = kVnmMagic;
+    A.R = R;
+    A.K = K;
+    A.V = V;
+    A.M = M;
+    A.values = const_cast<void*>(values);
+    A.meta = const_cast<void*>(meta);
+    A.colidx = const_cast<void*>(colidx);
+    A.device = dev;
+    A.sm_count = sms;
+    A.cc_major = major;
+    A.cc_minor = minor;
+    A.status = status != nullptr ? status : reinterpret_cast<int*>(area);
+
+    // the plan vnm_spmm makes with unlimited workspace; its split-K partials
+    // must fit the static scratch
+    vnm_spmm_plan plan;
+    vnm_status st = vnm_spmm_plan_query(&A, B, ld_b, N, c_type, SIZE_MAX / 2, &plan);
+    if (st != VNM_OK) return st;
+    size_t need = 0;
+    if (plan.path == VNM_PATH_TC && plan.splits > 1)
+        need = static_cast<size_t>(plan.splits) * static_cast<size_t>(R) * static_cast<size_t>(N) * sizeof(float);
+    if (need > kScratchBytes) return VNM_ERR_INVALID_ARG;  // partials would exceed the 8 MiB static scratch
+
+    // the internal status words must start at zero for this call
+    if (status == nullptr && cudaMemsetAsync(area, 0, kStatusBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return VNM_ERR_CUDA;
+    return vnm_spmm(&A, B, ld_b, N, C, ld_c, c_type, need ? area + kStatusRegionBytes : nullptr, need, stream);
+}

@@ -65,9 +65,10 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.vnm_spmm_plan_query.argtypes = [p, p, i64, i64, ctypes.c_int, sz, ctypes.POINTER(vnm_spmm_plan)]
     L.vnm_spmm_with_plan.argtypes = [p, ctypes.POINTER(vnm_spmm_plan), p, i64, i64, p, i64, ctypes.c_int, p, sz, p]
     L.vnm_get_status.argtypes = [p, p]
+    L.vnm_spmm_noalloc.argtypes = [i64, i64, i32, i32, p, p, p, p, i64, i64, p, i64, ctypes.c_int, p, p]
     for name in ("vnm_sizes", "vnm_matrix_create", "vnm_matrix_destroy", "vnm_compress", "vnm_decompress",
                  "vnm_spmm", "vnm_spmm_workspace_size", "vnm_spmm_plan_query", "vnm_spmm_with_plan",
-                 "vnm_get_status"):
+                 "vnm_get_status", "vnm_spmm_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -247,3 +248,29 @@ def workspace_for(A: VnmMatrix, N: int, device=None) -> Optional[torch.Tensor]:
         return None
     dev = device if device is not None else A.values.device
     return torch.empty(nbytes // 4 + 64, dtype=torch.float32, device=dev)
+
+
+def vnm_spmm_noalloc(R: int, K: int, V: int, M: int, values: torch.Tensor, meta: torch.Tensor,
+                     colidx: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+                     status: Optional[torch.Tensor] = None, stream=None) -> None:
+    """C = A . B from the compressed arrays, without any device allocation.
+
+    For callers that cannot call cudaMalloc (memory held in full by another
+    allocator, or a path that must not synchronise the device): the split-K
+    scratch is a static 8 MiB device array inside libvnm. ``status`` is an
+    optional int32 CUDA tensor of 3 zeroed words that receives kernel errors.
+    """
+    if B.dtype != torch.float16 or not B.is_cuda or B.dim() != 2 or B.shape[0] != K:
+        raise ValueError("B must be a CUDA fp16 tensor of shape (K, N)")
+    N = int(B.shape[1])
+    if not C.is_cuda or tuple(C.shape) != (R, N):
+        raise ValueError("C must be a CUDA tensor of shape (R, N)")
+    sp = None
+    if status is not None:
+        if status.dtype != torch.int32 or not status.is_cuda or status.numel() < 3:
+            raise ValueError("status must be a CUDA int32 tensor of at least 3 words")
+        sp = status.data_ptr()
+    _check(lib().vnm_spmm_noalloc(R, K, V, M, values.data_ptr() or None, meta.data_ptr() or None,
+                                  colidx.data_ptr() or None, B.data_ptr() or None, _rowmajor(B, "B"), N,
+                                  C.data_ptr() or None, _rowmajor(C, "C"), _c_type(C), sp, _stream_ptr(stream)),
+           "vnm_spmm_noalloc")
