@@ -480,6 +480,225 @@ __global__ void __launch_bounds__(kCompressThreads) compress_stream_kernel(const
     if (threadIdx.x == 0 && bad) record_error(p.status, VNM_ERR_NONFINITE, 3);
 }
 
+// Half `idx` (0 .. 2*NW-1) of a block row held as NW 32-bit words.
+template <int NW>
+__device__ __forceinline__ uint16_t half_at(const uint32_t (&w)[NW], int idx) {
+    // masked OR over the words (keeps w in registers: no indexed access)
+    uint32_t x = 0;
+#pragma unroll
+    for (int u = 0; u < NW; ++u) x |= w[u] & (0u - static_cast<uint32_t>((idx >> 1) == u));
+    return static_cast<uint16_t>((idx & 1) ? (x >> 16) : (x & 0xFFFFu));
+}
+
+__device__ __forceinline__ float shfl_any(float v, int src) { return __shfl_sync(0xFFFFFFFFu, v, src); }
+__device__ __forceinline__ uint64_t shfl_any(uint64_t v, int src) {
+    const uint32_t lo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), src);
+    const uint32_t hi = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v >> 32), src);
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Lane c < n of a warp holds the score of column c. Column order: larger
+// score first, lower index first on equal scores. Returns the bit mask of
+// the 4 leading columns and puts this lane's place in that order in *rank
+// (32 for lanes >= n).
+template <typename T>
+__device__ __forceinline__ uint32_t warp_top4_mask(T score, int n, int lane, int* rank) {
+    int rk = 0;
+    for (int c = 0; c < n; ++c) {
+        const T o = shfl_any(score, c);
+        rk += (o > score) || (o == score && c < lane);
+    }
+    *rank = lane < n ? rk : 32;
+    return __ballot_sync(0xFFFFFFFFu, lane < n && rk < 4);
+}
+
+// The 4 lowest set bits of `mask` as ascending bytes of a word.
+__device__ __forceinline__ uint32_t mask_to_cols(uint32_t mask) {
+    uint32_t sel = 0;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int c = __ffs(mask) - 1;
+        sel |= static_cast<uint32_t>(c & 0xFF) << (8 * q);
+        mask &= mask - 1;
+    }
+    return sel;
+}
+
+constexpr int kColsBlocks = 8;   // blocks per CTA: consecutive blocks of one block row
+constexpr int kColsWarps = 8;
+
+// Compress for M in {8, 16, 32}. A CTA owns blocks (i, j0 .. j0+7) over all
+// V rows. Lane (b, g) = (lane % 8, lane / 8) of warp w handles block j0+b in
+// rows r = 4w + g + 32t, so each row a warp reads is 8 adjacent block rows
+// (coalesced 16-byte loads). Pass 1: fp32 column sums of |w|, combined over
+// g by shuffles and over warps in shared memory. Ranking: warp w ranks block
+// j0+w with lane c holding column c; the fp32 ranking is the exact one
+// whenever the gap between the 4th and 5th sums is beyond the fp32 error
+// bound of such a sum (relative V * 2^-24; 2.5 x that is required), else that
+// warp re-sums the block's columns exactly as integers (units of 2^-24).
+// Pass 2: keep 2 of the 4 selected values per row, write values and m-index
+// bytes (two blocks per byte, paired by a shuffle). With RPL > 0 (V <= 32 *
+// RPL) the rows stay in registers between the passes; with RPL == 0 pass 2
+// re-reads them (L1-resident: a CTA's rows are V * 16 * M bytes).
+template <int MB, int RPL>
+__global__ void __launch_bounds__(kColsWarps * 32, 2) compress_cols_kernel(const CompressArgs p) {
+    constexpr int kVec = MB / 8;     // 16-byte chunks per block row
+    constexpr int kNW = MB / 2;      // 32-bit words per block row
+    constexpr int kRowStep = 4 * kColsWarps;
+    __shared__ float s_sum[kColsWarps][kColsBlocks][MB];
+    __shared__ uint32_t s_sel[kColsBlocks];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = lane & 7, g = lane >> 3;
+    const int64_t cpr = (p.nblk + kColsBlocks - 1) / kColsBlocks;  // CTAs per block row
+    const int64_t i = blockIdx.x / cpr;
+    const int64_t j0 = (blockIdx.x % cpr) * kColsBlocks;
+    const int64_t j = j0 + b;
+    const bool valid = j < p.nblk;
+    const int V = p.V;
+    const int64_t ld = p.ld_w;
+    const uint16_t* Wrow = p.W + (i * V) * ld;  // row 0 of block row i
+    const uint16_t* Wb = Wrow + (valid ? j : 0) * MB;
+
+    // ---- pass 1: partial column sums
+    float sum[MB];
+#pragma unroll
+    for (int c = 0; c < MB; ++c) sum[c] = 0.f;
+    uint4 x[RPL > 0 ? RPL : 1][kVec];
+    auto add_pair = [&](uint32_t w, int c) {  // |w| of two fp16 (sign bits cleared) into sum[c], sum[c+1]
+        const uint32_t m = w & 0x7FFF7FFFu;
+        sum[c] += __half2float(__ushort_as_half(static_cast<unsigned short>(m & 0xFFFFu)));
+        sum[c + 1] += __half2float(__ushort_as_half(static_cast<unsigned short>(m >> 16)));
+    };
+    auto accumulate = [&](const uint4 (&xr)[kVec]) {
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+            add_pair(xr[v].x, 8 * v);
+            add_pair(xr[v].y, 8 * v + 2);
+            add_pair(xr[v].z, 8 * v + 4);
+            add_pair(xr[v].w, 8 * v + 6);
+        }
+    };
+    if constexpr (RPL > 0) {
+#pragma unroll
+        for (int t = 0; t < RPL; ++t) {
+            const int r = 4 * warp + g + kRowStep * t;
+            const bool act = valid && r < V;
+#pragma unroll
+            for (int v = 0; v < kVec; ++v)
+                x[t][v] = act ? __ldg(reinterpret_cast<const uint4*>(Wb + r * ld) + v) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int t = 0; t < RPL; ++t) accumulate(x[t]);
+    } else {
+#pragma unroll 2
+        for (int r = 4 * warp + g; r < V; r += kRowStep) {
+            if (!valid) break;
+#pragma unroll
+            for (int v = 0; v < kVec; ++v) x[0][v] = __ldg(reinterpret_cast<const uint4*>(Wb + r * ld) + v);
+            accumulate(x[0]);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < MB; ++c) {
+        sum[c] += __shfl_xor_sync(0xFFFFFFFFu, sum[c], 8);
+        sum[c] += __shfl_xor_sync(0xFFFFFFFFu, sum[c], 16);
+    }
+    if (g == 0) {
+#pragma unroll
+        for (int c = 0; c < MB; ++c) s_sum[warp][b][c] = sum[c];
+    }
+    __syncthreads();
+
+    // ---- ranking: warp w ranks block j0 + w (warp-uniform condition)
+    if (j0 + warp < p.nblk) {
+        const int blk = warp;
+        float s = -1.f;  // below every column's sum
+        if (lane < MB) {
+            s = 0.f;
+#pragma unroll
+            for (int w = 0; w < kColsWarps; ++w) s += s_sum[w][blk][lane];
+        }
+        const bool any_bad = __any_sync(0xFFFFFFFFu, lane < MB && !(s <= 3.4e38f));
+        int rank;
+        uint32_t mask = warp_top4_mask(s, MB, lane, &rank);
+        const int l3 = __ffs(__ballot_sync(0xFFFFFFFFu, rank == 3)) - 1;
+        const int l4 = __ffs(__ballot_sync(0xFFFFFFFFu, rank == 4)) - 1;
+        const float v3 = __shfl_sync(0xFFFFFFFFu, s, l3 & 31);
+        const float v4 = __shfl_sync(0xFFFFFFFFu, s, l4 & 31);
+        const bool safe = !any_bad && l3 >= 0 && l4 >= 0 &&
+                          (v3 - v4 > 2.5f * static_cast<float>(V) * 5.9604645e-8f * v3);
+        if (!safe) {
+            uint64_t e = 0;
+            if (lane < MB) {
+                const uint16_t* col = Wrow + (j0 + blk) * MB + lane;
+                for (int r = 0; r < V; ++r) e += mag_units(col[r * ld]);
+            }
+            mask = warp_top4_mask(e, MB, lane, &rank);
+        }
+        const uint32_t sel = mask_to_cols(mask);
+        if (lane == 0) {
+            s_sel[blk] = sel;
+            p.colidx[i * p.nblk + j0 + blk] = sel;
+            if (any_bad) record_error(p.status, VNM_ERR_NONFINITE, 5);
+        }
+    }
+    __syncthreads();
+
+    // ---- pass 2: 2 of the 4 selected values per row
+    const uint32_t sel = s_sel[b];
+    const int col0 = sel & 0xFF, col1 = (sel >> 8) & 0xFF, col2 = (sel >> 16) & 0xFF, col3 = sel >> 24;
+    const bool pair_lo = (j & 1) == 0;
+    auto emit = [&](const uint4 (&xr)[kVec], int r, bool act) {
+        uint32_t w[kNW];
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+            w[4 * v] = xr[v].x;
+            w[4 * v + 1] = xr[v].y;
+            w[4 * v + 2] = xr[v].z;
+            w[4 * v + 3] = xr[v].w;
+        }
+        const uint16_t a[4] = {half_at<kNW>(w, col0), half_at<kNW>(w, col1), half_at<kNW>(w, col2),
+                               half_at<kNW>(w, col3)};
+        uint16_t v0, v1;
+        uint32_t code = keep2of4(a, v0, v1);
+        if (!act) code = 0;
+        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, code, 1);  // the neighbouring block's code
+        if (act) {
+            const int64_t row = i * V + r;
+            *reinterpret_cast<uint32_t*>(p.values + row * (2 * p.nblk) + 2 * j) =
+                static_cast<uint32_t>(v0) | (static_cast<uint32_t>(v1) << 16);
+            if (pair_lo) p.meta[row * p.mpitch + (j >> 1)] = static_cast<uint8_t>(code | (other << 4));
+        }
+    };
+    if constexpr (RPL > 0) {
+#pragma unroll
+        for (int t = 0; t < RPL; ++t) {
+            const int r = 4 * warp + g + kRowStep * t;
+            emit(x[t], r, valid && r < V);
+        }
+    } else {
+        // r0 is uniform over the warp, so every lane reaches the shuffle in emit
+        for (int r0 = 4 * warp; r0 < V; r0 += kRowStep) {
+            const int r = r0 + g;
+            const bool act = valid && r < V;
+#pragma unroll
+            for (int v = 0; v < kVec; ++v)
+                x[0][v] = act ? __ldg(reinterpret_cast<const uint4*>(Wb + r * ld) + v) : make_uint4(0, 0, 0, 0);
+            emit(x[0], r, act);
+        }
+    }
+}
+
+template <int MB>
+void launch_cols(const CompressArgs& p, unsigned ctas, cudaStream_t stream) {
+    const int V = p.V;
+    const unsigned threads = kColsWarps * 32;
+    if (V <= 32) compress_cols_kernel<MB, 1><<<ctas, threads, 0, stream>>>(p);
+    else if (V <= 64) compress_cols_kernel<MB, 2><<<ctas, threads, 0, stream>>>(p);
+    else if (V <= 128) compress_cols_kernel<MB, 4><<<ctas, threads, 0, stream>>>(p);
+    else compress_cols_kernel<MB, 0><<<ctas, threads, 0, stream>>>(p);
+}
+
 // M == 4: column-loc is the identity, so prune-and-encode is the 2:4 step
 // alone, on each group of 4 consecutive weights of a row. One thread turns
 // 16 consecutive weights (32 bytes) into 8 values (16 bytes) and 4 nibbles
@@ -569,6 +788,14 @@ cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, 
         const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((chunks + kM4Threads - 1) / kM4Threads,
                                                                       static_cast<int64_t>(A.sm_count) * 8));
         compress_m4_kernel<<<static_cast<unsigned>(blocks), kM4Threads, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+    // M in {8, 16, 32}: eight blocks x V rows per CTA, no staging
+    if ((A.M == 8 || A.M == 16 || A.M == 32) && reinterpret_cast<uintptr_t>(W) % 16 == 0 && ld_w % 8 == 0) {
+        const int64_t ctas = (A.R / A.V) * ((p.nblk + kColsBlocks - 1) / kColsBlocks);
+        if (A.M == 8) launch_cols<8>(p, static_cast<unsigned>(ctas), stream);
+        else if (A.M == 16) launch_cols<16>(p, static_cast<unsigned>(ctas), stream);
+        else launch_cols<32>(p, static_cast<unsigned>(ctas), stream);
         return cudaGetLastError();
     }
     // tile width: an even number of blocks, as many as fit the budget

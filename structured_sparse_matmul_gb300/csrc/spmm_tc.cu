@@ -49,9 +49,7 @@
 namespace vnm {
 namespace {
 
-constexpr int kTcThreadsTile = 192;    // warps 0-5
-constexpr int kTcThreadsGather = 320;  // warps 0-5 plus 4 gather warps
-constexpr int kGatherThreads = 128;
+constexpr int kTcThreadsTile = 192;    // warps 0-5; gathering CTAs add gather warps after them
 constexpr int kKTile = 128;        // condensed K per stage = 4 MMAs of K = 32
 constexpr int kValsPerKTile = 64;  // stored values per row per stage (128 bytes)
 constexpr int kMetaSlotCols = 8;   // TMEM columns between consecutive MMAs' m-index words
@@ -100,6 +98,19 @@ struct TcCfg {
     static_assert(TM == 64 || TM == 128, "MMA M");
 };
 
+// Gather threads of a gathering CTA: the gathered B tile needs many 16-byte
+// copies in flight per SM (one CTA per SM), and a 64-row tile has half the
+// A bytes per gathered B byte, so it takes twice the gather warps; never
+// more threads than 16-byte chunks per stage (kKTile * BN / 8).
+__host__ __device__ constexpr int gather_threads(int tm, int bn) {
+    return (tm == 64 ? 512 : 256) < kKTile * bn / 8 ? (tm == 64 ? 512 : 256) : kKTile * bn / 8;
+}
+
+template <int TM, int BN, bool GATHER>
+__host__ __device__ constexpr int tc_threads() {
+    return kTcThreadsTile + (GATHER ? gather_threads(TM, BN) : 0);
+}
+
 // TMEM lane quarter q (warp % 4), lane l -> row of the tile (or -1).
 template <int TM>
 __device__ __forceinline__ int tile_row_of_lane(int q, int l) {
@@ -108,11 +119,12 @@ __device__ __forceinline__ int tile_row_of_lane(int q, int l) {
 }
 
 template <int TM, int BN, bool GATHER>
-__global__ void __launch_bounds__(GATHER ? kTcThreadsGather : kTcThreadsTile, 1)
+__global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_e,
                    const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
     using Cfg = TcCfg<TM, BN>;
     constexpr int STAGES = Cfg::kStages;
+    constexpr int kGatherThreads = gather_threads(TM, BN);
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];   // TMA bytes landed
     __shared__ __align__(8) uint64_t meta_bar[STAGES];   // m-indices written to TMEM (4 warps)
@@ -387,7 +399,7 @@ cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, dim3 grid, cudaSt
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    kern<<<grid, GATHER ? kTcThreadsGather : kTcThreadsTile, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_e, L.tm_b, p);
+    kern<<<grid, tc_threads<TM, BN, GATHER>(), Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_e, L.tm_b, p);
     return cudaGetLastError();
 }
 

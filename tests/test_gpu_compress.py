@@ -44,6 +44,10 @@ SHAPES = [
     (4, 4096, 1, 4),
     (8, 64, 8, 64),
     (256, 4096, 256, 8),
+    (64, 296, 16, 8),       # M in {8, 16, 32} with an odd number of blocks per row
+    (32, 80, 4, 16),
+    (36, 96, 12, 32),
+    (384, 640, 192, 16),    # V above 128: the two-pass (re-read) variant
 ]
 
 
@@ -63,7 +67,8 @@ def test_padded_rows(R, K, V, M, ld):
     assert_compress_bitexact(A, W, V, M)
 
 
-@pytest.mark.parametrize("R,K,V,M", [(32, 96, 4, 6), (64, 512, 16, 8), (16, 256, 8, 16), (16, 768, 16, 12)])
+@pytest.mark.parametrize("R,K,V,M", [(32, 96, 4, 6), (64, 512, 16, 8), (16, 256, 8, 16), (16, 768, 16, 12),
+                                     (64, 1056, 32, 32), (128, 72, 128, 8), (256, 96, 256, 16)])
 def test_tie_heavy(R, K, V, M):
     W = inputs.choice_f16((R, K), 13, M, [0, 0.5, -0.5, 1, -1, 0.0])
     A, st = gpu_compress(W, V, M)
@@ -83,7 +88,7 @@ def test_subnormals_and_signed_zeros():
 
 @pytest.mark.parametrize("bad", [np.inf, -np.inf, np.nan])
 def test_nonfinite_reported(bad):
-    for (R, K, V, M) in ((64, 256, 16, 8), (128, 512, 128, 256)):
+    for (R, K, V, M) in ((64, 256, 16, 8), (128, 512, 128, 256), (256, 512, 128, 32), (256, 128, 256, 8)):
         W = inputs.normal_f16((R, K), 15, 0, 0.02)
         W[R // 2, K - 3] = bad
         A, st = gpu_compress(W, V, M)
