@@ -219,6 +219,48 @@ def run_reference(args, case):
     print(json.dumps(line), flush=True)
 
 
+# Sources of each profiled kernel: a summary's DRAM traffic is used only
+# while these files are unchanged since the capture.
+KERNEL_SOURCES = {
+    "spmm_tc_kernel": ["spmm_tc.cu", "vnm_ptx.cuh", "vnm_internal.h"],
+    "compress": ["compress.cu", "vnm_internal.h"],
+}
+
+
+def sources_sha256(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "structured_sparse_matmul_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes (read + write) per launch of `kernel` on `workload` from the
+    ncu summary under profiles/, or None when there is none or the kernel's
+    sources changed after it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as fh:
+        for line in fh:
+            if ":" in line and not line.startswith(" "):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    try:
+        if fields.get("source_sha256") != sources_sha256(kernel):
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError, OSError):
+        return None
+
+
+def workload_tag(case) -> str:
+    return f"{case.R}x{case.K}x{case.N}_v{case.V}m{case.M}"
+
+
 def config_of(case, l2_note):
     c = {"workload": (f"V:N:M magnitude compress + SpMM, A {case.R}x{case.K} fp16 N(0,0.02) {case.V}:2:{case.M} "
                       f"({100 * (1 - 2 / case.M):.1f}% sparse), B {case.K}x{case.N} fp16 N(0,1), "
@@ -391,7 +433,8 @@ def main():
                 "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                 "per_launch": f"{comp_bytes} bytes (dense W read, compressed arrays written)"}
     roof["peak_source"] = f"{peak_src} ({'MEASURED_PEAKS.json' if peak_src == 'measured' else 'recipe fallback'})"
-    roof["traffic"] = None
+    roof["traffic"] = profiled_traffic("spmm_tc_kernel" if roof["kernel"].startswith("vnm_spmm") else "compress",
+                                       workload_tag(case))
 
     # end to end: host buffers, copies inside the timed region
     e2e = None
