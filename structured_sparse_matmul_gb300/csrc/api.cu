@@ -116,18 +116,7 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     if (tiles < A.sm_count) splits = std::min<int64_t>(num_kt, std::max<int64_t>(1, A.sm_count / tiles));
     const int64_t per_split = A.R * N * static_cast<int64_t>(sizeof(float));
     if (splits > 1) splits = std::min<int64_t>(splits, static_cast<int64_t>(workspace_bytes) / per_split);
-    // a gathering CTA covers at most tc_gather_max_stages() stages
-    const int64_t min_splits = A.M > 4 ? ceil_div(num_kt, vnm::tc_gather_max_stages()) : 1;
     splits = std::max<int64_t>(1, splits);
-    if (splits < min_splits) {
-        if (min_splits * per_split > static_cast<int64_t>(workspace_bytes)) {
-            pl.path = VNM_PATH_SIMT;  // such a long K needs split-K partials; no workspace for them
-            pl.tile_m = pl.tile_n = pl.stages = 0;
-            pl.splits = 1;
-            return pl;
-        }
-        splits = min_splits;
-    }
     pl.splits = static_cast<int32_t>(std::max<int64_t>(1, splits));
     return pl;
 }
@@ -150,8 +139,6 @@ vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void
     if (depth == 0 || (pl.stages != 0 && pl.stages != depth)) return VNM_ERR_UNSUPPORTED;
     if (pl.splits < 1) return VNM_ERR_INVALID_ARG;
     const int s = effective_splits(A, pl.splits);
-    const int num_kt = static_cast<int>((A.K / A.M) / 32);
-    if (A.M > 4 && ceil_div(num_kt, s) > vnm::tc_gather_max_stages()) return VNM_ERR_UNSUPPORTED;
     if (s > 1) {
         const size_t need = static_cast<size_t>(s) * A.R * N * sizeof(float);
         if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)) return VNM_ERR_INVALID_ARG;
@@ -173,10 +160,11 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         L.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n);
         L.splits = effective_splits(*A, pl.splits);
         L.gather = A->M > 4;
+        L.sm_count = A->sm_count;
         const uint64_t vpr = static_cast<uint64_t>(values_per_row(A->K, A->M));
         const uint64_t mp = static_cast<uint64_t>(meta_pitch(A->K, A->M));
-        bool ok = encode_2d(&L.tm_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A->values, vpr, A->R, vpr * 2, 16,
-                            static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_32B);
+        bool ok = encode_2d(&L.tm_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A->values, vpr, A->R, vpr * 2, 64,
+                            static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_128B);
         ok = ok && encode_2d(&L.tm_e, CU_TENSOR_MAP_DATA_TYPE_UINT32, A->meta, mp / 4, A->R, mp, 4,
                              static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_NONE);
         ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, A->K, ld_b * 2, 64, L.gather ? 1 : 128,

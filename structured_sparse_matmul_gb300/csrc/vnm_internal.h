@@ -55,17 +55,18 @@ cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b,
 // column-loc words, at most 8.
 __host__ __device__ constexpr int tc_stages_for(int tile_m, int tile_n) {
     const int stage = ((tile_n + 63) / 64) * 128 * 128 + tile_m * 128 + tile_m * 16;
-    const int budget = 227 * 1024 - 8 * 1024 - 2 * 1024;  // minus column-loc words, barriers, alignment
+    const int budget = 227 * 1024 - 10 * 1024;  // minus barriers, alignment slack and headroom
     const int s = budget / stage;
     return s > 8 ? 8 : s;
 }
 
 struct TcLaunch {
-    CUtensorMap tm_a;   // values, box {16, tile_m}: one MMA k-step, 32B swizzle
+    CUtensorMap tm_a;   // values, box {64, tile_m}: one stage (4 MMA k-steps), 128B swizzle
     CUtensorMap tm_e;   // m-indices as u32 words, box {4, tile_m}, no swizzle
     CUtensorMap tm_b;   // B, box {64, 128} (tile) or {64, 1} (gather4), 128B swizzle
     int tile_m, tile_n, stages, splits;
     bool gather;        // M > 4: rows of B selected through colidx
+    int sm_count;       // persistent grid: at most sm_count x resident CTAs per SM
 };
 
 // tcgen05 sparse SpMM; with splits > 1 it writes fp32 partials to
@@ -79,8 +80,5 @@ cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, in
 // Pipeline depth the tensor-core kernel is built with for a tile (0: no such tile).
 int tc_default_stages(int tile_m, int tile_n);
 
-// Most 128-column stages of the condensed K one CTA covers when it gathers B
-// rows (M > 4); a longer K is split across CTAs.
-int tc_gather_max_stages();
 
 }  // namespace vnm

@@ -73,6 +73,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     return false;
 }
 
+// Warp-wide bounded wait: every lane polls (one instruction per poll for
+// the warp) and the lanes agree by a vote, which keeps the shared-memory
+// pipe free of the lane-0-then-shuffle pattern.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort) {
+    const bool ok = mbar_wait(bar, parity, abort);
+    return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // Same bounded wait, but it ignores the abort flag: used while draining
 // copies and MMAs that were already issued, before the CTA exits.
 __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
@@ -223,6 +231,10 @@ __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Each thread of the warp writes 4 consecutive 32-bit columns of its lane.
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t a) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c,
                                                   uint32_t d) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a),
