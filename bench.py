@@ -222,7 +222,7 @@ def run_reference(args, case):
 # Sources of each profiled kernel: a summary's DRAM traffic is used only
 # while these files are unchanged since the capture.
 KERNEL_SOURCES = {
-    "spmm_tc_kernel": ["spmm_tc.cu", "vnm_ptx.cuh", "vnm_internal.h"],
+    "spmm_tc_kernel": ["spmm_tc.cu", "vnm_ptx.cuh", "vnm_internal.h", "api.cu"],  # api.cu: the tile plan
     "compress": ["compress.cu", "vnm_internal.h"],
 }
 

@@ -104,7 +104,9 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     }
     pl.path = VNM_PATH_TC;
     pl.tile_m = tc_tile_m_ok(A, 128) ? 128 : 64;
-    pl.tile_n = N >= 128 ? 128 : static_cast<int32_t>(ceil_div(N, 16) * 16);
+    // gathering (M > 4): 256-column tiles when N allows (twice the MMA work per
+    // stage for the same per-stage costs); plain 2:4: 128 (finer waves)
+    pl.tile_n = (A.M > 4 && N >= 256) ? 256 : N >= 128 ? 128 : static_cast<int32_t>(ceil_div(N, 16) * 16);
     if (pl.tile_n > 64 && pl.tile_n < 128) pl.tile_n = 128;
     if (pl.tile_n > 32 && pl.tile_n < 64) pl.tile_n = 64;
     if (pl.tile_n > 16 && pl.tile_n < 32) pl.tile_n = 32;

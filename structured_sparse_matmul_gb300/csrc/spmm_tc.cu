@@ -66,6 +66,13 @@ constexpr int kKTile = 128;        // condensed K per stage = 4 MMAs of K = 32
 constexpr int kValsPerKTile = 64;  // stored values per row per stage (128 bytes)
 constexpr int kMetaSlotCols = 8;   // TMEM columns between consecutive MMAs' m-index words
 constexpr int kMetaStageCols = 4 * kMetaSlotCols;
+// Sleep between polls of a barrier, per role (ns): the MMA thread polls
+// flat out; the others park so that ~20 waiting warps do not take the issue
+// slots of the ones doing work. The epilogue waits a whole tile.
+constexpr uint32_t kSleepProducer = 32;
+constexpr uint32_t kSleepMeta = 64;
+constexpr uint32_t kSleepGather = 64;
+constexpr uint32_t kSleepEpilogue = 256;
 // m-index word of a row that lies beyond R: slots (0, 1) in all 8 groups
 constexpr uint32_t kPadMeta = 0x44444444u;
 
@@ -227,7 +234,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             for (int k = 0; k < g.nkt; ++k, ++it) {
                 const int slot = it % STAGES;
                 const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
-                const bool ok = mbar_wait_warp(smem_u32(&empty_bar[slot]), ph ^ 1u, abort);
+                const bool ok = mbar_wait_warp(smem_u32(&empty_bar[slot]), ph ^ 1u, abort, kSleepProducer);
                 if (!ok) {
                     run = false;
                     break;
@@ -325,7 +332,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             for (int k = 0; k < g.nkt; ++k, ++it) {
                 const int slot = it % STAGES;
                 const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
-                const bool ok = mbar_wait_warp(smem_u32(&ae_bar[slot]), ph, abort);
+                const bool ok = mbar_wait_warp(smem_u32(&ae_bar[slot]), ph, abort, kSleepMeta);
                 if (!ok) {
                     run = false;
                     break;
@@ -364,7 +371,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             const TileGeom g = tile_geom<TM, BN>(p, t);
             const int buf = ti % ACC;
             const uint32_t use = static_cast<uint32_t>(ti / ACC) & 1u;
-            const bool ok = mbar_wait_warp(smem_u32(&accf_bar[buf]), use, abort) && !*abort;
+            const bool ok = mbar_wait_warp(smem_u32(&accf_bar[buf]), use, abort, kSleepEpilogue) && !*abort;
             if (!ok) break;
             tc_fence_after_sync();
             const int64_t row = trow >= 0 ? g.m0 + trow : p.R;
@@ -483,7 +490,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
 
                 const int slot = it % STAGES;
                 const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
-                const bool ok = mbar_wait_warp(smem_u32(&empty_bar[slot]), ph ^ 1u, abort);
+                const bool ok = mbar_wait_warp(smem_u32(&empty_bar[slot]), ph ^ 1u, abort, kSleepGather);
                 if (!ok) {
                     stop = true;
                     break;

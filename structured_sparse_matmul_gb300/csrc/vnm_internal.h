@@ -55,7 +55,7 @@ cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b,
 // column-loc words, at most 8.
 __host__ __device__ constexpr int tc_stages_for(int tile_m, int tile_n) {
     const int stage = ((tile_n + 63) / 64) * 128 * 128 + tile_m * 128 + tile_m * 16;
-    const int budget = 227 * 1024 - 10 * 1024;  // minus barriers, alignment slack and headroom
+    const int budget = 227 * 1024 - 2 * 1024;  // minus 1 KB alignment slack and 1 KB for barriers
     const int s = budget / stage;
     return s > 8 ? 8 : s;
 }

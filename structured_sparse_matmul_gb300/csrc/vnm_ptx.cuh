@@ -59,10 +59,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // Returns false (without completing) if `*abort` is raised by another role
 // or if the time / poll limit passes; in the latter case it raises `*abort`
 // itself so that every role of the CTA winds down.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// `sleep_ns` > 0 parks the warp between polls, leaving its issue slots to
+// the other roles of the CTA (waits off the critical path).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
     for (uint32_t it = 1; it < kWaitLimitPolls; ++it) {
+        if (sleep_ns) __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0u) {
             if (*abort) return false;
@@ -76,8 +80,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
 // Warp-wide bounded wait: every lane polls (one instruction per poll for
 // the warp) and the lanes agree by a vote, which keeps the shared-memory
 // pipe free of the lane-0-then-shuffle pattern.
-__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort) {
-    const bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               uint32_t sleep_ns = 0) {
+    const bool ok = mbar_wait(bar, parity, abort, sleep_ns);
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
