@@ -375,13 +375,10 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             if (!ok) break;
             tc_fence_after_sync();
             const int64_t row = trow >= 0 ? g.m0 + trow : p.R;
-#pragma unroll 1
-            for (int c = 0; c < BN; c += 16) {
-                uint32_t v[16];
-                tmem_ld_32x32b_x16(tmem_acc + buf * BN + lane_addr + c, v);
-                tmem_wait_ld();
+            // one 16-column chunk of this thread's row: fp32 partials, fp32 or fp16 C
+            auto store16 = [&](const uint32_t (&v)[16], int c) {
                 const int64_t col = g.n0 + c;
-                if (row >= p.R || col >= p.N) continue;
+                if (row >= p.R || col >= p.N) return;
                 const bool full = col + 16 <= p.N;
                 if (p.partial != nullptr) {
                     float* dst = p.partial + (static_cast<int64_t>(g.split) * p.R + row) * p.N + col;
@@ -417,6 +414,17 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                             dst[u] = __float2half_rn(__uint_as_float(v[u]));
                     }
                 }
+            };
+            // two TMEM loads in flight per wait
+            constexpr int kEpiStep = BN >= 32 ? 32 : 16;
+#pragma unroll 1
+            for (int c = 0; c < BN; c += kEpiStep) {
+                uint32_t v0[16], v1[16];
+                tmem_ld_32x32b_x16(tmem_acc + buf * BN + lane_addr + c, v0);
+                if (kEpiStep == 32) tmem_ld_32x32b_x16(tmem_acc + buf * BN + lane_addr + c + 16, v1);
+                tmem_wait_ld();
+                store16(v0, c);
+                if (kEpiStep == 32) store16(v1, c + 16);
             }
             // this warp's lanes of the accumulator are in registers: release it
             tc_fence_before_sync();
@@ -431,7 +439,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         const int gt = threadIdx.x - kTcWarpsFixed * 32;
         // Fixed thread -> (chunk, row) map: thread gt copies chunk c of the
         // kPasses consecutive rows q = q0 * kPasses + u (whole blocks of 4
-        // rows when kPasses >= 4, so a few column-loc words serve them);
+        // rows when kPasses >= 4, so one column-loc word serves 4 rows);
         // consecutive threads cover consecutive 16-byte chunks of a row
         // (coalesced reads).
         constexpr int kPasses = kChunks / kGatherThreads;
@@ -502,18 +510,20 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                 const uint16_t* bcol = p.B + (bytes ? col : 0);
                 const uint32_t sB = sB0 + slot * Cfg::kBBytes + dst_atom;
                 const int64_t kbase = static_cast<int64_t>(g.kt0 + cur.k) * 32 * p.M;
-                uint32_t wsel[kWords];
+                constexpr int kRowsPerWord = kPasses >= 4 ? 4 : kPasses;
+#pragma unroll 2
+                for (int wi = 0; wi < kWords; ++wi) {
+                    // the column-loc word of the block holding rows q0*kPasses + 4*wi ..
+                    const uint32_t sel = __shfl_sync(0xFFFFFFFFu, word, ((q0 * kPasses) >> 2) + wi);
 #pragma unroll
-                for (int j = 0; j < kWords; ++j) wsel[j] = __shfl_sync(0xFFFFFFFFu, word, ((q0 * kPasses) >> 2) + j);
-#pragma unroll
-                for (int u = 0; u < kPasses; ++u) {
-                    const int qq = q0 * kPasses + u;  // row of the gathered tile: block qq/4, slot qq%4
-                    const uint32_t sel = wsel[kPasses >= 4 ? (u >> 2) : 0];
-                    // column-loc byte, clamped so that a corrupt array cannot address past K
-                    const uint32_t cb = min((sel >> (8 * (qq & 3))) & 0xFFu, static_cast<uint32_t>(p.M - 1));
-                    const int64_t kr = kbase + (qq >> 2) * p.M + static_cast<int64_t>(cb);
-                    // 128B swizzle: chunk cx of row qq sits at chunk cx ^ (qq % 8)
-                    cp_async_16(sB + qq * 128 + ((cx ^ (qq & 7)) << 4), bcol + kr * p.ld_b, bytes);
+                    for (int r = 0; r < kRowsPerWord; ++r) {
+                        const int qq = q0 * kPasses + wi * 4 + r;  // row of the gathered tile: block qq/4, slot qq%4
+                        // column-loc byte, clamped so that a corrupt array cannot address past K
+                        const uint32_t cb = min((sel >> (8 * (qq & 3))) & 0xFFu, static_cast<uint32_t>(p.M - 1));
+                        const int64_t kr = kbase + (qq >> 2) * p.M + static_cast<int64_t>(cb);
+                        // 128B swizzle: chunk cx of row qq sits at chunk cx ^ (qq % 8)
+                        cp_async_16(sB + qq * 128 + ((cx ^ (qq & 7)) << 4), bcol + kr * p.ld_b, bytes);
+                    }
                 }
                 cp_async_arrive_noinc(smem_u32(&b_bar[slot]));
                 ++it;
