@@ -480,16 +480,6 @@ __global__ void __launch_bounds__(kCompressThreads) compress_stream_kernel(const
     if (threadIdx.x == 0 && bad) record_error(p.status, VNM_ERR_NONFINITE, 3);
 }
 
-// Half `idx` (0 .. 2*NW-1) of a block row held as NW 32-bit words.
-template <int NW>
-__device__ __forceinline__ uint16_t half_at(const uint32_t (&w)[NW], int idx) {
-    // masked OR over the words (keeps w in registers: no indexed access)
-    uint32_t x = 0;
-#pragma unroll
-    for (int u = 0; u < NW; ++u) x |= w[u] & (0u - static_cast<uint32_t>((idx >> 1) == u));
-    return static_cast<uint16_t>((idx & 1) ? (x >> 16) : (x & 0xFFFFu));
-}
-
 __device__ __forceinline__ float shfl_any(float v, int src) { return __shfl_sync(0xFFFFFFFFu, v, src); }
 __device__ __forceinline__ uint64_t shfl_any(uint64_t v, int src) {
     const uint32_t lo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(v), src);
@@ -522,6 +512,65 @@ __device__ __forceinline__ uint32_t mask_to_cols(uint32_t mask) {
         mask &= mask - 1;
     }
     return sel;
+}
+
+// sum += (float)h for the fp16 h in the low 16 bits of x (exact conversion,
+// one rounding: the same value as converting then adding).
+__device__ __forceinline__ void add_f16(float& sum, uint32_t x) {
+    const unsigned short h = static_cast<unsigned short>(x & 0xFFFFu);
+    asm("add.rn.f32.f16 %0, %1, %0;" : "+f"(sum) : "h"(h));
+}
+
+// Word pair holding half `col` of a block row of NW words: words 2*(col/4)
+// and 2*(col/4)+1, picked by a select tree on the bits of col/4.
+template <int NW>
+__device__ __forceinline__ void pair_of(const uint32_t (&w)[NW], int pair, uint32_t& x, uint32_t& y) {
+    constexpr int NP = NW / 2;
+    uint32_t xs[NP], ys[NP];
+#pragma unroll
+    for (int q = 0; q < NP; ++q) {
+        xs[q] = w[2 * q];
+        ys[q] = w[2 * q + 1];
+    }
+#pragma unroll
+    for (int lvl = 1; lvl < NP; lvl <<= 1) {
+        const bool hi = (pair & lvl) != 0;
+#pragma unroll
+        for (int q = 0; q < NP; q += 2 * lvl) {
+            xs[q] = hi ? xs[q + lvl] : xs[q];
+            ys[q] = hi ? ys[q + lvl] : ys[q];
+        }
+    }
+    x = xs[0];
+    y = ys[0];
+}
+
+// Byte-permute selector that moves half (col % 4) of a word pair into the
+// low 16 bits.
+__device__ __forceinline__ uint32_t half_selector(int col) {
+    const uint32_t b = 2u * static_cast<uint32_t>(col & 3);
+    return b | ((b + 1u) << 4);
+}
+
+// 2 of the 4 values packed as P = a0 | a1 << 16, Q = a2 | a3 << 16: the two
+// with the largest |a| (lower slot on ties), in slot order, as one word
+// v0 | v1 << 16; returns the 4-bit code s0 | s1 << 2.
+__device__ __forceinline__ uint32_t keep2of4_packed(uint32_t P, uint32_t Q, uint32_t& out) {
+    const uint32_t mP = P & 0x7FFF7FFFu, mQ = Q & 0x7FFF7FFFu;
+    const uint32_t m0 = mP & 0xFFFFu, m1 = mP >> 16, m2 = mQ & 0xFFFFu, m3 = mQ >> 16;
+    const uint32_t g01 = m0 >= m1, g02 = m0 >= m2, g03 = m0 >= m3;
+    const uint32_t g12 = m1 >= m2, g13 = m1 >= m3, g23 = m2 >= m3;
+    const uint32_t r0 = 3u - g01 - g02 - g03;
+    const uint32_t r1 = g01 + 2u - g12 - g13;
+    const uint32_t r2 = g02 + g12 + 1u - g23;
+    const uint32_t r3 = g03 + g13 + g23;
+    const uint32_t keep = (r0 < 2u) | ((r1 < 2u) << 1) | ((r2 < 2u) << 2) | ((r3 < 2u) << 3);
+    const uint32_t s0 = __ffs(keep) - 1u;  // exactly two bits are set
+    const uint32_t s1 = 31u - __clz(keep);
+    // bytes 2s, 2s+1 of the 8-byte (P, Q) for s0 then s1
+    const uint32_t sel = (2u * s0) | ((2u * s0 + 1u) << 4) | ((2u * s1) << 8) | ((2u * s1 + 1u) << 12);
+    out = __byte_perm(P, Q, sel);
+    return s0 | (s1 << 2);
 }
 
 constexpr int kColsBlocks = 8;   // blocks per CTA: consecutive blocks of one block row
@@ -566,8 +615,8 @@ __global__ void __launch_bounds__(kColsWarps * 32, 2) compress_cols_kernel(const
     uint4 x[RPL > 0 ? RPL : 1][kVec];
     auto add_pair = [&](uint32_t w, int c) {  // |w| of two fp16 (sign bits cleared) into sum[c], sum[c+1]
         const uint32_t m = w & 0x7FFF7FFFu;
-        sum[c] += __half2float(__ushort_as_half(static_cast<unsigned short>(m & 0xFFFFu)));
-        sum[c + 1] += __half2float(__ushort_as_half(static_cast<unsigned short>(m >> 16)));
+        add_f16(sum[c], m);
+        add_f16(sum[c + 1], m >> 16);
     };
     auto accumulate = [&](const uint4 (&xr)[kVec]) {
 #pragma unroll
@@ -647,6 +696,8 @@ __global__ void __launch_bounds__(kColsWarps * 32, 2) compress_cols_kernel(const
     // ---- pass 2: 2 of the 4 selected values per row
     const uint32_t sel = s_sel[b];
     const int col0 = sel & 0xFF, col1 = (sel >> 8) & 0xFF, col2 = (sel >> 16) & 0xFF, col3 = sel >> 24;
+    const uint32_t bs0 = half_selector(col0), bs1 = half_selector(col1), bs2 = half_selector(col2),
+                   bs3 = half_selector(col3);
     const bool pair_lo = (j & 1) == 0;
     auto emit = [&](const uint4 (&xr)[kVec], int r, bool act) {
         uint32_t w[kNW];
@@ -657,16 +708,24 @@ __global__ void __launch_bounds__(kColsWarps * 32, 2) compress_cols_kernel(const
             w[4 * v + 2] = xr[v].z;
             w[4 * v + 3] = xr[v].w;
         }
-        const uint16_t a[4] = {half_at<kNW>(w, col0), half_at<kNW>(w, col1), half_at<kNW>(w, col2),
-                               half_at<kNW>(w, col3)};
-        uint16_t v0, v1;
-        uint32_t code = keep2of4(a, v0, v1);
+        // the 4 selected values as P = a0 | a1 << 16, Q = a2 | a3 << 16
+        uint32_t x, y;
+        pair_of<kNW>(w, col0 >> 2, x, y);
+        const uint32_t h0 = __byte_perm(x, y, bs0);
+        pair_of<kNW>(w, col1 >> 2, x, y);
+        const uint32_t h1 = __byte_perm(x, y, bs1);
+        pair_of<kNW>(w, col2 >> 2, x, y);
+        const uint32_t h2 = __byte_perm(x, y, bs2);
+        pair_of<kNW>(w, col3 >> 2, x, y);
+        const uint32_t h3 = __byte_perm(x, y, bs3);
+        const uint32_t P = __byte_perm(h0, h1, 0x5410u), Q = __byte_perm(h2, h3, 0x5410u);
+        uint32_t vals;
+        uint32_t code = keep2of4_packed(P, Q, vals);
         if (!act) code = 0;
         const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, code, 1);  // the neighbouring block's code
         if (act) {
             const int64_t row = i * V + r;
-            *reinterpret_cast<uint32_t*>(p.values + row * (2 * p.nblk) + 2 * j) =
-                static_cast<uint32_t>(v0) | (static_cast<uint32_t>(v1) << 16);
+            *reinterpret_cast<uint32_t*>(p.values + row * (2 * p.nblk) + 2 * j) = vals;
             if (pair_lo) p.meta[row * p.mpitch + (j >> 1)] = static_cast<uint8_t>(code | (other << 4));
         }
     };
