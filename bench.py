@@ -9,7 +9,8 @@ vnm_compress(W) then vnm_spmm(B) -> C, for the square compute-bound workload
 another). Inputs are resident in HBM when the timed region starts; the steps
 rotate over enough distinct input/output sets that each set is evicted from
 L2 before it is used again. The K timed steps are captured once in a CUDA
-graph (with an event node around every kernel) and replayed.
+graph and replayed between two events; each kernel's own launch duration
+comes from graphs of K launches of that kernel alone over the same sets.
 
 Output: one JSON line (rank 0). ``value`` is the dense-equivalent TFLOP/s of
 the whole step (2*R*N*K per step over the step time); ``e2e`` is the same
@@ -323,16 +324,12 @@ def main():
 
     stream = torch.cuda.current_stream(dev)
 
-    def step(i, ev=None):
+    def step(i, comp=True, spmm=True):
         s = sets[i % n_sets]
-        if ev is not None:
-            ev[0].record(stream)
-        vnm.vnm_compress(s["A"], s["W"], stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        vnm.vnm_spmm(s["A"], s["B"], s["C"], workspace=s["ws"], stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
+        if comp:
+            vnm.vnm_compress(s["A"], s["W"], stream=stream)
+        if spmm:
+            vnm.vnm_spmm(s["A"], s["B"], s["C"], workspace=s["ws"], stream=stream)
 
     # warm-up (eager), then check the status words
     for i in range(max(args.warmup, 1)):
@@ -343,56 +340,56 @@ def main():
         if st != vnm.VNM_OK:
             raise RuntimeError(f"kernel status {vnm.status_string(st)} during warm-up")
 
-    # capture the K timed steps (with event nodes) in one CUDA graph
+    # Three CUDA graphs over the same rotating sets, each captured once:
+    # K whole steps (the timed region: no event nodes inside, which would
+    # add microseconds per kernel), K SpMM launches and K compress launches
+    # (each kernel's average launch duration, for the breakdown and the
+    # roofline).
     steps = args.steps
-    try:  # event record nodes inside the graph (external events)
-        evs = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(3)] for _ in range(steps)]
-    except TypeError:
-        evs = None
-    graph = torch.cuda.CUDAGraph()
-    cap_stream = torch.cuda.Stream(dev)
-    cap_stream.wait_stream(stream)
-    with torch.cuda.stream(cap_stream):
-        stream = cap_stream
-        with torch.cuda.graph(graph, stream=cap_stream):
-            for i in range(steps):
-                step(i, evs[i] if evs is not None else None)
-    stream = torch.cuda.current_stream(dev)
-    torch.cuda.synchronize(dev)
-    graph.replay()  # warm replay
-    torch.cuda.synchronize(dev)
+
+    def capture(**kw):
+        nonlocal stream
+        g = torch.cuda.CUDAGraph()
+        cap_stream = torch.cuda.Stream(dev)
+        cap_stream.wait_stream(torch.cuda.current_stream(dev))
+        prev = stream
+        with torch.cuda.stream(cap_stream):
+            stream = cap_stream
+            with torch.cuda.graph(g, stream=cap_stream):
+                for i in range(steps):
+                    step(i, **kw)
+        stream = prev
+        torch.cuda.synchronize(dev)
+        g.replay()  # warm replay
+        torch.cuda.synchronize(dev)
+        return g
+
+    graph = capture()
+    graph_spmm = capture(comp=False)
+    graph_comp = capture(spmm=False)
+
+    def timed(g):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
 
     # clocks: sample across a load phase that brackets the timed replay
     sampler = ClockSampler(local)
     sampler.start()
     t_load0 = time.time()
-    reps = 0
     while time.time() - t_load0 < args.clock_seconds / 2:
         graph.replay()
         torch.cuda.synchronize(dev)
-        reps += 1
-    g0 = torch.cuda.Event(enable_timing=True)
-    g1 = torch.cuda.Event(enable_timing=True)
     dist_barrier(world, dev)
     torch.cuda.synchronize(dev)
-    t_timed0 = time.time()
-    g0.record(stream)
-    graph.replay()
-    g1.record(stream)
-    torch.cuda.synchronize(dev)
-    t_timed1 = time.time()
+    elapsed_ms = timed(graph)
     dist_barrier(world, dev)
-    elapsed_ms = g0.elapsed_time(g1)
-    if evs is not None:
-        comp_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
-        spmm_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
-    else:  # per-kernel events on an eager replay of the same steps
-        ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-        for i in range(steps):
-            step(i, ev2[i])
-        torch.cuda.synchronize(dev)
-        comp_ms = sum(e[0].elapsed_time(e[1]) for e in ev2) / steps
-        spmm_ms = sum(e[1].elapsed_time(e[2]) for e in ev2) / steps
+    spmm_ms = timed(graph_spmm) / steps
+    comp_ms = timed(graph_comp) / steps
     t_load1 = time.time()
     while time.time() - t_load1 < args.clock_seconds / 2:
         graph.replay()

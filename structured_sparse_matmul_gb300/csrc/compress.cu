@@ -769,30 +769,35 @@ __global__ void __launch_bounds__(kM4Threads) compress_m4_kernel(const CompressA
     const int64_t cpr = p.K / 16;  // 16-weight chunks per row
     const int64_t total = p.R * cpr;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kM4Threads;
-    int nonfinite = 0;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * kM4Threads + threadIdx.x; q < total; q += stride) {
-        const int64_t r = q / cpr, x = q % cpr;
+    const int64_t sr = stride / cpr, sx = stride % cpr;  // the stride in rows and chunks
+    int64_t q = static_cast<int64_t>(blockIdx.x) * kM4Threads + threadIdx.x;
+    int64_t r = q / cpr, x = q % cpr;
+    uint32_t nonfinite = 0;
+#pragma unroll 2
+    for (; q < total; q += stride) {
         const uint4* src = reinterpret_cast<const uint4*>(p.W + r * p.ld_w + 16 * x);
         const uint4 a = __ldg(src), b = __ldg(src + 1);
         const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        uint16_t out[8];
+        uint32_t v[4];
         uint32_t code = 0;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-            const uint16_t e[4] = {static_cast<uint16_t>(w[2 * g] & 0xFFFFu), static_cast<uint16_t>(w[2 * g] >> 16),
-                                   static_cast<uint16_t>(w[2 * g + 1] & 0xFFFFu),
-                                   static_cast<uint16_t>(w[2 * g + 1] >> 16)};
+            // a group of 4 weights is the word pair (w[2g], w[2g+1])
 #pragma unroll
-            for (int u = 0; u < 4; ++u) nonfinite |= half_nonfinite(e[u]);
-            code |= keep2of4(e, out[2 * g], out[2 * g + 1]) << (4 * g);
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t e = w[2 * g + h] & 0x7C007C00u;  // exponent fields of both halves
+                nonfinite |= ((e & 0xFFFFu) == 0x7C00u) | ((e >> 16) == 0x7C00u);
+            }
+            code |= keep2of4_packed(w[2 * g], w[2 * g + 1], v[g]) << (4 * g);
         }
-        uint4 v;
-        v.x = out[0] | (static_cast<uint32_t>(out[1]) << 16);
-        v.y = out[2] | (static_cast<uint32_t>(out[3]) << 16);
-        v.z = out[4] | (static_cast<uint32_t>(out[5]) << 16);
-        v.w = out[6] | (static_cast<uint32_t>(out[7]) << 16);
-        *reinterpret_cast<uint4*>(p.values + r * (p.K / 2) + 8 * x) = v;
+        *reinterpret_cast<uint4*>(p.values + r * (p.K / 2) + 8 * x) = make_uint4(v[0], v[1], v[2], v[3]);
         *reinterpret_cast<uint16_t*>(p.meta + r * p.mpitch + 2 * x) = static_cast<uint16_t>(code);
+        x += sx;
+        r += sr;
+        if (x >= cpr) {
+            x -= cpr;
+            ++r;
+        }
     }
     const int64_t ncw = (p.R / p.V) * p.nblk;  // column-loc words: always 0, 1, 2, 3
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * kM4Threads + threadIdx.x; q < ncw; q += stride)
@@ -843,9 +848,17 @@ cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, 
     p.status = A.status;
     if (A.R == 0 || A.K == 0) return cudaSuccess;
     if (A.M == 4 && A.K % 16 == 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0 && ld_w % 8 == 0) {
+        // one full wave of resident CTAs, each striding over the chunks
+        static int per_sm = 0;
+        if (per_sm == 0) {
+            int occ = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, compress_m4_kernel, kM4Threads, 0) != cudaSuccess)
+                occ = 4;
+            per_sm = std::max(1, occ);
+        }
         const int64_t chunks = A.R * (A.K / 16);
         const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((chunks + kM4Threads - 1) / kM4Threads,
-                                                                      static_cast<int64_t>(A.sm_count) * 8));
+                                                                      static_cast<int64_t>(A.sm_count) * per_sm));
         compress_m4_kernel<<<static_cast<unsigned>(blocks), kM4Threads, 0, stream>>>(p);
         return cudaGetLastError();
     }
