@@ -176,3 +176,30 @@ def _workload_case(case: workloads.Case, max_rows: int):
                          ids=lambda c: c.name)
 def test_workloads(case):
     _workload_case(case, max_rows=256 if case.N >= 2048 else 1024)
+
+
+@pytest.mark.parametrize("case", workloads.workload_cases(5), ids=lambda c: c.name)
+def test_workload5_full_size_sampled(case):
+    """The large FFN shape at full size, through the same calls and plan the
+    bench times: the whole W is compressed and multiplied on the GPU; the
+    oracle compresses three block rows (first, middle, last) from the host W
+    and computes a sample of their rows of C, which must match the GPU's
+    arrays bit for bit and its C within the tolerance."""
+    R, K, N, V, M = case.R, case.K, case.N, case.V, case.M
+    W = inputs.normal_f16((R, K), case.seed, case.a_stream, workloads.A_SIGMA)
+    B = inputs.normal_f16((K, N), case.seed, case.b_stream, workloads.B_SIGMA)
+    A, st = gpu_compress(W, V, M)
+    assert st == vnm.VNM_OK
+    got, _ = run_spmm(A, B, torch.float16)
+    nb = R // V
+    rng = np.random.default_rng(5)
+    for i in (0, nb // 2, nb - 1):
+        Wi = W[i * V:(i + 1) * V]
+        values, meta, colidx = oracle.compress(Wi, V, M)
+        rows = slice(i * V, (i + 1) * V)
+        assert np.array_equal(A.values[rows].cpu().numpy().view(np.uint16), values), f"values, block row {i}"
+        assert np.array_equal(A.meta[rows].cpu().numpy(), meta), f"meta, block row {i}"
+        assert np.array_equal(A.colidx[i:i + 1].cpu().numpy(), colidx), f"column-loc, block row {i}"
+        local = sorted(set([0, 1, V // 2, V - 1] + rng.integers(0, V, 4).tolist()))
+        ref = oracle.spmm(values, meta, colidx, V, K, V, M, B, rows=local)
+        check_close(got[[i * V + r for r in local]], ref, f"{case.name} block row {i}")
