@@ -119,6 +119,147 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int spli
     }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming path for N <= 8 (decode-like): one CTA per (V-block row, K split).
+// The rows of a V-block row share column-loc, so per chunk of 32*U blocks
+// the CTA first stages the 4 selected rows of B of every block (N <= 8
+// values each) in shared memory; each of the 16 warps owns RW rows and
+// issues all its loads of the chunk at once (lane = block, RW*U = 16 loads
+// per lane), so a chunk costs one round trip to memory; the multiply-adds
+// then read B from shared memory. Splits write fp32 partials that the
+// split-K reduction sums in order.
+constexpr int kStreamWarps = 16;
+
+struct StreamArgs {
+    const uint32_t* values;  // [R][nblk] words: the 2 fp16 values of one block
+    const uint8_t* meta;     // [R][mpitch]
+    const uint32_t* colidx;  // [R/V][nblk] words: 4 column bytes
+    const __half* B;
+    int64_t ld_b;
+    void* C;
+    int64_t ld_c;
+    float* partial;          // [splits][R][N] fp32 when splits > 1
+    int64_t R, N;
+    int V, M;
+    int64_t nblk, mpitch;
+    int splits;
+    int64_t bps;             // blocks per split
+    bool c_f32;
+};
+
+template <int NB, int RW, int U>
+__global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const StreamArgs p) {
+    constexpr int kChunk = 32 * U;                       // blocks per chunk
+    constexpr int kStride = 4 * NB + (NB >= 4 ? 8 : 0);  // halves per staged block (padded: spread banks)
+    __shared__ __align__(16) __half Bc[kChunk * kStride];
+    const int64_t i = blockIdx.x / p.splits;
+    const int s = static_cast<int>(blockIdx.x % p.splits);
+    const int64_t jb = s * p.bps;
+    const int64_t je = jb + p.bps < p.nblk ? jb + p.bps : p.nblk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t* crow = p.colidx + i * p.nblk;
+
+    // the same trip count for every warp (the loop holds CTA barriers); rows
+    // past V are masked
+    for (int rbase = 0; rbase < p.V; rbase += kStreamWarps * RW) {
+        const int r0 = rbase + warp;
+        float acc[RW][NB];
+#pragma unroll
+        for (int t = 0; t < RW; ++t)
+#pragma unroll
+            for (int n = 0; n < NB; ++n) acc[t][n] = 0.f;
+        for (int64_t j0 = jb; j0 < je; j0 += kChunk) {
+            // this warp's rows of the chunk: all loads in flight at once
+            uint32_t vv[RW][U], mb[RW][U];
+#pragma unroll
+            for (int t = 0; t < RW; ++t) {
+                const int r = r0 + kStreamWarps * t;
+                const int64_t row = i * p.V + r;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t jj = j0 + lane + 32 * u;
+                    vv[t][u] = 0u;
+                    mb[t][u] = 0u;
+                    if (r < p.V && jj < je) {
+                        vv[t][u] = __ldg(p.values + row * p.nblk + jj);
+                        mb[t][u] = __ldg(p.meta + row * p.mpitch + (jj >> 1));
+                    }
+                }
+            }
+            // stage the chunk's selected rows of B (the previous chunk's reads are done)
+            __syncthreads();
+            const int nb = static_cast<int>(je - j0 < kChunk ? je - j0 : kChunk);
+            for (int q = threadIdx.x; q < nb * 4; q += blockDim.x) {
+                const int jl = q >> 2, slot = q & 3;
+                const uint32_t w = __ldg(crow + j0 + jl);
+                // column-loc byte, clamped so that a corrupt array cannot address past K
+                const uint32_t cb = min((w >> (8 * slot)) & 0xFFu, static_cast<uint32_t>(p.M - 1));
+                const __half* src = p.B + ((j0 + jl) * p.M + cb) * p.ld_b;
+                __half* dst = Bc + jl * kStride + slot * NB;
+#pragma unroll
+                for (int n = 0; n < NB; ++n) dst[n] = n < p.N ? src[n] : __float2half_rn(0.f);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int t = 0; t < RW; ++t) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t jj = j0 + lane + 32 * u;
+                    if (jj >= je) continue;
+                    const uint32_t code = (mb[t][u] >> (4 * (jj & 1))) & 0xFu;
+                    const float a0 = __half2float(__ushort_as_half(static_cast<unsigned short>(vv[t][u] & 0xFFFFu)));
+                    const float a1 = __half2float(__ushort_as_half(static_cast<unsigned short>(vv[t][u] >> 16)));
+                    const __half* b = Bc + (lane + 32 * u) * kStride;
+                    const __half* b0 = b + (code & 3u) * NB;
+                    const __half* b1 = b + (code >> 2) * NB;
+#pragma unroll
+                    for (int n = 0; n < NB; ++n) {
+                        acc[t][n] = fmaf(a0, __half2float(b0[n]), acc[t][n]);
+                        acc[t][n] = fmaf(a1, __half2float(b1[n]), acc[t][n]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < RW; ++t) {
+            const int r = r0 + kStreamWarps * t;
+            float out = 0.f;
+#pragma unroll
+            for (int n = 0; n < NB; ++n) {
+                float v = acc[t][n];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+                if (lane == n) out = v;
+            }
+            if (r < p.V && lane < p.N && lane < NB) {
+                const int64_t row = i * p.V + r;
+                if (p.partial != nullptr)
+                    p.partial[(static_cast<int64_t>(s) * p.R + row) * p.N + lane] = out;
+                else if (p.c_f32)
+                    static_cast<float*>(p.C)[row * p.ld_c + lane] = out;
+                else
+                    static_cast<__half*>(p.C)[row * p.ld_c + lane] = __float2half_rn(out);
+            }
+        }
+    }
+}
+
+template <int NB, int RW, int U>
+cudaError_t launch_stream3(const StreamArgs& p, cudaStream_t stream) {
+    const int64_t ctas = (p.R / p.V) * p.splits;
+    spmm_stream_kernel<NB, RW, U><<<static_cast<unsigned>(ctas), 32 * kStreamWarps, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+template <int NB>
+cudaError_t launch_stream_nb(const StreamArgs& p, cudaStream_t stream) {
+    // RW rows per warp (V <= 16 * RW in one pass), U = 16 / RW blocks per lane
+    if (p.V <= 16) return launch_stream3<NB, 1, 8>(p, stream);
+    if (p.V <= 32) return launch_stream3<NB, 2, 8>(p, stream);
+    if (p.V <= 64) return launch_stream3<NB, 4, 4>(p, stream);
+    return launch_stream3<NB, 8, 2>(p, stream);
+}
+
 template <int NB>
 cudaError_t launch_nb(const SimtArgs& p, cudaStream_t stream) {
     const unsigned grid = static_cast<unsigned>((p.R + kSimtWarps - 1) / kSimtWarps);
@@ -151,6 +292,41 @@ cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b,
     if (N <= 4) return launch_nb<4>(p, stream);
     if (N <= 8) return launch_nb<8>(p, stream);
     return launch_nb<16>(p, stream);
+}
+
+int stream_chunk_blocks(int V) { return V <= 32 ? 256 : V <= 64 ? 128 : 64; }
+
+cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
+                               int64_t ld_c, bool c_f32, int splits, float* partial, cudaStream_t stream) {
+    StreamArgs p;
+    p.values = static_cast<const uint32_t*>(A.values);
+    p.meta = static_cast<const uint8_t*>(A.meta);
+    p.colidx = static_cast<const uint32_t*>(A.colidx);
+    p.B = static_cast<const __half*>(B);
+    p.ld_b = ld_b;
+    p.C = C;
+    p.ld_c = ld_c;
+    p.R = A.R;
+    p.N = N;
+    p.V = A.V;
+    p.M = A.M;
+    p.nblk = A.K / A.M;
+    p.mpitch = meta_pitch(A.K, A.M);
+    p.c_f32 = c_f32;
+    if (A.R == 0 || N == 0) return cudaSuccess;
+    if (N > 8) return cudaErrorInvalidValue;
+    const int64_t req = std::max<int64_t>(1, std::min<int64_t>(splits, p.nblk));
+    p.bps = (p.nblk + req - 1) / req;
+    p.splits = static_cast<int>((p.nblk + p.bps - 1) / p.bps);  // no empty split
+    if (p.splits > 1 && partial == nullptr) return cudaErrorInvalidValue;
+    p.partial = p.splits > 1 ? partial : nullptr;
+    cudaError_t e;
+    if (N <= 1) e = launch_stream_nb<1>(p, stream);
+    else if (N <= 2) e = launch_stream_nb<2>(p, stream);
+    else if (N <= 4) e = launch_stream_nb<4>(p, stream);
+    else e = launch_stream_nb<8>(p, stream);
+    if (e != cudaSuccess || p.splits == 1) return e;
+    return launch_splitk_reduce(partial, p.splits, A.R, N, C, ld_c, c_f32, stream);
 }
 
 cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, void* C, int64_t ld_c,

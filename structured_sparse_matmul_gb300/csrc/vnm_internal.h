@@ -46,6 +46,13 @@ __device__ __forceinline__ void record_error(int* status, int code, int where) {
 cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, cudaStream_t stream);
 cudaError_t launch_decompress(const vnm_matrix_s& A, void* W, int64_t ld_w, cudaStream_t stream);
 
+// Streaming CUDA-core SpMM for N <= 8: one CTA per (V-block row, K split);
+// with splits > 1 it writes fp32 partials to `partial` ([splits][R][N]) and
+// reduces them into C. `stream_chunk_blocks(V)` blocks are staged per pass.
+cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
+                               int64_t ld_c, bool c_f32, int splits, float* partial, cudaStream_t stream);
+int stream_chunk_blocks(int V);
+
 // CUDA-core SpMM; writes C directly (fp16 or fp32).
 cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
                              int64_t ld_c, bool c_f32, cudaStream_t stream);

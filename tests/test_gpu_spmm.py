@@ -203,3 +203,40 @@ def test_workload5_full_size_sampled(case):
         local = sorted(set([0, 1, V // 2, V - 1] + rng.integers(0, V, 4).tolist()))
         ref = oracle.spmm(values, meta, colidx, V, K, V, M, B, rows=local)
         check_close(got[[i * V + r for r in local]], ref, f"{case.name} block row {i}")
+
+
+STREAM_SHAPES = [
+    (64, 512, 8, 4, 3),       # V < 16: rows of a block row spread over fewer warps
+    (96, 600, 8, 5, 2),       # odd M, K not a multiple of the stage
+    (256, 1024, 128, 8, 1),
+    (272, 256, 16, 4, 7),
+    (512, 8192, 32, 16, 4),   # several staged chunks per split
+    (4096, 4096, 64, 4, 1),   # decode shape
+]
+
+
+@pytest.mark.parametrize("R,K,V,M,N", STREAM_SHAPES)
+@pytest.mark.parametrize("c_dtype", [torch.float16, torch.float32], ids=["f16", "f32"])
+def test_streaming_small_n(R, K, V, M, N, c_dtype):
+    """N <= 8 takes the streaming CUDA-core path: with the workspace it asks
+    for (split K, partials reduced in order) and without one (one split)."""
+    A, B, comp = _setup(R, K, N, V, M, seed=28)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B), c_dtype, 1 << 40)
+    assert plan.path == vnm.VNM_PATH_SIMT, plan.as_dict()
+    rows = None if R <= 512 else sample_rows(R, V, 64)
+    ref = _ref(comp, R, K, V, M, B, rows=rows)
+    for ws in (True, False):
+        got, _ = run_spmm(A, B, c_dtype, workspace=ws)
+        check_close(got if rows is None else got[rows], ref, f"stream {R}x{K}x{N} {V}:2:{M} ws={ws}")
+
+
+def test_streaming_at_n8_by_plan():
+    """N = 8 runs on the tensor cores by default; a plan may ask for the
+    streaming path instead, with a chosen split."""
+    R, K, N, V, M = 1024, 4096, 8, 64, 8
+    A, B, comp = _setup(R, K, N, V, M, seed=29)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    plan.path = vnm.VNM_PATH_SIMT
+    plan.splits = 3
+    got, _ = run_spmm(A, B, plan=plan)
+    check_close(got, _ref(comp, R, K, V, M, B), "stream N=8")
