@@ -125,7 +125,8 @@ struct TcCfg {
 // A bytes per gathered B byte, so it takes twice the gather warps; never
 // more threads than 16-byte chunks per stage (kKTile * BN / 8).
 __host__ __device__ constexpr int gather_threads(int tm, int bn) {
-    return (tm == 64 ? 512 : 256) < kKTile * bn / 8 ? (tm == 64 ? 512 : 256) : kKTile * bn / 8;
+    // 192 columns are 24 chunks a row: a multiple of 24 threads, 8 rows each
+    return bn == 192 ? 384 : (tm == 64 ? 512 : 256) < kKTile * bn / 8 ? (tm == 64 ? 512 : 256) : kKTile * bn / 8;
 }
 
 template <int TM, int BN, bool GATHER>
@@ -574,6 +575,7 @@ cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, cudaStream_t stream)
         case 32: return launch_variant<TM, 32, GATHER>(L, p, stream);
         case 64: return launch_variant<TM, 64, GATHER>(L, p, stream);
         case 128: return launch_variant<TM, 128, GATHER>(L, p, stream);
+        case 192: return launch_variant<TM, 192, GATHER>(L, p, stream);
         case 256: return launch_variant<TM, 256, GATHER>(L, p, stream);
         default: return cudaErrorInvalidValue;
     }
@@ -583,7 +585,7 @@ cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, cudaStream_t stream)
 
 int tc_default_stages(int tile_m, int tile_n) {
     if (tile_m != 64 && tile_m != 128) return 0;
-    if (tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 && tile_n != 256) return 0;
+    if (tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 && tile_n != 192 && tile_n != 256) return 0;
     return tc_stages_for(tile_m, tile_n);
 }
 

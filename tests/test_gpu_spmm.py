@@ -79,7 +79,7 @@ def test_tensor_core_path(R, K, N, V, M, c_dtype):
     check_close(got, _ref(comp, R, K, V, M, B), f"tc {R}x{K}x{N} {V}:2:{M}")
 
 
-@pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 256])
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 192, 256])
 @pytest.mark.parametrize("V,tile_m", [(128, 128), (64, 64), (128, 64)])
 def test_tensor_core_tiles(tile_n, V, tile_m):
     R, K, N, M = 256, 1024, 296, 8  # N % 8 == 0 (TMA rows), ragged against every tile_n
@@ -92,6 +92,20 @@ def test_tensor_core_tiles(tile_n, V, tile_m):
     plan.splits = 1
     got, _ = run_spmm(A, B, plan=plan)
     check_close(got, _ref(comp, R, K, V, M, B), f"tile_n {tile_n}")
+
+
+@pytest.mark.parametrize("tile_n", [64, 192, 256])
+def test_tensor_core_tiles_plain_2to4(tile_n):
+    """M = 4 (B rows by TMA, no gather) at several tile widths, ragged N."""
+    R, K, N, V, M = 256, 1024, 296, 16, 4
+    A, B, comp = _setup(R, K, N, V, M, seed=30)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    assert plan.path == vnm.VNM_PATH_TC
+    plan.tile_n = tile_n
+    plan.stages = 0
+    plan.splits = 1
+    got, _ = run_spmm(A, B, plan=plan)
+    check_close(got, _ref(comp, R, K, V, M, B), f"plain 2:4 tile_n {tile_n}")
 
 
 @pytest.mark.parametrize("splits", [2, 3, 5])
