@@ -556,17 +556,14 @@ __device__ __forceinline__ uint32_t half_selector(int col) {
 // with the largest |a| (lower slot on ties), in slot order, as one word
 // v0 | v1 << 16; returns the 4-bit code s0 | s1 << 2.
 __device__ __forceinline__ uint32_t keep2of4_packed(uint32_t P, uint32_t Q, uint32_t& out) {
+    // unique keys (|a| << 2 | 3 - slot): larger |a| first, then the lower slot
     const uint32_t mP = P & 0x7FFF7FFFu, mQ = Q & 0x7FFF7FFFu;
-    const uint32_t m0 = mP & 0xFFFFu, m1 = mP >> 16, m2 = mQ & 0xFFFFu, m3 = mQ >> 16;
-    const uint32_t g01 = m0 >= m1, g02 = m0 >= m2, g03 = m0 >= m3;
-    const uint32_t g12 = m1 >= m2, g13 = m1 >= m3, g23 = m2 >= m3;
-    const uint32_t r0 = 3u - g01 - g02 - g03;
-    const uint32_t r1 = g01 + 2u - g12 - g13;
-    const uint32_t r2 = g02 + g12 + 1u - g23;
-    const uint32_t r3 = g03 + g13 + g23;
-    const uint32_t keep = (r0 < 2u) | ((r1 < 2u) << 1) | ((r2 < 2u) << 2) | ((r3 < 2u) << 3);
-    const uint32_t s0 = __ffs(keep) - 1u;  // exactly two bits are set
-    const uint32_t s1 = 31u - __clz(keep);
+    const uint32_t k0 = ((mP & 0xFFFFu) << 2) | 3u, k1 = ((mP >> 16) << 2) | 2u;
+    const uint32_t k2 = ((mQ & 0xFFFFu) << 2) | 1u, k3 = (mQ >> 16) << 2;
+    const uint32_t a = max(k0, k1), b = min(k0, k1), c = max(k2, k3), d = min(k2, k3);
+    const uint32_t t1 = max(a, c), t2 = max(min(a, c), max(b, d));  // largest and second largest
+    const uint32_t i1 = 3u - (t1 & 3u), i2 = 3u - (t2 & 3u);
+    const uint32_t s0 = min(i1, i2), s1 = max(i1, i2);
     // bytes 2s, 2s+1 of the 8-byte (P, Q) for s0 then s1
     const uint32_t sel = (2u * s0) | ((2u * s0 + 1u) << 4) | ((2u * s1) << 8) | ((2u * s1 + 1u) << 12);
     out = __byte_perm(P, Q, sel);
@@ -574,7 +571,6 @@ __device__ __forceinline__ uint32_t keep2of4_packed(uint32_t P, uint32_t Q, uint
 }
 
 constexpr int kColsBlocks = 8;   // blocks per CTA: consecutive blocks of one block row
-constexpr int kColsWarps = 8;
 
 // Compress for M in {8, 16, 32}. A CTA owns blocks (i, j0 .. j0+7) over all
 // V rows. Lane (b, g) = (lane % 8, lane / 8) of warp w handles block j0+b in
@@ -589,8 +585,11 @@ constexpr int kColsWarps = 8;
 // bytes (two blocks per byte, paired by a shuffle). With RPL > 0 (V <= 32 *
 // RPL) the rows stay in registers between the passes; with RPL == 0 pass 2
 // re-reads them (L1-resident: a CTA's rows are V * 16 * M bytes).
-template <int MB, int RPL>
-__global__ void __launch_bounds__(kColsWarps * 32, 2) compress_cols_kernel(const CompressArgs p) {
+// Two resident CTAs per SM bound the registers; measured faster for every
+// variant except M = 16 with four rows per lane, which runs best unbounded.
+template <int MB, int RPL, int kColsWarps>
+__global__ void __launch_bounds__(kColsWarps * 32, (MB == 16 && RPL == 4) ? 1 : 2)
+    compress_cols_kernel(const CompressArgs p) {
     constexpr int kVec = MB / 8;     // 16-byte chunks per block row
     constexpr int kNW = MB / 2;      // 32-bit words per block row
     constexpr int kRowStep = 4 * kColsWarps;
@@ -598,9 +597,10 @@ __global__ void __launch_bounds__(kColsWarps * 32, 2) compress_cols_kernel(const
     __shared__ uint32_t s_sel[kColsBlocks];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = lane & 7, g = lane >> 3;
-    const int64_t cpr = (p.nblk + kColsBlocks - 1) / kColsBlocks;  // CTAs per block row
-    const int64_t i = blockIdx.x / cpr;
-    const int64_t j0 = (blockIdx.x % cpr) * kColsBlocks;
+    // grid: x = tiles of 8 blocks along a block row, (y, z) = block row
+    const int64_t i = static_cast<int64_t>(blockIdx.z) * 65535 + blockIdx.y;
+    if (i >= p.R / p.V) return;  // the whole CTA (before any barrier)
+    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * kColsBlocks;
     const int64_t j = j0 + b;
     const bool valid = j < p.nblk;
     const int V = p.V;
@@ -658,34 +658,53 @@ __global__ void __launch_bounds__(kColsWarps * 32, 2) compress_cols_kernel(const
     }
     __syncthreads();
 
-    // ---- ranking: warp w ranks block j0 + w (warp-uniform condition)
-    if (j0 + warp < p.nblk) {
-        const int blk = warp;
-        float s = -1.f;  // below every column's sum
-        if (lane < MB) {
-            s = 0.f;
+    // ---- ranking: 32/MB blocks per warp, lane = MB * group + column; the
+    // first MB/4 warps rank the CTA's 8 blocks
+    constexpr int kGroups = 32 / MB;
+    constexpr int kRankWarps = kColsBlocks / kGroups;
+    for (int rw = warp; rw < kRankWarps; rw += kColsWarps) {  // warp-uniform
+        const int grp = lane / MB, c = lane % MB;
+        const int blk = rw * kGroups + grp;
+        const bool has = j0 + blk < p.nblk;  // per lane group
+        const uint32_t gshift = static_cast<uint32_t>(grp * MB);
+        const uint32_t gbits = MB == 32 ? 0xFFFFFFFFu : ((1u << MB) - 1u);
+        float s = 0.f;
 #pragma unroll
-            for (int w = 0; w < kColsWarps; ++w) s += s_sum[w][blk][lane];
+        for (int w = 0; w < kColsWarps; ++w) s += s_sum[w][blk][c];
+        const bool any_bad = ((__ballot_sync(0xFFFFFFFFu, has && !(s <= 3.4e38f)) >> gshift) & gbits) != 0;
+        int rk = 0;
+#pragma unroll
+        for (int c2 = 0; c2 < MB; ++c2) {
+            const float o = __shfl_sync(0xFFFFFFFFu, s, c2, MB);
+            rk += (o > s) || (o == s && c2 < c);
         }
-        const bool any_bad = __any_sync(0xFFFFFFFFu, lane < MB && !(s <= 3.4e38f));
-        int rank;
-        uint32_t mask = warp_top4_mask(s, MB, lane, &rank);
-        const int l3 = __ffs(__ballot_sync(0xFFFFFFFFu, rank == 3)) - 1;
-        const int l4 = __ffs(__ballot_sync(0xFFFFFFFFu, rank == 4)) - 1;
-        const float v3 = __shfl_sync(0xFFFFFFFFu, s, l3 & 31);
-        const float v4 = __shfl_sync(0xFFFFFFFFu, s, l4 & 31);
+        uint32_t mask = (__ballot_sync(0xFFFFFFFFu, rk < 4) >> gshift) & gbits;
+        const int l3 = __ffs((__ballot_sync(0xFFFFFFFFu, rk == 3) >> gshift) & gbits) - 1;
+        const int l4 = __ffs((__ballot_sync(0xFFFFFFFFu, rk == 4) >> gshift) & gbits) - 1;
+        const float v3 = __shfl_sync(0xFFFFFFFFu, s, l3 & (MB - 1), MB);
+        const float v4 = __shfl_sync(0xFFFFFFFFu, s, l4 & (MB - 1), MB);
         const bool safe = !any_bad && l3 >= 0 && l4 >= 0 &&
                           (v3 - v4 > 2.5f * static_cast<float>(V) * 5.9604645e-8f * v3);
-        if (!safe) {
+        if (__any_sync(0xFFFFFFFFu, has && !safe)) {
+            // exact sums in units of 2^-24 (the whole warp, for the groups that need them)
             uint64_t e = 0;
-            if (lane < MB) {
-                const uint16_t* col = Wrow + (j0 + blk) * MB + lane;
+            if (has) {
+                const uint16_t* col = Wrow + (j0 + blk) * MB + c;
                 for (int r = 0; r < V; ++r) e += mag_units(col[r * ld]);
             }
-            mask = warp_top4_mask(e, MB, lane, &rank);
+            int rk2 = 0;
+#pragma unroll
+            for (int c2 = 0; c2 < MB; ++c2) {
+                const uint32_t lo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(e), c2, MB);
+                const uint32_t hi = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(e >> 32), c2, MB);
+                const uint64_t o = (static_cast<uint64_t>(hi) << 32) | lo;
+                rk2 += (o > e) || (o == e && c2 < c);
+            }
+            const uint32_t m2 = (__ballot_sync(0xFFFFFFFFu, rk2 < 4) >> gshift) & gbits;
+            if (!safe) mask = m2;
         }
-        const uint32_t sel = mask_to_cols(mask);
-        if (lane == 0) {
+        if (has && c == 0) {
+            const uint32_t sel = mask_to_cols(mask);
             s_sel[blk] = sel;
             p.colidx[i * p.nblk + j0 + blk] = sel;
             if (any_bad) record_error(p.status, VNM_ERR_NONFINITE, 5);
@@ -749,13 +768,13 @@ __global__ void __launch_bounds__(kColsWarps * 32, 2) compress_cols_kernel(const
 }
 
 template <int MB>
-void launch_cols(const CompressArgs& p, unsigned ctas, cudaStream_t stream) {
+void launch_cols(const CompressArgs& p, dim3 grid, cudaStream_t stream) {
     const int V = p.V;
-    const unsigned threads = kColsWarps * 32;
-    if (V <= 32) compress_cols_kernel<MB, 1><<<ctas, threads, 0, stream>>>(p);
-    else if (V <= 64) compress_cols_kernel<MB, 2><<<ctas, threads, 0, stream>>>(p);
-    else if (V <= 128) compress_cols_kernel<MB, 4><<<ctas, threads, 0, stream>>>(p);
-    else compress_cols_kernel<MB, 0><<<ctas, threads, 0, stream>>>(p);
+    constexpr int W = 8;  // warps per CTA (4 measured slower: fewer rows in flight per CTA)
+    if (V <= 32) compress_cols_kernel<MB, 1, W><<<grid, 32 * W, 0, stream>>>(p);
+    else if (V <= 64) compress_cols_kernel<MB, 2, W><<<grid, 32 * W, 0, stream>>>(p);
+    else if (V <= 128) compress_cols_kernel<MB, 4, W><<<grid, 32 * W, 0, stream>>>(p);
+    else compress_cols_kernel<MB, 0, W><<<grid, 32 * W, 0, stream>>>(p);
 }
 
 // M == 4: column-loc is the identity, so prune-and-encode is the 2:4 step
@@ -864,10 +883,13 @@ cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, 
     }
     // M in {8, 16, 32}: eight blocks x V rows per CTA, no staging
     if ((A.M == 8 || A.M == 16 || A.M == 32) && reinterpret_cast<uintptr_t>(W) % 16 == 0 && ld_w % 8 == 0) {
-        const int64_t ctas = (A.R / A.V) * ((p.nblk + kColsBlocks - 1) / kColsBlocks);
-        if (A.M == 8) launch_cols<8>(p, static_cast<unsigned>(ctas), stream);
-        else if (A.M == 16) launch_cols<16>(p, static_cast<unsigned>(ctas), stream);
-        else launch_cols<32>(p, static_cast<unsigned>(ctas), stream);
+        const int64_t rows = A.R / A.V;  // block rows: grid y (then z past 65535)
+        const dim3 grid(static_cast<unsigned>((p.nblk + kColsBlocks - 1) / kColsBlocks),
+                        static_cast<unsigned>(std::min<int64_t>(rows, 65535)),
+                        static_cast<unsigned>((rows + 65534) / 65535));
+        if (A.M == 8) launch_cols<8>(p, grid, stream);
+        else if (A.M == 16) launch_cols<16>(p, grid, stream);
+        else launch_cols<32>(p, grid, stream);
         return cudaGetLastError();
     }
     // tile width: an even number of blocks, as many as fit the budget
