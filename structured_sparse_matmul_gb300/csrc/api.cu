@@ -133,7 +133,7 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     if (pl.tile_n > 64 && pl.tile_n < 128) pl.tile_n = 128;
     if (pl.tile_n > 32 && pl.tile_n < 64) pl.tile_n = 64;
     if (pl.tile_n > 16 && pl.tile_n < 32) pl.tile_n = 32;
-    pl.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n);
+    pl.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n, A.M > 4);
     // split K when the tiles alone cannot fill the GPU
     const int64_t tiles = ceil_div(A.R, pl.tile_m) * ceil_div(N, pl.tile_n);
     const int64_t num_kt = (A.K / A.M) / 32;
@@ -167,7 +167,7 @@ vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void
     if (pl.path != VNM_PATH_TC) return VNM_ERR_UNSUPPORTED;
     if (!tc_geometry_ok(A) || !tc_operands_ok(B, ld_b, N)) return VNM_ERR_UNSUPPORTED;
     if (!tc_tile_m_ok(A, pl.tile_m)) return VNM_ERR_UNSUPPORTED;
-    const int depth = vnm::tc_default_stages(pl.tile_m, pl.tile_n);
+    const int depth = vnm::tc_default_stages(pl.tile_m, pl.tile_n, A.M > 4);
     if (depth == 0 || (pl.stages != 0 && pl.stages != depth)) return VNM_ERR_UNSUPPORTED;
     if (pl.splits < 1) return VNM_ERR_INVALID_ARG;
     const int s = effective_splits(A, pl.splits);
@@ -193,7 +193,7 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         std::memset(&L, 0, sizeof(L));
         L.tile_m = pl.tile_m;
         L.tile_n = pl.tile_n;
-        L.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n);
+        L.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n, A->M > 4);
         L.splits = effective_splits(*A, pl.splits);
         L.gather = A->M > 4;
         L.sm_count = A->sm_count;
@@ -203,8 +203,13 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
                             static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_128B);
         ok = ok && encode_2d(&L.tm_e, CU_TENSOR_MAP_DATA_TYPE_UINT32, A->meta, mp / 4, A->R, mp, 4,
                              static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_NONE);
-        ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, A->K, ld_b * 2, 64, L.gather ? 1 : 128,
-                             CU_TENSOR_MAP_SWIZZLE_128B);
+        // B tiles by TMA (M == 4): 64-column atoms, or exactly tile_n columns with the
+        // matching swizzle for 16- and 32-column tiles
+        const bool narrow = vnm::tc_narrow_b(pl.tile_n, L.gather);
+        ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, A->K, ld_b * 2,
+                             narrow ? static_cast<uint32_t>(pl.tile_n) : 64, L.gather ? 1 : 128,
+                             !narrow ? CU_TENSOR_MAP_SWIZZLE_128B
+                                     : pl.tile_n == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
         if (!ok) return VNM_ERR_CUDA;
         e = vnm::launch_spmm_tc(*A, L, B, ld_b, N, C, ld_c, c_f32, static_cast<float*>(workspace), stream);
     }

@@ -101,14 +101,15 @@ __host__ __device__ constexpr int pow2_at_least(int x) {
     return p;
 }
 
-template <int TM, int BN>
+template <int TM, int BN, bool NARROW>
 struct TcCfg {
     static constexpr int kAtoms = (BN + 63) / 64;            // 64-column swizzle atoms of B
     static constexpr int kABytes = TM * 128;                 // TM rows x 64 values, 128B swizzle
-    static constexpr int kBBytes = kAtoms * kKTile * 128;    // per atom: 128 rows x 128 B
+    // per atom: 128 rows x 128 B; narrow: 128 rows x BN x 2 B
+    static constexpr int kBBytes = NARROW ? kKTile * BN * 2 : kAtoms * kKTile * 128;
     static constexpr int kEBytes = TM * 16;                  // 4 m-index words per row
     static constexpr int kStageBytes = kABytes + kBBytes + kEBytes;
-    static constexpr int kStages = tc_stages_for(TM, BN);
+    static constexpr int kStages = tc_stages_for(TM, BN, NARROW);
     // two accumulators (the epilogue of one tile overlaps the next tile's
     // main loop) when they fit TMEM beside the m-index slots
     static constexpr int kAccBufs = 2 * BN + kStages * kMetaStageCols <= 512 ? 2 : 1;
@@ -167,7 +168,7 @@ template <int TM, int BN, bool GATHER>
 __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_e,
                    const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
-    using Cfg = TcCfg<TM, BN>;
+    using Cfg = TcCfg<TM, BN, tc_narrow_b(BN, GATHER)>;
     constexpr int STAGES = Cfg::kStages;
     constexpr int ACC = Cfg::kAccBufs;
     constexpr int kGatherThreads = gather_threads(TM, BN);
@@ -253,10 +254,14 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                     if (!GATHER) {
                         const uint32_t bb = smem_u32(&b_bar[slot]);
                         mbar_arrive_expect_tx(bb, Cfg::kBBytes);
+                        if (tc_narrow_b(BN, GATHER)) {
+                            tma_load_2d(sB, &tm_b, static_cast<int32_t>(g.n0), kt * kKTile, bb);
+                        } else {
 #pragma unroll
-                        for (int a = 0; a < Cfg::kAtoms; ++a)
-                            tma_load_2d(sB + a * kKTile * 128, &tm_b, static_cast<int32_t>(g.n0 + 64 * a),
-                                        kt * kKTile, bb);
+                            for (int a = 0; a < Cfg::kAtoms; ++a)
+                                tma_load_2d(sB + a * kKTile * 128, &tm_b, static_cast<int32_t>(g.n0 + 64 * a),
+                                            kt * kKTile, bb);
+                        }
                     }
                     last_it[slot] = it;
                 }
@@ -305,8 +310,12 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                         const uint64_t ad = make_smem_desc(sA + s * 32, 16, 1024, kLayoutSw128);
                         // B: N-major, 128B swizzle; 64-column atoms kKTile*128 bytes apart (leading
                         // dimension), 8-row groups of K 1024 bytes apart (stride dimension)
-                        const uint64_t bd = make_smem_desc(sB + s * 32 * 128, Cfg::kAtoms > 1 ? kKTile * 128 : 1024,
-                                                           1024, kLayoutSw128);
+                        // narrow: BN * 2-byte rows, 32B/64B swizzle, 8-row groups 16 * BN bytes apart
+                        const uint64_t bd =
+                            tc_narrow_b(BN, GATHER)
+                                ? make_smem_desc(sB + s * 32 * (BN * 2), 16, 16 * BN, BN == 16 ? kLayoutSw32 : kLayoutSw64)
+                                : make_smem_desc(sB + s * 32 * 128, Cfg::kAtoms > 1 ? kKTile * 128 : 1024, 1024,
+                                                 kLayoutSw128);
                         const uint32_t te = tmem_e + slot * kMetaStageCols + s * kMetaSlotCols;
                         tc_mma_sp_f16(d, ad, bd, te, idesc, (k > 0 || s > 0) ? 1u : 0u);
                     }
@@ -550,7 +559,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
 
 template <int TM, int BN, bool GATHER>
 cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stream) {
-    using Cfg = TcCfg<TM, BN>;
+    using Cfg = TcCfg<TM, BN, tc_narrow_b(BN, GATHER)>;
     auto kern = spmm_tc_kernel<TM, BN, GATHER>;
     constexpr int threads = tc_threads<TM, BN, GATHER>();
     static int per_sm = 0;  // resident CTAs per SM, once per process (the attribute is per function)
@@ -583,15 +592,16 @@ cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, cudaStream_t stream)
 
 }  // namespace
 
-int tc_default_stages(int tile_m, int tile_n) {
+int tc_default_stages(int tile_m, int tile_n, bool gather) {
     if (tile_m != 64 && tile_m != 128) return 0;
     if (tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 && tile_n != 192 && tile_n != 256) return 0;
-    return tc_stages_for(tile_m, tile_n);
+    return tc_stages_for(tile_m, tile_n, tc_narrow_b(tile_n, gather));
 }
 
 cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void* B, int64_t ld_b, int64_t N, void* C,
                            int64_t ld_c, bool c_f32, float* partial, cudaStream_t stream) {
-    if (tc_default_stages(L.tile_m, L.tile_n) == 0 || L.stages != tc_default_stages(L.tile_m, L.tile_n))
+    if (tc_default_stages(L.tile_m, L.tile_n, L.gather) == 0 ||
+        L.stages != tc_default_stages(L.tile_m, L.tile_n, L.gather))
         return cudaErrorInvalidValue;
     TcArgs p;
     p.colidx = static_cast<const uint32_t*>(A.colidx);

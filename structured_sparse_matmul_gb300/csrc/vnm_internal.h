@@ -60,17 +60,23 @@ cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b,
 // Shared-memory pipeline depth of the tensor-core kernel for a tile: as many
 // 128-column stages (B rows, A values, m-indices) as fit next to the staged
 // column-loc words, at most 8.
-__host__ __device__ constexpr int tc_stages_for(int tile_m, int tile_n) {
-    const int stage = ((tile_n + 63) / 64) * 128 * 128 + tile_m * 128 + tile_m * 16;
+// `narrow_b`: B rows loaded by TMA into a tile exactly tile_n wide (tile_n
+// 16 or 32, 32B/64B swizzle) instead of whole 64-column atoms.
+__host__ __device__ constexpr int tc_stages_for(int tile_m, int tile_n, bool narrow_b = false) {
+    const int b_bytes = narrow_b ? 128 * tile_n * 2 : ((tile_n + 63) / 64) * 128 * 128;
+    const int stage = b_bytes + tile_m * 128 + tile_m * 16;
     const int budget = 227 * 1024 - 2 * 1024;  // minus 1 KB alignment slack and 1 KB for barriers
     const int s = budget / stage;
     return s > 8 ? 8 : s;
 }
 
+// B of a tensor-core launch is loaded narrow (see tc_stages_for).
+__host__ __device__ constexpr bool tc_narrow_b(int tile_n, bool gather) { return !gather && tile_n < 64; }
+
 struct TcLaunch {
     CUtensorMap tm_a;   // values, box {64, tile_m}: one stage (4 MMA k-steps), 128B swizzle
     CUtensorMap tm_e;   // m-indices as u32 words, box {4, tile_m}, no swizzle
-    CUtensorMap tm_b;   // B, box {64, 128} (tile) or {64, 1} (gather4), 128B swizzle
+    CUtensorMap tm_b;   // B, box {64, 128}, 128B swizzle; {tile_n, 128}, 32B/64B swizzle when narrow
     int tile_m, tile_n, stages, splits;
     bool gather;        // M > 4: rows of B selected through colidx
     int sm_count;       // persistent grid: at most sm_count x resident CTAs per SM
@@ -85,7 +91,7 @@ cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, in
                                  int64_t ld_c, bool c_f32, cudaStream_t stream);
 
 // Pipeline depth the tensor-core kernel is built with for a tile (0: no such tile).
-int tc_default_stages(int tile_m, int tile_n);
+int tc_default_stages(int tile_m, int tile_n, bool gather);
 
 
 }  // namespace vnm

@@ -94,7 +94,7 @@ def test_tensor_core_tiles(tile_n, V, tile_m):
     check_close(got, _ref(comp, R, K, V, M, B), f"tile_n {tile_n}")
 
 
-@pytest.mark.parametrize("tile_n", [64, 192, 256])
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 192, 256])
 def test_tensor_core_tiles_plain_2to4(tile_n):
     """M = 4 (B rows by TMA, no gather) at several tile widths, ragged N."""
     R, K, N, V, M = 256, 1024, 296, 16, 4
