@@ -147,10 +147,20 @@ struct StreamArgs {
     bool c_f32;
 };
 
+// acc + (float)a * (float)b for the fp16 a, b in the low 16 bits (exact
+// products, one rounding: the same value as converting then fmaf).
+__device__ __forceinline__ float fma_f16(uint32_t a, uint32_t b, float acc) {
+    const unsigned short ha = static_cast<unsigned short>(a & 0xFFFFu), hb = static_cast<unsigned short>(b & 0xFFFFu);
+    asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(acc) : "h"(ha), "h"(hb));
+    return acc;
+}
+
 template <int NB, int RW, int U>
 __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const StreamArgs p) {
     constexpr int kChunk = 32 * U;                       // blocks per chunk
-    constexpr int kStride = 4 * NB + (NB >= 4 ? 8 : 0);  // halves per staged block (padded: spread banks)
+    // staged block: [NB columns][4 slots] halves (a column's 4 slots in 8
+    // bytes), padded for NB >= 4 to spread the banks
+    constexpr int kStride = 4 * NB + (NB >= 4 ? 4 : 0);
     __shared__ __align__(16) __half Bc[kChunk * kStride];
     const int64_t i = blockIdx.x / p.splits;
     const int s = static_cast<int>(blockIdx.x % p.splits);
@@ -195,9 +205,9 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
                 // column-loc byte, clamped so that a corrupt array cannot address past K
                 const uint32_t cb = min((w >> (8 * slot)) & 0xFFu, static_cast<uint32_t>(p.M - 1));
                 const __half* src = p.B + ((j0 + jl) * p.M + cb) * p.ld_b;
-                __half* dst = Bc + jl * kStride + slot * NB;
+                __half* dst = Bc + jl * kStride + slot;
 #pragma unroll
-                for (int n = 0; n < NB; ++n) dst[n] = n < p.N ? src[n] : __float2half_rn(0.f);
+                for (int n = 0; n < NB; ++n) dst[4 * n] = n < p.N ? src[n] : __float2half_rn(0.f);
             }
             __syncthreads();
 #pragma unroll
@@ -207,15 +217,16 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
                     const int64_t jj = j0 + lane + 32 * u;
                     if (jj >= je) continue;
                     const uint32_t code = (mb[t][u] >> (4 * (jj & 1))) & 0xFu;
-                    const float a0 = __half2float(__ushort_as_half(static_cast<unsigned short>(vv[t][u] & 0xFFFFu)));
-                    const float a1 = __half2float(__ushort_as_half(static_cast<unsigned short>(vv[t][u] >> 16)));
-                    const __half* b = Bc + (lane + 32 * u) * kStride;
-                    const __half* b0 = b + (code & 3u) * NB;
-                    const __half* b1 = b + (code >> 2) * NB;
+                    // byte-permute selector of slots s0 = code & 3 (low half) and s1 = code >> 2
+                    const uint32_t sel = ((code & 3u) * 0x22u + 0x10u) | (((code >> 2) * 0x22u + 0x10u) << 8);
+                    const uint32_t a = vv[t][u];
+                    const uint2* b = reinterpret_cast<const uint2*>(Bc + (lane + 32 * u) * kStride);
 #pragma unroll
                     for (int n = 0; n < NB; ++n) {
-                        acc[t][n] = fmaf(a0, __half2float(b0[n]), acc[t][n]);
-                        acc[t][n] = fmaf(a1, __half2float(b1[n]), acc[t][n]);
+                        const uint2 w = b[n];  // the 4 slots of column n
+                        const uint32_t pr = __byte_perm(w.x, w.y, sel);
+                        acc[t][n] = fma_f16(a, pr, acc[t][n]);
+                        acc[t][n] = fma_f16(a >> 16, pr >> 16, acc[t][n]);
                     }
                 }
             }
