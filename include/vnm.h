@@ -66,7 +66,8 @@ typedef enum vnm_dtype { VNM_F16 = 0, VNM_F32 = 1 } vnm_dtype;
 typedef enum vnm_path {
     VNM_PATH_NONE = 0, /* nothing to compute (an empty product) */
     VNM_PATH_TC = 1,   /* tcgen05 2:4 sparse tensor-core MMA, TMEM accumulators */
-    VNM_PATH_SIMT = 2  /* CUDA-core kernel for small N (one warp per row) */
+    VNM_PATH_SIMT = 2  /* CUDA-core kernels: N <= 8 streams each V-block row with the selected rows of
+                          B staged in shared memory (split K); larger N, one warp per row */
 } vnm_path;
 
 /* A launch plan for vnm_spmm. vnm_spmm_plan_query fills one; a caller may
@@ -74,10 +75,11 @@ typedef enum vnm_path {
 typedef struct vnm_spmm_plan {
     int32_t path;      /* a vnm_path */
     int32_t tile_m;    /* TC: rows per CTA tile = MMA M (128; 64 when column-loc changes every 64 rows) */
-    int32_t tile_n;    /* TC: columns of C per CTA tile = MMA N (16..256, multiple of 16) */
+    int32_t tile_n;    /* TC: columns of C per CTA tile = MMA N (16, 32, 64, 128, 192 or 256) */
     int32_t stages;    /* TC: depth of the shared-memory pipeline (one depth is built per tile;
                           0 in a plan passed to vnm_spmm_with_plan means that depth) */
-    int32_t splits;    /* split-K factor over the condensed K (1 = none) */
+    int32_t splits;    /* split-K factor (1 = none): TC over the condensed K, SIMT with N <= 8 over
+                          the blocks of a row; partials go to the workspace */
     int32_t reserved[3];
 } vnm_spmm_plan;
 
@@ -178,7 +180,8 @@ vnm_status vnm_spmm_workspace_size(vnm_matrix A, int64_t N, size_t* bytes);
  * device's SM count). B and C alignment decide whether the tensor-core path
  * is allowed: it needs B 16-byte aligned with ld_b % 8 == 0 and N >= 8, and
  * a block geometry it serves (K/M % 32 == 0, and V % 64 == 0 or M == 4);
- * everything else takes the CUDA-core path.
+ * everything else takes the CUDA-core path (N <= 8: the streaming kernel,
+ * which splits K when the workspace allows).
  * Errors: VNM_ERR_INVALID_ARG.
  */
 vnm_status vnm_spmm_plan_query(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, vnm_dtype c_type,
