@@ -31,7 +31,7 @@ def _nvcc() -> str:
 
 def _inputs() -> List[str]:
     files = [os.path.join(CSRC, s) for s in SOURCES + HEADERS]
-    files.append(os.path.join(ROOT, "include", "vnm.h"))
+    files += [os.path.join(ROOT, "include", h) for h in ("vnm.h", "vnm_testing.h")]
     return files
 
 

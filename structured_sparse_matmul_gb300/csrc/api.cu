@@ -11,6 +11,7 @@
 #include <new>
 
 #include "vnm_internal.h"
+#include "vnm_testing.h"
 
 namespace {
 
@@ -179,7 +180,7 @@ vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void
 }
 
 vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_t ld_b, int64_t N, void* C,
-                    int64_t ld_c, vnm_dtype c_type, void* workspace, cudaStream_t stream) {
+                    int64_t ld_c, vnm_dtype c_type, void* workspace, cudaStream_t stream, int skip_stage = -1) {
     const bool c_f32 = c_type == VNM_F32;
     cudaError_t e = cudaSuccess;
     if (pl.path == VNM_PATH_SIMT) {
@@ -197,6 +198,7 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         L.splits = effective_splits(*A, pl.splits);
         L.gather = A->M > 4;
         L.sm_count = A->sm_count;
+        L.skip_stage = skip_stage;
         const uint64_t vpr = static_cast<uint64_t>(values_per_row(A->K, A->M));
         const uint64_t mp = static_cast<uint64_t>(meta_pitch(A->K, A->M));
         bool ok = encode_2d(&L.tm_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A->values, vpr, A->R, vpr * 2, 64,
@@ -375,6 +377,22 @@ vnm_status vnm_spmm(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, void* 
     if (workspace == nullptr) workspace_bytes = 0;
     vnm_spmm_plan pl = make_plan(*A, B, ld_b, N, workspace_bytes);
     return vnm_spmm_with_plan(A, &pl, B, ld_b, N, C, ld_c, c_type, workspace, workspace_bytes, stream);
+}
+
+vnm_status vnm_testing_spmm_skip_stage(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, void* C, int64_t ld_c,
+                                       vnm_dtype c_type, void* workspace, size_t workspace_bytes, int32_t skip_stage,
+                                       vnm_stream_t stream) {
+    vnm_status st = check_spmm_args(A, B, ld_b, N, C, ld_c, c_type);
+    if (st != VNM_OK) return st;
+    if (workspace == nullptr) workspace_bytes = 0;
+    const vnm_spmm_plan pl = make_plan(*A, B, ld_b, N, workspace_bytes);
+    if (pl.path != VNM_PATH_TC || A->K == 0 || skip_stage < 0) return VNM_ERR_UNSUPPORTED;
+    st = check_device(A);
+    if (st != VNM_OK) return st;
+    st = check_plan(*A, pl, B, ld_b, N, workspace_bytes, workspace);
+    if (st != VNM_OK) return st;
+    return run_spmm(A, pl, B, ld_b, N, C, ld_c, c_type, workspace, reinterpret_cast<cudaStream_t>(stream),
+                    skip_stage);
 }
 
 vnm_status vnm_get_status(vnm_matrix A, vnm_stream_t stream) {

@@ -92,6 +92,7 @@ struct TcArgs {
     int total_tiles;
     int c_f32;
     int vec_store;           // C row starts 16-byte aligned
+    int skip_stage;          // tests of the bounded waits: CTA 0 never issues this stage's loads (-1: none)
     int* status;
 };
 
@@ -246,7 +247,9 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                 const uint32_t sA = sA0 + slot * Cfg::kABytes;
                 const uint32_t sB = sB0 + slot * Cfg::kBBytes;
                 const uint32_t sE = sE0 + slot * Cfg::kEBytes;
-                if (lane == 0) {
+                if (lane == 0 && blockIdx.x == 0 && it == p.skip_stage) {
+                    // test hook: this stage's loads stay unissued, so the waits on it run out
+                } else if (lane == 0) {
                     // one box each for the stage's A values (64 per row) and m-index words
                     mbar_arrive_expect_tx(aeb, Cfg::kABytes + Cfg::kEBytes);
                     tma_load_2d(sA, &tm_a, kt * kValsPerKTile, static_cast<int32_t>(g.m0), aeb);
@@ -623,6 +626,7 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
     const int64_t esz = c_f32 ? 4 : 2;
     p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ld_c * esz) % 16 == 0);
     p.status = A.status;
+    p.skip_stage = L.skip_stage;
     if (splits > 1 && partial == nullptr) return cudaErrorInvalidValue;
     p.n_tiles = static_cast<int>((N + L.tile_n - 1) / L.tile_n);
     p.m_tiles = static_cast<int>((A.R + L.tile_m - 1) / L.tile_m);

@@ -80,6 +80,7 @@ struct TcLaunch {
     int tile_m, tile_n, stages, splits;
     bool gather;        // M > 4: rows of B selected through colidx
     int sm_count;       // persistent grid: at most sm_count x resident CTAs per SM
+    int skip_stage;     // tests of the bounded waits only (-1: none)
 };
 
 // tcgen05 sparse SpMM; with splits > 1 it writes fp32 partials to

@@ -66,9 +66,10 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.vnm_spmm_with_plan.argtypes = [p, ctypes.POINTER(vnm_spmm_plan), p, i64, i64, p, i64, ctypes.c_int, p, sz, p]
     L.vnm_get_status.argtypes = [p, p]
     L.vnm_spmm_noalloc.argtypes = [i64, i64, i32, i32, p, p, p, p, i64, i64, p, i64, ctypes.c_int, p, p]
+    L.vnm_testing_spmm_skip_stage.argtypes = [p, p, i64, i64, p, i64, ctypes.c_int, p, sz, i32, p]
     for name in ("vnm_sizes", "vnm_matrix_create", "vnm_matrix_destroy", "vnm_compress", "vnm_decompress",
                  "vnm_spmm", "vnm_spmm_workspace_size", "vnm_spmm_plan_query", "vnm_spmm_with_plan",
-                 "vnm_get_status", "vnm_spmm_noalloc"):
+                 "vnm_get_status", "vnm_spmm_noalloc", "vnm_testing_spmm_skip_stage"):
         getattr(L, name).restype = ctypes.c_int
     return L
 
@@ -234,6 +235,18 @@ def vnm_spmm_with_plan(A: VnmMatrix, plan: vnm_spmm_plan, B: torch.Tensor, C: to
     _check(lib().vnm_spmm_with_plan(A.handle, ctypes.byref(plan), B.data_ptr() or None, ld_b, N,
                                     C.data_ptr() or None, ld_c, ct, wp, wb, _stream_ptr(stream)),
            "vnm_spmm_with_plan")
+
+
+def vnm_testing_spmm_skip_stage(A: VnmMatrix, B: torch.Tensor, C: torch.Tensor, skip_stage: int,
+                                workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Test support: vnm_spmm with the first CTA's loads of one pipeline stage
+    never issued, so that its bounded waits run out (include/vnm_testing.h)."""
+    N, ld_b, ld_c, ct = _spmm_operands(A, B, C)
+    wp = workspace.data_ptr() if workspace is not None and workspace.numel() else None
+    wb = workspace.numel() * workspace.element_size() if wp else 0
+    _check(lib().vnm_testing_spmm_skip_stage(A.handle, B.data_ptr() or None, ld_b, N, C.data_ptr() or None, ld_c,
+                                             ct, wp, wb, int(skip_stage), _stream_ptr(stream)),
+           "vnm_testing_spmm_skip_stage")
 
 
 def vnm_get_status(A: VnmMatrix, stream=None) -> int:

@@ -1,4 +1,4 @@
-"""The C ABI without a GPU: libvnm loads, exports every function include/vnm.h
+"""The C ABI without a GPU: libvnm loads, exports every function include/*.h
 declares, and its host-only calls (sizes, status strings, argument checks
 that fail before any CUDA call) behave as documented."""
 import ctypes
@@ -11,13 +11,17 @@ import pytest
 import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "vnm.h")
+HEADERS = [os.path.join(ROOT, "include", h) for h in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if h.endswith(".h")]
 
 
 def _declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(vnm_\w+)\s*\(", text, flags=re.M)))
+    names = set()
+    for header in HEADERS:
+        text = open(header).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"^[A-Za-z_][\w \*]*?\b(vnm_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
 
 
 @pytest.fixture(scope="module")
