@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target seconds of oracle work")
     ap.add_argument("--clock-seconds", type=float, default=2.0, help="seconds of load around the timed region")
     ap.add_argument("--no-context", action="store_true", help="skip the dense torch.matmul context timing")
+    ap.add_argument("--e2e-in-streams", type=int, default=1,
+                    help="streams that carry a step's host-to-device copies (row chunks of W, then B)")
     return ap.parse_args()
 
 
@@ -433,38 +435,77 @@ def main():
     roof["traffic"] = profiled_traffic("spmm_tc_kernel" if roof["kernel"].startswith("vnm_spmm") else "compress",
                                        workload_tag(case))
 
-    # end to end: host buffers, copies inside the timed region
+    # end to end: host buffers, copies inside the timed region. Every step
+    # copies its W and B in from pinned host memory and its C out; the steps
+    # are pipelined over three streams (inputs in, compute, result out) and
+    # the rotating device sets, so step i+1's inputs and step i-1's result
+    # move while step i computes. Events order each step's copy -> compute ->
+    # copy and keep a set from being overwritten before its last use is done.
     e2e = None
     if not args.no_e2e:
         W_pin = torch.from_numpy(W_h).pin_memory()
         B_pin = torch.from_numpy(B_h).pin_memory()
-        C_pin = torch.empty((R, N), dtype=c_dtype).pin_memory()
+        C_pin = [torch.empty((R, N), dtype=c_dtype).pin_memory() for _ in range(2)]
         e_steps = max(3, min(steps, 50))
-        s0 = sets[0]
-        for _ in range(2):
-            s0["W"].copy_(W_pin, non_blocking=True)
-            s0["B"].copy_(B_pin, non_blocking=True)
-            vnm.vnm_compress(s0["A"], s0["W"])
-            vnm.vnm_spmm(s0["A"], s0["B"], s0["C"], workspace=s0["ws"])
-            C_pin.copy_(s0["C"], non_blocking=True)
+        n_in = max(1, args.e2e_in_streams)
+        s_ins = [torch.cuda.Stream(dev) for _ in range(n_in)]
+        s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        # W row chunks, one per input stream; B goes with the last one
+        bounds = [R * q // n_in for q in range(n_in + 1)]
+
+        def run_e2e(count):
+            ev_cmp = [None] * count
+            ev_out = [None] * count
+            for i in range(count):
+                st = sets[i % n_sets]
+                prev = i - n_sets  # the step that used this set last
+                for q, s_in in enumerate(s_ins):
+                    if prev >= 0:
+                        s_in.wait_event(ev_cmp[prev])  # its W and B are no longer read
+                    with torch.cuda.stream(s_in):
+                        if bounds[q + 1] > bounds[q]:
+                            st["W"][bounds[q]:bounds[q + 1]].copy_(W_pin[bounds[q]:bounds[q + 1]], non_blocking=True)
+                        if q == n_in - 1:
+                            st["B"].copy_(B_pin, non_blocking=True)
+                    ev_in = torch.cuda.Event()
+                    ev_in.record(s_in)
+                    s_cmp.wait_event(ev_in)
+                if prev >= 0:
+                    s_cmp.wait_event(ev_out[prev])  # its C has been copied out
+                vnm.vnm_compress(st["A"], st["W"], stream=s_cmp)
+                vnm.vnm_spmm(st["A"], st["B"], st["C"], workspace=st["ws"], stream=s_cmp)
+                ev_cmp[i] = torch.cuda.Event()
+                ev_cmp[i].record(s_cmp)
+                s_out.wait_event(ev_cmp[i])
+                with torch.cuda.stream(s_out):
+                    C_pin[i % 2].copy_(st["C"], non_blocking=True)
+                ev_out[i] = torch.cuda.Event()
+                ev_out[i].record(s_out)
+            return ev_out[count - 1]
+
+        run_e2e(min(e_steps, 4))  # warm
         torch.cuda.synchronize(dev)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         dist_barrier(world, dev)
-        e0.record(stream)
-        for i in range(e_steps):
-            s = sets[i % n_sets]
-            s["W"].copy_(W_pin, non_blocking=True)
-            s["B"].copy_(B_pin, non_blocking=True)
-            vnm.vnm_compress(s["A"], s["W"])
-            vnm.vnm_spmm(s["A"], s["B"], s["C"], workspace=s["ws"])
-            C_pin.copy_(s["C"], non_blocking=True)
-        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e0.record(s_cmp)
+        for s_ in s_ins + [s_out]:
+            s_.wait_event(e0)
+        last = run_e2e(e_steps)
+        s_out.wait_event(last)
+        e1.record(s_out)
         torch.cuda.synchronize(dev)
         e_ms = dist_max(e0.elapsed_time(e1), world, dev)
+        for s_ in sets:
+            st_ = vnm.vnm_get_status(s_["A"])
+            if st_ != vnm.VNM_OK:
+                raise RuntimeError(f"kernel status {vnm.status_string(st_)} during the end-to-end leg")
         e2e = {"value": dense_flops * e_steps * world / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-               "h2d_bytes_per_step": int(W_h.nbytes + B_h.nbytes), "d2h_bytes_per_step": int(C_pin.numel() * C_pin.element_size()),
-               "steps": e_steps, "ms_per_step": e_ms / e_steps}
+               "h2d_bytes_per_step": int(W_h.nbytes + B_h.nbytes),
+               "d2h_bytes_per_step": int(C_pin[0].numel() * C_pin[0].element_size()),
+               "steps": e_steps, "ms_per_step": e_ms / e_steps,
+               "pipelined": f"inputs in ({n_in} streams) / compute / result out, overlapped across steps"}
 
     # context: dense torch.matmul on the same shape (fp16 in, fp32 accumulate)
     ctx = {}
