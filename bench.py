@@ -205,19 +205,49 @@ def time_oracle(case, seconds: float):
 # --------------------------------------------------------------------------- reference arm
 
 def run_reference(args, case):
+    """The oracle as it stands, on the host: W untimed warm-up steps, then K
+    timed steps, each a bounded sample of the workload (whole V-block rows
+    of compress + fp32 SpMM), sized so that all K + W steps take about 2.5
+    minutes (at most --cpu-seconds each)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    cb = time_oracle(case, args.cpu_seconds)
-    step_s = cb["seconds"]
+    import numpy as np
+
+    import oracle
+    from structured_sparse_matmul_gb300 import inputs, workloads
+
+    V = case.V
+    budget = max(0.05, min(args.cpu_seconds, 150.0 / max(1, args.steps + args.warmup)))
+    B = inputs.normal_f16((case.K, case.N), case.seed, case.b_stream, workloads.B_SIGMA)
+
+    def sample(blocks):
+        rows = blocks * V
+        W = inputs.normal_f16((rows, case.K), case.seed, case.a_stream, workloads.A_SIGMA)
+        t0 = time.perf_counter()
+        values, meta, colidx = oracle.compress(W, V, case.M)
+        oracle.spmm(values, meta, colidx, rows, case.K, V, case.M, B)
+        return time.perf_counter() - t0
+
+    t1 = sample(1)
+    blocks = max(1, min(case.R // V, int(budget / max(t1, 1e-6))))
+    for _ in range(args.warmup):
+        sample(blocks)
+    total = 0.0
+    for _ in range(max(1, args.steps)):
+        total += sample(blocks)
+    steps = max(1, args.steps)
+    flops = 2.0 * blocks * V * case.N * case.K * steps
+    value = flops / total / 1e12
+    desc = (f"compress + fp32 SpMM of rows 0..{blocks * V - 1} ({blocks} of {case.R // V} V-block rows) of "
+            f"{case.R}x{case.K}x{case.N} per step, single-threaded, {total / steps:.3f} s a step")
     line = {
-        "impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "TFLOP/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": total / steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": config_of(case, None),
-        "cpu_baseline": {k: cb[k] for k in ("value", "unit", "cores", "kind", "sample")},
-        "e2e": {"value": cb["value"], "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-        "note": "one bounded oracle sample per run (the oracle is a deliberately slow checker)",
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
