@@ -767,6 +767,160 @@ __global__ void __launch_bounds__(kColsWarps * 32, (MB == 16 && RPL == 4) ? 1 : 
     }
 }
 
+// Warp-tile compress for M in {8, 16} when a lane can hold all its rows
+// (RPL = V/4 rows, RPL * M/8 16-byte chunks <= 16): each warp owns blocks
+// (i, j0 .. j0+7) over all V rows on its own, with warp-level
+// synchronisation only. Lane (b, g) = (lane % 8, lane / 8) holds rows
+// r = g + 4t of block j0 + b in registers; the column sums are reduced over g
+// by shuffles, handed to the ranking lanes (32/M blocks per pass, lane =
+// M * group + column) through the warp's shared-memory slot, and the 2-of-4
+// step runs from the registers.
+constexpr int kTileWarps = 4;  // warp tiles per CTA (consecutive along a block row)
+
+template <int MB, int RPL>
+__global__ void __launch_bounds__(kTileWarps * 32) compress_warp_kernel(const CompressArgs p) {
+    constexpr int kVec = MB / 8;
+    constexpr int kNW = MB / 2;
+    constexpr int kGroups = 32 / MB;
+    __shared__ float s_sum[kTileWarps][kColsBlocks][MB];
+    __shared__ uint32_t s_sel[kTileWarps][kColsBlocks];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = lane & 7, g = lane >> 3;
+    const int64_t i = static_cast<int64_t>(blockIdx.z) * 65535 + blockIdx.y;
+    const int64_t j0 = (static_cast<int64_t>(blockIdx.x) * kTileWarps + warp) * kColsBlocks;
+    if (i >= p.R / p.V || j0 >= p.nblk) return;  // the whole warp; no CTA barrier follows
+    const int64_t j = j0 + b;
+    const bool valid = j < p.nblk;
+    const int V = p.V;
+    const int64_t ld = p.ld_w;
+    const uint16_t* Wrow = p.W + (i * V) * ld;
+    const uint16_t* Wb = Wrow + (valid ? j : 0) * MB;
+
+    // ---- pass 1: all rows of this lane in flight, column sums
+    uint4 x[RPL][kVec];
+#pragma unroll
+    for (int t = 0; t < RPL; ++t) {
+        const int r = g + 4 * t;
+        const bool act = valid && r < V;
+#pragma unroll
+        for (int v = 0; v < kVec; ++v)
+            x[t][v] = act ? __ldg(reinterpret_cast<const uint4*>(Wb + r * ld) + v) : make_uint4(0, 0, 0, 0);
+    }
+    float sum[MB];
+#pragma unroll
+    for (int c = 0; c < MB; ++c) sum[c] = 0.f;
+#pragma unroll
+    for (int t = 0; t < RPL; ++t) {
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+            const uint32_t w4[4] = {x[t][v].x & 0x7FFF7FFFu, x[t][v].y & 0x7FFF7FFFu, x[t][v].z & 0x7FFF7FFFu,
+                                    x[t][v].w & 0x7FFF7FFFu};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                add_f16(sum[8 * v + 2 * h], w4[h]);
+                add_f16(sum[8 * v + 2 * h + 1], w4[h] >> 16);
+            }
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < MB; ++c) {
+        sum[c] += __shfl_xor_sync(0xFFFFFFFFu, sum[c], 8);
+        sum[c] += __shfl_xor_sync(0xFFFFFFFFu, sum[c], 16);
+    }
+    if (g == 0) {
+#pragma unroll
+        for (int c = 0; c < MB; ++c) s_sum[warp][b][c] = sum[c];
+    }
+    __syncwarp();
+
+    // ---- ranking: 32/M blocks per pass
+    for (int pass = 0; pass < kColsBlocks / kGroups; ++pass) {
+        const int grp = lane / MB, c = lane % MB;
+        const int blk = pass * kGroups + grp;
+        const bool has = j0 + blk < p.nblk;
+        const uint32_t gshift = static_cast<uint32_t>(grp * MB);
+        const uint32_t gbits = (1u << MB) - 1u;
+        const float s = s_sum[warp][blk][c];
+        const bool any_bad = ((__ballot_sync(0xFFFFFFFFu, has && !(s <= 3.4e38f)) >> gshift) & gbits) != 0;
+        int rk = 0;
+#pragma unroll
+        for (int c2 = 0; c2 < MB; ++c2) {
+            const float o = __shfl_sync(0xFFFFFFFFu, s, c2, MB);
+            rk += (o > s) || (o == s && c2 < c);
+        }
+        uint32_t mask = (__ballot_sync(0xFFFFFFFFu, rk < 4) >> gshift) & gbits;
+        const int l3 = __ffs((__ballot_sync(0xFFFFFFFFu, rk == 3) >> gshift) & gbits) - 1;
+        const int l4 = __ffs((__ballot_sync(0xFFFFFFFFu, rk == 4) >> gshift) & gbits) - 1;
+        const float v3 = __shfl_sync(0xFFFFFFFFu, s, l3 & (MB - 1), MB);
+        const float v4 = __shfl_sync(0xFFFFFFFFu, s, l4 & (MB - 1), MB);
+        const bool safe = !any_bad && l3 >= 0 && l4 >= 0 &&
+                          (v3 - v4 > 2.5f * static_cast<float>(V) * 5.9604645e-8f * v3);
+        if (__any_sync(0xFFFFFFFFu, has && !safe)) {
+            uint64_t e = 0;
+            if (has) {
+                const uint16_t* col = Wrow + (j0 + blk) * MB + c;
+                for (int r = 0; r < V; ++r) e += mag_units(col[r * ld]);
+            }
+            int rk2 = 0;
+#pragma unroll
+            for (int c2 = 0; c2 < MB; ++c2) {
+                const uint32_t lo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(e), c2, MB);
+                const uint32_t hi = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(e >> 32), c2, MB);
+                const uint64_t o = (static_cast<uint64_t>(hi) << 32) | lo;
+                rk2 += (o > e) || (o == e && c2 < c);
+            }
+            const uint32_t m2 = (__ballot_sync(0xFFFFFFFFu, rk2 < 4) >> gshift) & gbits;
+            if (!safe) mask = m2;
+        }
+        if (has && c == 0) {
+            const uint32_t sel = mask_to_cols(mask);
+            s_sel[warp][blk] = sel;
+            p.colidx[i * p.nblk + j0 + blk] = sel;
+            if (any_bad) record_error(p.status, VNM_ERR_NONFINITE, 6);
+        }
+    }
+    __syncwarp();
+
+    // ---- pass 2: 2 of the 4 selected values per row, from the registers
+    const uint32_t sel = valid ? s_sel[warp][b] : 0x03020100u;
+    const int col0 = sel & 0xFF, col1 = (sel >> 8) & 0xFF, col2 = (sel >> 16) & 0xFF, col3 = sel >> 24;
+    const uint32_t bs0 = half_selector(col0), bs1 = half_selector(col1), bs2 = half_selector(col2),
+                   bs3 = half_selector(col3);
+    const bool pair_lo = (j & 1) == 0;
+#pragma unroll
+    for (int t = 0; t < RPL; ++t) {
+        const int r = g + 4 * t;
+        const bool act = valid && r < V;
+        uint32_t w[kNW];
+#pragma unroll
+        for (int v = 0; v < kVec; ++v) {
+            w[4 * v] = x[t][v].x;
+            w[4 * v + 1] = x[t][v].y;
+            w[4 * v + 2] = x[t][v].z;
+            w[4 * v + 3] = x[t][v].w;
+        }
+        uint32_t xx, yy;
+        pair_of<kNW>(w, col0 >> 2, xx, yy);
+        const uint32_t h0 = __byte_perm(xx, yy, bs0);
+        pair_of<kNW>(w, col1 >> 2, xx, yy);
+        const uint32_t h1 = __byte_perm(xx, yy, bs1);
+        pair_of<kNW>(w, col2 >> 2, xx, yy);
+        const uint32_t h2 = __byte_perm(xx, yy, bs2);
+        pair_of<kNW>(w, col3 >> 2, xx, yy);
+        const uint32_t h3 = __byte_perm(xx, yy, bs3);
+        const uint32_t P = __byte_perm(h0, h1, 0x5410u), Q = __byte_perm(h2, h3, 0x5410u);
+        uint32_t vals;
+        uint32_t code = keep2of4_packed(P, Q, vals);
+        if (!act) code = 0;
+        const uint32_t other = __shfl_xor_sync(0xFFFFFFFFu, code, 1);  // the neighbouring block's code
+        if (act) {
+            const int64_t row = i * V + r;
+            *reinterpret_cast<uint32_t*>(p.values + row * (2 * p.nblk) + 2 * j) = vals;
+            if (pair_lo) p.meta[row * p.mpitch + (j >> 1)] = static_cast<uint8_t>(code | (other << 4));
+        }
+    }
+}
+
 template <int MB>
 void launch_cols(const CompressArgs& p, dim3 grid, cudaStream_t stream) {
     const int V = p.V;
@@ -884,8 +1038,24 @@ cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, 
     // M in {8, 16, 32}: eight blocks x V rows per CTA, no staging
     if ((A.M == 8 || A.M == 16 || A.M == 32) && reinterpret_cast<uintptr_t>(W) % 16 == 0 && ld_w % 8 == 0) {
         const int64_t rows = A.R / A.V;  // block rows: grid y (then z past 65535)
-        const dim3 grid(static_cast<unsigned>((p.nblk + kColsBlocks - 1) / kColsBlocks),
-                        static_cast<unsigned>(std::min<int64_t>(rows, 65535)),
+        const int64_t tiles = (p.nblk + kColsBlocks - 1) / kColsBlocks;
+        // one warp per tile when a lane holds all its rows (V <= 64 at M = 8, V <= 32 at M = 16)
+        if ((A.M == 8 && A.V <= 64 && A.V % 4 == 0) || (A.M == 16 && A.V <= 32 && A.V % 4 == 0)) {
+            const dim3 wgrid(static_cast<unsigned>((tiles + kTileWarps - 1) / kTileWarps),
+                             static_cast<unsigned>(std::min<int64_t>(rows, 65535)),
+                             static_cast<unsigned>((rows + 65534) / 65535));
+            const unsigned th = kTileWarps * 32;
+            if (A.M == 8) {
+                if (A.V <= 16) compress_warp_kernel<8, 4><<<wgrid, th, 0, stream>>>(p);
+                else if (A.V <= 32) compress_warp_kernel<8, 8><<<wgrid, th, 0, stream>>>(p);
+                else compress_warp_kernel<8, 16><<<wgrid, th, 0, stream>>>(p);
+            } else {
+                if (A.V <= 16) compress_warp_kernel<16, 4><<<wgrid, th, 0, stream>>>(p);
+                else compress_warp_kernel<16, 8><<<wgrid, th, 0, stream>>>(p);
+            }
+            return cudaGetLastError();
+        }
+        const dim3 grid(static_cast<unsigned>(tiles), static_cast<unsigned>(std::min<int64_t>(rows, 65535)),
                         static_cast<unsigned>((rows + 65534) / 65535));
         if (A.M == 8) launch_cols<8>(p, grid, stream);
         else if (A.M == 16) launch_cols<16>(p, grid, stream);
