@@ -254,3 +254,16 @@ def test_streaming_at_n8_by_plan():
     plan.splits = 3
     got, _ = run_spmm(A, B, plan=plan)
     check_close(got, _ref(comp, R, K, V, M, B), "stream N=8")
+
+
+@pytest.mark.parametrize("R,K,N,V,M", [(1024, 4096, 512, 64, 8),   # tensor cores, gathered B
+                                       (256, 2560, 40, 128, 4),    # tensor cores, split K
+                                       (512, 4096, 3, 64, 8)])     # streaming small N, split K
+def test_repeatable_bit_for_bit(R, K, N, V, M):
+    """The same inputs give the same C bit for bit (fixed accumulation and
+    split-K reduction orders)."""
+    A, B, _ = _setup(R, K, N, V, M, seed=31)
+    first, _ = run_spmm(A, B)
+    for _ in range(2):
+        again, _ = run_spmm(A, B)
+        assert np.array_equal(first.view(np.uint32), again.view(np.uint32))
