@@ -80,7 +80,12 @@ typedef struct vnm_spmm_plan {
                           0 in a plan passed to vnm_spmm_with_plan means that depth) */
     int32_t splits;    /* split-K factor (1 = none): TC over the condensed K, SIMT with N <= 8 over
                           the blocks of a row; partials go to the workspace */
-    int32_t reserved[3];
+    int32_t cluster;   /* TC with B loaded by TMA (M == 4): CTAs per thread-block cluster (0 or 1 =
+                          none; 2 or 4 with tile_m 128, tile_n 128, 192 or 256 and a whole number of
+                          clusters over the row tiles); the CTAs of a cluster take consecutive
+                          row tiles of one column tile and each loads 1/cluster of every B tile,
+                          multicast to all of them */
+    int32_t reserved[2];
 } vnm_spmm_plan;
 
 /* Opaque handle of one compressed matrix. It records R, K, V, M and the

@@ -108,6 +108,70 @@ def test_tensor_core_tiles_plain_2to4(tile_n):
     check_close(got, _ref(comp, R, K, V, M, B), f"plain 2:4 tile_n {tile_n}")
 
 
+@pytest.mark.parametrize("cluster", [2, 4])
+@pytest.mark.parametrize("tile_n", [128, 192, 256])
+def test_tensor_core_clusters(cluster, tile_n):
+    """M = 4 with clusters of CTAs on consecutive row tiles sharing every B
+    tile by TMA multicast: ragged rows (the last row tile half empty), ragged
+    N, both C types."""
+    R, K, N, V, M = 960, 1024, 424, 64, 4
+    A, B, comp = _setup(R, K, N, V, M, seed=31)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    assert plan.path == vnm.VNM_PATH_TC and plan.tile_m == 128
+    plan.tile_n = tile_n
+    plan.stages = 0
+    plan.splits = 1
+    plan.cluster = cluster
+    ref = _ref(comp, R, K, V, M, B)
+    for c_dtype in (torch.float16, torch.float32):
+        got, _ = run_spmm(A, B, c_dtype, plan=plan)
+        check_close(got, ref, f"cluster {cluster} tile_n {tile_n}")
+
+
+@pytest.mark.parametrize("cluster", [2, 4])
+def test_tensor_core_clusters_persistent(cluster):
+    """Many more tile groups than resident clusters (each cluster walks
+    several), checked on sampled rows; and clusters with split K."""
+    R, K, N, V, M = 4096, 1024, 2048, 128, 4
+    A, B, comp = _setup(R, K, N, V, M, seed=32)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    plan.tile_n = 128
+    plan.stages = 0
+    plan.splits = 1
+    plan.cluster = cluster
+    got, _ = run_spmm(A, B, plan=plan)
+    rows = sample_rows(R, V, 40)
+    check_close(got[rows], _ref(comp, R, K, V, M, B, rows=rows), f"cluster {cluster} persistent")
+
+    R, K, N = 512, 4096, 136
+    A, B, comp = _setup(R, K, N, V, M, seed=33)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    plan.tile_n = 128
+    plan.stages = 0
+    plan.splits = 3
+    plan.cluster = cluster
+    got, _ = run_spmm(A, B, torch.float32, plan=plan)
+    check_close(got, _ref(comp, R, K, V, M, B), f"cluster {cluster} split K")
+
+
+def test_cluster_plans_rejected():
+    """Clusters need TMA-loaded B (M = 4), 128-row tiles, tile_n >= 128 and a
+    whole number of clusters over the row tiles."""
+    cases = [((384, 512, 128, 128, 4), {"cluster": 2}),                  # 3 row tiles
+             ((512, 512, 128, 128, 4), {"cluster": 3}),
+             ((512, 512, 128, 128, 4), {"cluster": 2, "tile_n": 64}),
+             ((512, 1024, 256, 128, 8), {"cluster": 2})]                 # gathered B
+    for (R, K, N, V, M), edits in cases:
+        A, B, _ = _setup(R, K, N, V, M, seed=34)
+        plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+        plan.stages = 0
+        for k, v in edits.items():
+            setattr(plan, k, v)
+        with pytest.raises(vnm.VnmError) as e:
+            run_spmm(A, B, plan=plan)
+        assert e.value.code == vnm.VNM_ERR_UNSUPPORTED, (R, K, N, V, M, edits)
+
+
 @pytest.mark.parametrize("splits", [2, 3, 5])
 def test_tensor_core_split_k(splits):
     R, K, N, V, M = 256, 2560, 40, 128, 4
