@@ -129,8 +129,12 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     pl.path = VNM_PATH_TC;
     pl.tile_m = tc_tile_m_ok(A, 128) ? 128 : 64;
     // gathering (M > 4): 256-column tiles when N allows (twice the MMA work per
-    // stage for the same per-stage costs); plain 2:4: 128 (finer waves)
-    pl.tile_n = (A.M > 4 && N >= 256) ? 256 : N >= 128 ? 128 : static_cast<int32_t>(ceil_div(N, 16) * 16);
+    // stage for the same per-stage costs); plain 2:4: 192 for wide B (three
+    // pipeline stages of 66 KB and two accumulators), else 128 (finer waves)
+    if (A.M == 4 && N >= 1024)
+        pl.tile_n = 192;
+    else
+        pl.tile_n = (A.M > 4 && N >= 256) ? 256 : N >= 128 ? 128 : static_cast<int32_t>(ceil_div(N, 16) * 16);
     if (pl.tile_n > 64 && pl.tile_n < 128) pl.tile_n = 128;
     if (pl.tile_n > 32 && pl.tile_n < 64) pl.tile_n = 64;
     if (pl.tile_n > 16 && pl.tile_n < 32) pl.tile_n = 32;
@@ -144,6 +148,11 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     if (splits > 1) splits = std::min<int64_t>(splits, static_cast<int64_t>(workspace_bytes) / per_split);
     splits = std::max<int64_t>(1, splits);
     pl.splits = static_cast<int32_t>(std::max<int64_t>(1, splits));
+    // B by TMA over whole waves of tiles: pairs of CTAs on consecutive row
+    // tiles share each B tile (multicast), halving its L2 reads
+    pl.cluster = 1;
+    if (A.M == 4 && pl.tile_m == 128 && pl.tile_n >= 128 && pl.splits == 1 && ceil_div(A.R, 128) % 2 == 0)
+        pl.cluster = 2;
     return pl;
 }
 

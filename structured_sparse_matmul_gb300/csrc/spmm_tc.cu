@@ -88,14 +88,14 @@ struct TcArgs {
     int64_t nblk;
     int num_kt;              // condensed K / kKTile
     int kt_per_split;
-    int n_tiles, m_tiles;    // tile grid
-    int m_groups;            // m_tiles / CS: tile (group) t -> n = t % n_tiles, m-group = t / n_tiles % m_groups,
-                             // split = t / n_tiles / m_groups; CTA rank r of a cluster takes m = m-group * CS + r
-    int total_tiles;         // groups
+    int n_tiles, m_tiles;    // tile grid; CS = 1: tile t -> (n = t % n_tiles, m = t / n_tiles % m_tiles, split)
+    int total_tiles;         // tiles (CS = 1) or tile groups
     int c_f32;
     int vec_store;           // C row starts 16-byte aligned
     int skip_stage;          // tests of the bounded waits: CTA 0 never issues this stage's loads (-1: none)
     int* status;
+    int m_groups;            // m_tiles / CS: group t -> n = t % n_tiles, m-group = t / n_tiles % m_groups,
+                             // split = t / n_tiles / m_groups; CTA rank r of a cluster takes m = m-group * CS + r
 };
 
 __host__ __device__ constexpr int pow2_at_least(int x) {
@@ -151,13 +151,35 @@ struct TileGeom {
     int kt0, nkt;    // first stage (of kKTile condensed columns) and stage count
 };
 
+// First tile (group) of this CTA (cluster) and the stride between its tiles.
+template <int CS>
+__device__ __forceinline__ int tile_first() {
+    if constexpr (CS == 1)
+        return static_cast<int>(blockIdx.x);
+    else
+        return static_cast<int>(cluster_index_x());
+}
+template <int CS>
+__device__ __forceinline__ int tile_step() {
+    if constexpr (CS == 1)
+        return static_cast<int>(gridDim.x);
+    else
+        return static_cast<int>(cluster_count_x());
+}
+
 template <int TM, int BN, int CS>
 __device__ __forceinline__ TileGeom tile_geom(const TcArgs& p, int t, int rank) {
     TileGeom g;
     const int n_idx = t % p.n_tiles;
     const int rest = t / p.n_tiles;
-    const int m_idx = (rest % p.m_groups) * CS + rank;
-    g.split = rest / p.m_groups;
+    int m_idx;
+    if constexpr (CS == 1) {
+        m_idx = rest % p.m_tiles;
+        g.split = rest / p.m_tiles;
+    } else {
+        m_idx = (rest % p.m_groups) * CS + rank;
+        g.split = rest / p.m_groups;
+    }
     g.m0 = static_cast<int64_t>(m_idx) * TM;
     g.n0 = static_cast<int64_t>(n_idx) * BN;
     g.kt0 = g.split * p.kt_per_split;
@@ -204,8 +226,6 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    const int t_first = CS > 1 ? static_cast<int>(cluster_index_x()) : static_cast<int>(blockIdx.x);
-    const int t_step = CS > 1 ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
     constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CS) - 1u);
 
     if (threadIdx.x == 0) {
@@ -248,7 +268,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         for (int s = 0; s < STAGES; ++s) last_it[s] = -1;
         int it = 0;
         bool run = true;
-        for (int t = t_first; run && t < p.total_tiles; t += t_step) {
+        for (int t = tile_first<CS>(); run && t < p.total_tiles; t += tile_step<CS>()) {
             const TileGeom g = tile_geom<TM, BN, CS>(p, t, rank);
             for (int k = 0; k < g.nkt; ++k, ++it) {
                 const int slot = it % STAGES;
@@ -310,7 +330,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             constexpr uint32_t idesc = make_idesc_f16_f32(TM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/true);
             int it = 0, ti = 0;
             bool run = true;
-            for (int t = t_first; run && t < p.total_tiles; t += t_step, ++ti) {
+            for (int t = tile_first<CS>(); run && t < p.total_tiles; t += tile_step<CS>(), ++ti) {
                 const TileGeom g = tile_geom<TM, BN, CS>(p, t, rank);
                 const int buf = ti % ACC;
                 const uint32_t use = static_cast<uint32_t>(ti / ACC) & 1u;
@@ -367,7 +387,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         int it = 0;
         bool run = true;
-        for (int t = t_first; run && t < p.total_tiles; t += t_step) {
+        for (int t = tile_first<CS>(); run && t < p.total_tiles; t += tile_step<CS>()) {
             const TileGeom g = tile_geom<TM, BN, CS>(p, t, rank);
             const bool pad = trow < 0 || g.m0 + trow >= p.R;  // lanes with no row act as padding
             for (int k = 0; k < g.nkt; ++k, ++it) {
@@ -408,7 +428,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         const int trow = tile_row_of_lane<TM>(q, lane);
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         int ti = 0;
-        for (int t = t_first; t < p.total_tiles; t += t_step, ++ti) {
+        for (int t = tile_first<CS>(); t < p.total_tiles; t += tile_step<CS>(), ++ti) {
             const TileGeom g = tile_geom<TM, BN, CS>(p, t, rank);
             const int buf = ti % ACC;
             const uint32_t use = static_cast<uint32_t>(ti / ACC) & 1u;
@@ -496,7 +516,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             bool valid;
         };
         auto it_start = [&](StageIt& x) {
-            x.t = t_first;
+            x.t = tile_first<CS>();
             x.k = 0;
             x.valid = x.t < p.total_tiles;
             if (x.valid) x.g = tile_geom<TM, BN, CS>(p, x.t, rank);
@@ -504,7 +524,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         auto it_next = [&](StageIt& x) {
             if (++x.k == x.g.nkt) {
                 x.k = 0;
-                x.t += t_step;
+                x.t += tile_step<CS>();
                 x.valid = x.t < p.total_tiles;
                 if (x.valid) x.g = tile_geom<TM, BN, CS>(p, x.t, rank);
             }
@@ -638,6 +658,10 @@ cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stre
     }
     // p.total_tiles counts tile groups of CS m-tiles
     const int64_t units = std::min<int64_t>(p.total_tiles, resident);
+    if constexpr (CS == 1) {
+        kern<<<static_cast<unsigned>(units), threads, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_e, L.tm_b, p);
+        return cudaGetLastError();
+    }
     cfg.gridDim = dim3(static_cast<unsigned>(units * CS));
     return cudaLaunchKernelEx(&cfg, kern, L.tm_a, L.tm_e, L.tm_b, p);
 }

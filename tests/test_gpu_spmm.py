@@ -104,6 +104,7 @@ def test_tensor_core_tiles_plain_2to4(tile_n):
     plan.tile_n = tile_n
     plan.stages = 0
     plan.splits = 1
+    plan.cluster = 1  # one CTA per tile (the default plan pairs CTAs for wide tiles)
     got, _ = run_spmm(A, B, plan=plan)
     check_close(got, _ref(comp, R, K, V, M, B), f"plain 2:4 tile_n {tile_n}")
 
