@@ -187,6 +187,66 @@ __device__ __forceinline__ TileGeom tile_geom(const TcArgs& p, int t, int rank) 
     return g;
 }
 
+// Columns [c0, c1) of this warp's lanes of an accumulator (TMEM address
+// `tacc`: the buffer's column 0 in this warp's lane quarter) -> registers ->
+// C (fp16, RNE, or fp32) or the split-K partials; `row` is this thread's row
+// of C (>= R: none). Each thread writes whole 32-byte sectors of its row.
+template <int BN>
+__device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g, uint32_t tacc, int64_t row, int c0,
+                                              int c1) {
+    // one 16-column chunk of this thread's row: fp32 partials, fp32 or fp16 C
+    auto store16 = [&](const uint32_t (&v)[16], int c) {
+        const int64_t col = g.n0 + c;
+        if (row >= p.R || col >= p.N) return;
+        const bool full = col + 16 <= p.N;
+        if (p.partial != nullptr) {
+            float* dst = p.partial + (static_cast<int64_t>(g.split) * p.R + row) * p.N + col;
+            if (full && (p.N % 4) == 0) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    reinterpret_cast<uint4*>(dst)[u] = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            } else {
+                for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u] = __uint_as_float(v[u]);
+            }
+        } else if (p.c_f32) {
+            float* dst = static_cast<float*>(p.C) + row * p.ld_c + col;
+            if (full && p.vec_store) {
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    reinterpret_cast<uint4*>(dst)[u] = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+            } else {
+                for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u] = __uint_as_float(v[u]);
+            }
+        } else {
+            __half* dst = static_cast<__half*>(p.C) + row * p.ld_c + col;
+            uint32_t h[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const __half2 t2 = __floats2half2_rn(__uint_as_float(v[2 * u]), __uint_as_float(v[2 * u + 1]));
+                h[u] = *reinterpret_cast<const uint32_t*>(&t2);
+            }
+            if (full && p.vec_store) {
+                reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
+            } else {
+                for (int u = 0; u < 16 && col + u < p.N; ++u)
+                    dst[u] = __float2half_rn(__uint_as_float(v[u]));
+            }
+        }
+    };
+    // two TMEM loads in flight per wait
+    constexpr int kEpiStep = BN >= 32 ? 32 : 16;
+#pragma unroll 1
+    for (int c = c0; c < c1; c += kEpiStep) {
+        uint32_t v0[16], v1[16];
+        tmem_ld_32x32b_x16(tacc + c, v0);
+        if (kEpiStep == 32) tmem_ld_32x32b_x16(tacc + c + 16, v1);
+        tmem_wait_ld();
+        store16(v0, c);
+        if (kEpiStep == 32) store16(v1, c + 16);
+    }
+}
+
 // Persistent: CTA b takes tiles b, b + gridDim.x, ... (all roles walk the
 // same sequence, so their stage and accumulator counters agree).
 // CS > 1 (B by TMA only): clusters of CS CTAs on CS consecutive m-tiles of
@@ -205,6 +265,14 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     constexpr int STAGES = Cfg::kStages;
     constexpr int ACC = Cfg::kAccBufs;
     constexpr int kGatherThreads = gather_threads(TM, BN);
+    // With a single accumulator the next tile's MMAs wait for the whole
+    // drain, so for 64-row tiles (16 rows per warp: the drain is bound by
+    // TMEM load latency, not by the stores) the m-index warps, idle then,
+    // drain the upper half of the columns while the epilogue warps drain the
+    // lower half. (128-row tiles measured slower this way: their drain is
+    // bound by the stores, and the next tile's m-indices wait.)
+    constexpr bool kSplitEpi = ACC == 1 && BN >= 64 && TM == 64;
+    constexpr int kEpiCols = kSplitEpi ? BN / 2 : BN;  // columns [0, kEpiCols) drained by the epilogue warps
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t ae_bar[STAGES];     // A values and m-indices landed (TMA)
     __shared__ __align__(8) uint64_t b_bar[STAGES];      // B rows landed (TMA, or every gather thread)
@@ -237,7 +305,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         }
         for (int b = 0; b < ACC; ++b) {
             mbar_init(smem_u32(&accf_bar[b]), 1);
-            mbar_init(smem_u32(&acce_bar[b]), 4);
+            mbar_init(smem_u32(&acce_bar[b]), kSplitEpi ? 8 : 4);
         }
         mbar_init(smem_u32(&done_bar), 1);
         abort_flag = 0;
@@ -387,8 +455,27 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         int it = 0;
         bool run = true;
-        for (int t = tile_first<CS>(); run && t < p.total_tiles; t += tile_step<CS>()) {
+        // upper half of tile ti's accumulator (single buffer: use ti & 1), when the split applies
+        auto drain_upper = [&](const TileGeom& g, int ti) -> bool {
+            const bool ok = mbar_wait_warp(smem_u32(&accf_bar[0]), static_cast<uint32_t>(ti) & 1u, abort, kSleepMeta) &&
+                            !*abort;
+            if (!ok) return false;
+            tc_fence_after_sync();
+            drain_columns<BN>(p, g, tmem_acc + lane_addr, trow >= 0 ? g.m0 + trow : p.R, kEpiCols, BN);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acce_bar[0]));
+            return true;
+        };
+        TileGeom prev;
+        int ti = 0;
+        for (int t = tile_first<CS>(); run && t < p.total_tiles; t += tile_step<CS>(), ++ti) {
             const TileGeom g = tile_geom<TM, BN, CS>(p, t, rank);
+            if (kSplitEpi && ti > 0 && !drain_upper(prev, ti - 1)) {
+                run = false;
+                break;
+            }
+            prev = g;
             const bool pad = trow < 0 || g.m0 + trow >= p.R;  // lanes with no row act as padding
             for (int k = 0; k < g.nkt; ++k, ++it) {
                 const int slot = it % STAGES;
@@ -422,6 +509,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                 if (lane == 0) mbar_arrive(smem_u32(&meta_bar[slot]));
             }
         }
+        if (kSplitEpi && run && ti > 0) drain_upper(prev, ti - 1);
     } else if (warp < kTcWarpsFixed) {
         // ------------------------------------------------ epilogue (warps 6-9)
         const int q = warp & 3;
@@ -436,57 +524,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             if (!ok) break;
             tc_fence_after_sync();
             const int64_t row = trow >= 0 ? g.m0 + trow : p.R;
-            // one 16-column chunk of this thread's row: fp32 partials, fp32 or fp16 C
-            auto store16 = [&](const uint32_t (&v)[16], int c) {
-                const int64_t col = g.n0 + c;
-                if (row >= p.R || col >= p.N) return;
-                const bool full = col + 16 <= p.N;
-                if (p.partial != nullptr) {
-                    float* dst = p.partial + (static_cast<int64_t>(g.split) * p.R + row) * p.N + col;
-                    if (full && (p.N % 4) == 0) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            reinterpret_cast<uint4*>(dst)[u] = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-                    } else {
-                        for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u] = __uint_as_float(v[u]);
-                    }
-                } else if (p.c_f32) {
-                    float* dst = static_cast<float*>(p.C) + row * p.ld_c + col;
-                    if (full && p.vec_store) {
-#pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            reinterpret_cast<uint4*>(dst)[u] = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
-                    } else {
-                        for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u] = __uint_as_float(v[u]);
-                    }
-                } else {
-                    __half* dst = static_cast<__half*>(p.C) + row * p.ld_c + col;
-                    uint32_t h[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const __half2 t2 = __floats2half2_rn(__uint_as_float(v[2 * u]), __uint_as_float(v[2 * u + 1]));
-                        h[u] = *reinterpret_cast<const uint32_t*>(&t2);
-                    }
-                    if (full && p.vec_store) {
-                        reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
-                        reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
-                    } else {
-                        for (int u = 0; u < 16 && col + u < p.N; ++u)
-                            dst[u] = __float2half_rn(__uint_as_float(v[u]));
-                    }
-                }
-            };
-            // two TMEM loads in flight per wait
-            constexpr int kEpiStep = BN >= 32 ? 32 : 16;
-#pragma unroll 1
-            for (int c = 0; c < BN; c += kEpiStep) {
-                uint32_t v0[16], v1[16];
-                tmem_ld_32x32b_x16(tmem_acc + buf * BN + lane_addr + c, v0);
-                if (kEpiStep == 32) tmem_ld_32x32b_x16(tmem_acc + buf * BN + lane_addr + c + 16, v1);
-                tmem_wait_ld();
-                store16(v0, c);
-                if (kEpiStep == 32) store16(v1, c + 16);
-            }
+            drain_columns<BN>(p, g, tmem_acc + buf * BN + lane_addr, row, 0, kEpiCols);
             // this warp's lanes of the accumulator are in registers: release it
             tc_fence_before_sync();
             __syncwarp();
