@@ -67,7 +67,8 @@ typedef enum vnm_path {
     VNM_PATH_NONE = 0, /* nothing to compute (an empty product) */
     VNM_PATH_TC = 1,   /* tcgen05 2:4 sparse tensor-core MMA, TMEM accumulators */
     VNM_PATH_SIMT = 2  /* CUDA-core kernels: N <= 8 streams each V-block row with the selected rows of
-                          B staged in shared memory (split K); larger N, one warp per row */
+                          B staged in shared memory (split K over a thread-block cluster, reduced in
+                          distributed shared memory); larger N, one warp per row */
 } vnm_path;
 
 /* A launch plan for vnm_spmm. vnm_spmm_plan_query fills one; a caller may
@@ -78,8 +79,9 @@ typedef struct vnm_spmm_plan {
     int32_t tile_n;    /* TC: columns of C per CTA tile = MMA N (16, 32, 64, 128, 192 or 256) */
     int32_t stages;    /* TC: depth of the shared-memory pipeline (one depth is built per tile;
                           0 in a plan passed to vnm_spmm_with_plan means that depth) */
-    int32_t splits;    /* split-K factor (1 = none): TC over the condensed K, SIMT with N <= 8 over
-                          the blocks of a row; partials go to the workspace */
+    int32_t splits;    /* split-K factor (1 = none): TC over the condensed K (partials go to the
+                          workspace); SIMT with N <= 8 over the blocks of a row, rounded down to 1, 2,
+                          4 or 8 CTAs of one cluster (no workspace) */
     int32_t cluster;   /* TC with B loaded by TMA (M == 4): CTAs per thread-block cluster (0 or 1 =
                           none; 2 or 4 with tile_m 128, tile_n 128, 192 or 256 and a whole number of
                           clusters over the row tiles); the CTAs of a cluster take consecutive
@@ -163,10 +165,10 @@ vnm_status vnm_decompress(vnm_matrix A, void* W_out, int64_t ld_w, vnm_stream_t 
  *   C: R x N, row-major, leading dimension ld_c >= N, of type c_type
  *      (VNM_F16: fp32 accumulation rounded once to fp16, round-to-nearest-
  *      even; VNM_F32: the fp32 accumulator); C is overwritten, never read;
- *   workspace: device scratch for split-K partial sums, at least
- *      vnm_spmm_workspace_size bytes, 256-byte aligned; it may be NULL when
- *      workspace_bytes is 0, and a smaller workspace only lowers the split
- *      factor (the result stays within the same tolerance).
+ *   workspace: device scratch for the tensor-core path's split-K partial
+ *      sums, at least vnm_spmm_workspace_size bytes, 256-byte aligned; it
+ *      may be NULL when workspace_bytes is 0, and a smaller workspace only
+ *      lowers the split factor (the result stays within the same tolerance).
  * The plan comes from vnm_spmm_plan_query. N = 0 or R = 0 is a no-op; K = 0
  * writes zeros.
  * Errors: VNM_ERR_INVALID_ARG (pointers, leading dimensions, c_type),
@@ -186,7 +188,7 @@ vnm_status vnm_spmm_workspace_size(vnm_matrix A, int64_t N, size_t* bytes);
  * is allowed: it needs B 16-byte aligned with ld_b % 8 == 0 and N >= 8, and
  * a block geometry it serves (K/M % 32 == 0, and V % 64 == 0 or M == 4);
  * everything else takes the CUDA-core path (N <= 8: the streaming kernel,
- * which splits K when the workspace allows).
+ * which splits K over a cluster of CTAs without a workspace).
  * Errors: VNM_ERR_INVALID_ARG.
  */
 vnm_status vnm_spmm_plan_query(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, vnm_dtype c_type,

@@ -91,26 +91,27 @@ bool tc_operands_ok(const void* B, int64_t ld_b, int64_t N) {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// The split the streaming kernel will actually use: 1, 2, 4 or 8 (the CTAs
+// of a V-block row form one cluster and reduce in distributed shared
+// memory), at most `requested`, no split empty.
+int effective_stream_splits(const vnm_matrix_s& A, int requested) {
+    const int64_t nblk = A.K / A.M;
+    int s = 1;
+    while (s * 2 <= std::min(requested, 8)) s *= 2;
+    while (s > 1 && (s - 1) * ceil_div(nblk, s) >= nblk) s /= 2;
+    return s;
+}
+
 // K splits of the streaming CUDA-core path (N <= 8): about two CTAs per SM,
-// every split at least one staged chunk of blocks, partials within the
-// workspace.
-int64_t stream_splits(const vnm_matrix_s& A, int64_t N, size_t workspace_bytes) {
+// every split at least one staged chunk of blocks. No workspace: the splits
+// of a V-block row reduce within their cluster.
+int64_t stream_splits(const vnm_matrix_s& A, int64_t N) {
     if (N > 8 || N < 1) return 1;
     const int64_t nblk = A.K / A.M;
     const int64_t rows_blocks = std::max<int64_t>(1, A.R / A.V);
     int64_t s = ceil_div(2 * static_cast<int64_t>(A.sm_count), rows_blocks);
     s = std::min<int64_t>(s, std::max<int64_t>(1, nblk / vnm::stream_chunk_blocks(A.V)));
-    const int64_t per_split = A.R * N * static_cast<int64_t>(sizeof(float));
-    if (s > 1) s = std::min<int64_t>(s, static_cast<int64_t>(workspace_bytes) / per_split);
-    return std::max<int64_t>(1, s);
-}
-
-// The split the streaming kernel will actually use (no empty split).
-int effective_stream_splits(const vnm_matrix_s& A, int requested) {
-    const int64_t nblk = A.K / A.M;
-    const int64_t req = std::max<int64_t>(1, std::min<int64_t>(requested, nblk));
-    const int64_t per = ceil_div(nblk, req);
-    return static_cast<int>(ceil_div(nblk, per));
+    return effective_stream_splits(A, static_cast<int>(std::min<int64_t>(s, 8)));
 }
 
 vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, size_t workspace_bytes) {
@@ -123,7 +124,7 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     }
     if (!(tc_geometry_ok(A) && tc_operands_ok(B, ld_b, N))) {
         pl.path = VNM_PATH_SIMT;
-        pl.splits = static_cast<int32_t>(stream_splits(A, N, workspace_bytes));
+        pl.splits = static_cast<int32_t>(stream_splits(A, N));
         return pl;
     }
     pl.path = VNM_PATH_TC;
@@ -166,14 +167,7 @@ int effective_splits(const vnm_matrix_s& A, int requested) {
 
 vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void* B, int64_t ld_b, int64_t N,
                       size_t workspace_bytes, const void* workspace) {
-    if (pl.path == VNM_PATH_SIMT) {
-        if (N > 8 || pl.splits <= 1) return VNM_OK;  // N > 8: one pass, no split
-        const int s = effective_stream_splits(A, pl.splits);
-        const size_t need = static_cast<size_t>(s) * A.R * N * sizeof(float);
-        if (s > 1 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)))
-            return VNM_ERR_INVALID_ARG;
-        return VNM_OK;
-    }
+    if (pl.path == VNM_PATH_SIMT) return pl.splits < 1 ? VNM_ERR_INVALID_ARG : VNM_OK;  // no workspace
     if (pl.path != VNM_PATH_TC) return VNM_ERR_UNSUPPORTED;
     if (!tc_geometry_ok(A) || !tc_operands_ok(B, ld_b, N)) return VNM_ERR_UNSUPPORTED;
     if (!tc_tile_m_ok(A, pl.tile_m)) return VNM_ERR_UNSUPPORTED;
@@ -203,7 +197,7 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
     if (pl.path == VNM_PATH_SIMT) {
         if (N <= 8)
             e = vnm::launch_spmm_stream(*A, B, ld_b, N, C, ld_c, c_f32, effective_stream_splits(*A, pl.splits),
-                                        static_cast<float*>(workspace), stream);
+                                        stream);
         else
             e = vnm::launch_spmm_simt(*A, B, ld_b, N, C, ld_c, c_f32, stream);
     } else if (pl.path == VNM_PATH_TC) {
@@ -366,7 +360,6 @@ vnm_status vnm_spmm_workspace_size(vnm_matrix A, int64_t N, size_t* bytes) {
     *bytes = 0;
     int s = 1;
     if (pl.path == VNM_PATH_TC) s = effective_splits(*A, pl.splits);
-    if (pl.path == VNM_PATH_SIMT && N <= 8) s = effective_stream_splits(*A, pl.splits);
     if (s > 1) *bytes = static_cast<size_t>(s) * A->R * N * sizeof(float);
     return VNM_OK;
 }

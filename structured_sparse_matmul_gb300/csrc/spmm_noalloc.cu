@@ -91,7 +91,7 @@ extern "C" vnm_status vnm_spmm_noalloc(int64_t R, int64_t K, int32_t V, int32_t 
     vnm_status st = vnm_spmm_plan_query(&A, B, ld_b, N, c_type, SIZE_MAX / 2, &plan);
     if (st != VNM_OK) return st;
     size_t need = 0;
-    if ((plan.path == VNM_PATH_TC || (plan.path == VNM_PATH_SIMT && N <= 8)) && plan.splits > 1)
+    if (plan.path == VNM_PATH_TC && plan.splits > 1)
         need = static_cast<size_t>(plan.splits) * static_cast<size_t>(R) * static_cast<size_t>(N) * sizeof(float);
     if (need > kScratchBytes) return VNM_ERR_INVALID_ARG;  // partials would exceed the 8 MiB static scratch
 

@@ -13,6 +13,7 @@
 #include <algorithm>
 
 #include "vnm_internal.h"
+#include "vnm_ptx.cuh"
 
 namespace vnm {
 namespace {
@@ -126,8 +127,11 @@ __global__ void splitk_reduce_kernel(const float* __restrict__ partial, int spli
 // values each) in shared memory; each of the 16 warps owns RW rows and
 // issues all its loads of the chunk at once (lane = block, RW*U = 16 loads
 // per lane), so a chunk costs one round trip to memory; the multiply-adds
-// then read B from shared memory. Splits write fp32 partials that the
-// split-K reduction sums in order.
+// then read B from shared memory. With K split over s CTAs (s = 2, 4 or 8),
+// the s CTAs of a V-block row form a thread-block cluster: each leaves its
+// fp32 partial sums in its shared memory, and after a cluster barrier CTA q
+// sums rows q, q + s, ... over the cluster in split order (distributed
+// shared memory), so C is written once by one kernel, deterministically.
 constexpr int kStreamWarps = 16;
 
 struct StreamArgs {
@@ -138,7 +142,6 @@ struct StreamArgs {
     int64_t ld_b;
     void* C;
     int64_t ld_c;
-    float* partial;          // [splits][R][N] fp32 when splits > 1
     int64_t R, N;
     int V, M;
     int64_t nblk, mpitch;
@@ -162,6 +165,7 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
     // bytes), padded for NB >= 4 to spread the banks
     constexpr int kStride = 4 * NB + (NB >= 4 ? 4 : 0);
     __shared__ __align__(16) __half Bc[kChunk * kStride];
+    __shared__ float red[kStreamWarps * RW][NB];  // this CTA's sums of the pass's rows (split K)
     const int64_t i = blockIdx.x / p.splits;
     const int s = static_cast<int>(blockIdx.x % p.splits);
     const int64_t jb = s * p.bps;
@@ -231,6 +235,13 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
                 }
             }
         }
+        auto store = [&](int r, int n, float v) {
+            const int64_t row = i * p.V + r;
+            if (p.c_f32)
+                static_cast<float*>(p.C)[row * p.ld_c + n] = v;
+            else
+                static_cast<__half*>(p.C)[row * p.ld_c + n] = __float2half_rn(v);
+        };
 #pragma unroll
         for (int t = 0; t < RW; ++t) {
             const int r = r0 + kStreamWarps * t;
@@ -242,15 +253,27 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
                 for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
                 if (lane == n) out = v;
             }
-            if (r < p.V && lane < p.N && lane < NB) {
-                const int64_t row = i * p.V + r;
-                if (p.partial != nullptr)
-                    p.partial[(static_cast<int64_t>(s) * p.R + row) * p.N + lane] = out;
-                else if (p.c_f32)
-                    static_cast<float*>(p.C)[row * p.ld_c + lane] = out;
-                else
-                    static_cast<__half*>(p.C)[row * p.ld_c + lane] = __float2half_rn(out);
+            if (p.splits > 1) {
+                if (lane < NB) red[warp + kStreamWarps * t][lane] = out;
+            } else if (r < p.V && lane < p.N && lane < NB) {
+                store(r, lane, out);
             }
+        }
+        if (p.splits > 1) {
+            // every CTA of the cluster holds its partial sums of the pass's rows
+            cluster_sync_all();
+            const uint32_t red0 = smem_u32(&red[0][0]);
+            for (int e = threadIdx.x; e < kStreamWarps * RW * NB; e += blockDim.x) {
+                const int l = e / NB, n = e % NB;  // row of the pass (warp + 16 t), column
+                const int r = rbase + l;
+                if (l % p.splits != s || r >= p.V || n >= p.N) continue;
+                float v = 0.f;
+                for (int q = 0; q < p.splits; ++q)
+                    v += dsmem_ld_f32(dsmem_map(red0 + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)));
+                store(r, n, v);
+            }
+            // no CTA reuses or leaves its partial sums while another may still read them
+            cluster_sync_all();
         }
     }
 }
@@ -258,8 +281,24 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
 template <int NB, int RW, int U>
 cudaError_t launch_stream3(const StreamArgs& p, cudaStream_t stream) {
     const int64_t ctas = (p.R / p.V) * p.splits;
-    spmm_stream_kernel<NB, RW, U><<<static_cast<unsigned>(ctas), 32 * kStreamWarps, 0, stream>>>(p);
-    return cudaGetLastError();
+    if (p.splits == 1) {
+        spmm_stream_kernel<NB, RW, U><<<static_cast<unsigned>(ctas), 32 * kStreamWarps, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+    // the splits of a V-block row are consecutive CTAs: one cluster
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(32 * kStreamWarps);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, spmm_stream_kernel<NB, RW, U>, p);
 }
 
 template <int NB>
@@ -308,7 +347,7 @@ cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b,
 int stream_chunk_blocks(int V) { return V <= 32 ? 256 : V <= 64 ? 128 : 64; }
 
 cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
-                               int64_t ld_c, bool c_f32, int splits, float* partial, cudaStream_t stream) {
+                               int64_t ld_c, bool c_f32, int splits, cudaStream_t stream) {
     StreamArgs p;
     p.values = static_cast<const uint32_t*>(A.values);
     p.meta = static_cast<const uint8_t*>(A.meta);
@@ -326,18 +365,16 @@ cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t ld_
     p.c_f32 = c_f32;
     if (A.R == 0 || N == 0) return cudaSuccess;
     if (N > 8) return cudaErrorInvalidValue;
-    const int64_t req = std::max<int64_t>(1, std::min<int64_t>(splits, p.nblk));
-    p.bps = (p.nblk + req - 1) / req;
-    p.splits = static_cast<int>((p.nblk + p.bps - 1) / p.bps);  // no empty split
-    if (p.splits > 1 && partial == nullptr) return cudaErrorInvalidValue;
-    p.partial = p.splits > 1 ? partial : nullptr;
-    cudaError_t e;
-    if (N <= 1) e = launch_stream_nb<1>(p, stream);
-    else if (N <= 2) e = launch_stream_nb<2>(p, stream);
-    else if (N <= 4) e = launch_stream_nb<4>(p, stream);
-    else e = launch_stream_nb<8>(p, stream);
-    if (e != cudaSuccess || p.splits == 1) return e;
-    return launch_splitk_reduce(partial, p.splits, A.R, N, C, ld_c, c_f32, stream);
+    // splits: 1, 2, 4 or 8 (a cluster), none of them empty
+    if (splits != 1 && splits != 2 && splits != 4 && splits != 8) return cudaErrorInvalidValue;
+    if (splits > p.nblk) return cudaErrorInvalidValue;
+    p.splits = splits;
+    p.bps = (p.nblk + splits - 1) / splits;
+    if ((splits - 1) * p.bps >= p.nblk) return cudaErrorInvalidValue;
+    if (N <= 1) return launch_stream_nb<1>(p, stream);
+    if (N <= 2) return launch_stream_nb<2>(p, stream);
+    if (N <= 4) return launch_stream_nb<4>(p, stream);
+    return launch_stream_nb<8>(p, stream);
 }
 
 cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, void* C, int64_t ld_c,

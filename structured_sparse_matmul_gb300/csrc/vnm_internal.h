@@ -47,10 +47,11 @@ cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, 
 cudaError_t launch_decompress(const vnm_matrix_s& A, void* W, int64_t ld_w, cudaStream_t stream);
 
 // Streaming CUDA-core SpMM for N <= 8: one CTA per (V-block row, K split);
-// with splits > 1 it writes fp32 partials to `partial` ([splits][R][N]) and
-// reduces them into C. `stream_chunk_blocks(V)` blocks are staged per pass.
+// splits (1, 2, 4 or 8, none empty) form a thread-block cluster and reduce
+// in distributed shared memory: no workspace. `stream_chunk_blocks(V)`
+// blocks are staged per pass.
 cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
-                               int64_t ld_c, bool c_f32, int splits, float* partial, cudaStream_t stream);
+                               int64_t ld_c, bool c_f32, int splits, cudaStream_t stream);
 int stream_chunk_blocks(int V);
 
 // CUDA-core SpMM; writes C directly (fp16 or fp32).

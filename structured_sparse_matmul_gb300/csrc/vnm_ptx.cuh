@@ -146,6 +146,20 @@ __device__ __forceinline__ uint32_t cluster_count_x() {
     return r;
 }
 
+// Address in the shared memory of cluster CTA `rank` of the variable at
+// shared-memory address `local` in this CTA (distributed shared memory).
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Every thread of every CTA of the cluster (all threads call it, converged).
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
