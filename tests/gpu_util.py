@@ -64,7 +64,7 @@ def run_spmm(A, B: np.ndarray, c_dtype=torch.float16, plan=None, ld_b=None, ld_c
         vnm.vnm_spmm(A, Bd, C, workspace=ws)
     else:
         s = max(1, plan.splits)
-        ws = torch.empty(s * A.R * N + 64, dtype=torch.float32, device=device()) if s > 1 else None
+        ws = torch.empty(s * A.R * N + 64, dtype=torch.float32, device=device()) if s > 1 and workspace else None
         vnm.vnm_spmm_with_plan(A, plan, Bd, C, workspace=ws)
     st = vnm.vnm_get_status(A)
     assert st == vnm.VNM_OK, vnm.status_string(st)

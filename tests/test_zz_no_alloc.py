@@ -48,7 +48,8 @@ def _noalloc_call(A, B, C, status=None):
     return rc
 
 
-@pytest.mark.parametrize("R,K,N,V,M", [(4096, 4096, 32, 64, 4), (4096, 4096, 16, 64, 8), (1024, 2048, 40, 128, 16)])
+@pytest.mark.parametrize("R,K,N,V,M", [(4096, 4096, 32, 64, 4), (4096, 4096, 16, 64, 8), (1024, 2048, 40, 128, 16),
+                                       (128, 4096, 256, 128, 4)])
 def test_matches_vnm_spmm_on_two_calls(R, K, N, V, M):
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
@@ -88,7 +89,7 @@ def test_without_status_pointer_and_fp32_output():
 def test_rejects_scratch_beyond_the_static_maximum():
     torch.cuda.set_device(0)
     dev = torch.device("cuda", 0)
-    # 9 x 8 tiles of 128 x 128 split K in two: 2 x 1152 x 1024 fp32 partials > 8 MiB
+    # 9 x 6 tiles of 128 x 192 split K in two: 2 x 1152 x 1024 fp32 partials > 8 MiB
     R, K, N, V, M = 1152, 4096, 1024, 128, 4
     A = _compressed(R, K, V, M, seed=71)
     B = torch.zeros((K, N), dtype=torch.float16, device=dev)
