@@ -102,16 +102,17 @@ int effective_stream_splits(const vnm_matrix_s& A, int requested) {
     return s;
 }
 
-// K splits of the streaming CUDA-core path (N <= 8): about two CTAs per SM,
-// every split at least one staged chunk of blocks. No workspace: the splits
-// of a V-block row reduce within their cluster.
+// K splits of the streaming CUDA-core path (N <= 8): up to four CTAs per SM,
+// at most 4 splits (8 measured slower on every decode shape), every split at
+// least one staged chunk of blocks. No workspace: the splits of a V-block
+// row reduce within their cluster.
 int64_t stream_splits(const vnm_matrix_s& A, int64_t N) {
     if (N > 8 || N < 1) return 1;
     const int64_t nblk = A.K / A.M;
     const int64_t rows_blocks = std::max<int64_t>(1, A.R / A.V);
-    int64_t s = ceil_div(2 * static_cast<int64_t>(A.sm_count), rows_blocks);
+    int64_t s = ceil_div(4 * static_cast<int64_t>(A.sm_count), rows_blocks);
     s = std::min<int64_t>(s, std::max<int64_t>(1, nblk / vnm::stream_chunk_blocks(A.V)));
-    return effective_stream_splits(A, static_cast<int>(std::min<int64_t>(s, 8)));
+    return effective_stream_splits(A, static_cast<int>(std::min<int64_t>(s, 4)));
 }
 
 vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, size_t workspace_bytes) {
