@@ -403,11 +403,12 @@ def main():
         if st != vnm.VNM_OK:
             raise RuntimeError(f"kernel status {vnm.status_string(st)} during warm-up")
 
-    # Three CUDA graphs over the same rotating sets, each captured once:
-    # K whole steps (the timed region: no event nodes inside, which would
-    # add microseconds per kernel), K SpMM launches and K compress launches
-    # (each kernel's average launch duration, for the breakdown and the
-    # roofline).
+    # CUDA graphs over the same rotating sets, each captured once: K whole
+    # steps on one stream (reported as the serial step), K SpMM launches and
+    # K compress launches (each kernel's average launch duration, for the
+    # breakdown and the roofline), and below the timed graph of K pipelined
+    # steps. No timing event sits inside a graph (an event node adds
+    # microseconds per kernel); cross-stream dependencies are graph edges.
     steps = args.steps
 
     def capture(**kw):
@@ -427,9 +428,43 @@ def main():
         torch.cuda.synchronize(dev)
         return g
 
-    graph = capture()
+    graph_serial = capture()
     graph_spmm = capture(comp=False)
     graph_comp = capture(spmm=False)
+
+    # The timed graph: the same K steps with the compressions on one stream
+    # and the products on another. Step i's SpMM waits for step i's compress;
+    # step i's compress waits for the last SpMM that read its set. So step
+    # i+1's compress runs while step i's SpMM finishes (on the SMs its last
+    # wave of tiles leaves idle); every step still compresses its W and
+    # multiplies its B.
+    def capture_pipelined():
+        g = torch.cuda.CUDAGraph()
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(torch.cuda.current_stream(dev))
+        s_c, s_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        with torch.cuda.stream(cap), torch.cuda.graph(g, stream=cap):
+            s_c.wait_stream(cap)
+            s_s.wait_stream(cap)
+            ev_c = [torch.cuda.Event() for _ in range(steps)]
+            ev_s = [torch.cuda.Event() for _ in range(steps)]
+            for i in range(steps):
+                st = sets[i % n_sets]
+                if i >= n_sets:
+                    s_c.wait_event(ev_s[i - n_sets])
+                vnm.vnm_compress(st["A"], st["W"], stream=s_c)
+                ev_c[i].record(s_c)
+                s_s.wait_event(ev_c[i])
+                vnm.vnm_spmm(st["A"], st["B"], st["C"], workspace=st["ws"], stream=s_s)
+                ev_s[i].record(s_s)
+            cap.wait_stream(s_c)
+            cap.wait_stream(s_s)
+        torch.cuda.synchronize(dev)
+        g.replay()  # warm replay
+        torch.cuda.synchronize(dev)
+        return g
+
+    graph = capture_pipelined()
 
     def timed(g):
         e0 = torch.cuda.Event(enable_timing=True)
@@ -451,6 +486,7 @@ def main():
     torch.cuda.synchronize(dev)
     elapsed_ms = timed(graph)
     dist_barrier(world, dev)
+    serial_ms = timed(graph_serial) / steps
     spmm_ms = timed(graph_spmm) / steps
     comp_ms = timed(graph_comp) / steps
     # launch floor: K empty kernels (a sleep of zero cycles), captured and
@@ -626,6 +662,9 @@ def main():
             "config": config_of(case, f"{n_sets} rotating input/output sets of {set_bytes / 2**20:.1f} MiB "
                                       f"(> 2x the {l2 / 2**20:.0f} MiB L2)"),
             "effective_tflops": eff_flops * steps * world / (max_ms * 1e-3) / 1e12,
+            "step_schedule": {"ms_per_step": max_ms / steps, "serial_ms_per_step": serial_ms,
+                              "pipelined": "compress on one stream, SpMM on another: step i+1's compress overlaps "
+                                           "step i's SpMM; serial_ms_per_step = the same steps on one stream"},
             "kernels": {"vnm_compress_ms": comp_ms, "vnm_spmm_ms": spmm_ms,
                         "spmm_dense_equiv_tflops": dense_flops / (spmm_ms * 1e-3) / 1e12,
                         "spmm_effective_tflops": eff_flops / (spmm_ms * 1e-3) / 1e12,
