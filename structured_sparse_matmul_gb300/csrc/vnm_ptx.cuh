@@ -1,6 +1,7 @@
 // Inline-PTX helpers for sm_103a: mbarriers with bounded waits, TMA tensor
-// loads (tiled and 4-row gather), and the tcgen05 tensor-core instructions
-// (TMEM allocation, sparse MMA, shared->TMEM copy, TMEM loads and stores).
+// loads (tiled, and multicast within a cluster), cluster and distributed
+// shared memory access, and the tcgen05 tensor-core instructions (TMEM
+// allocation, sparse MMA, TMEM loads and stores).
 // Every wait here gives up after a time limit and raises a CTA-wide abort
 // flag instead of spinning forever.
 #pragma once
@@ -165,18 +166,6 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// 2-D gather of four rows y0..y3 (any order, any rows), each the box width
-// starting at column x, into four consecutive box rows of shared memory.
-// The tensor map's box must be one row high.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y0,
-                                            int32_t y1, int32_t y2, int32_t y3, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
-        : "memory");
-}
-
 // 16-byte asynchronous copy global -> shared (L2 only); copies src_bytes
 // (0..16) and zero-fills the rest of the 16 bytes.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
@@ -204,11 +193,6 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 // later accesses through the async proxy (TMA, tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Barrier among `nthreads` threads (a multiple of 32) on hardware barrier `id`.
-__device__ __forceinline__ void named_barrier(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 // ----------------------------------------------------------------- tcgen05
@@ -265,23 +249,6 @@ __device__ __forceinline__ void tc_mma_sp_f16(uint32_t d_tmem, uint64_t adesc, u
         : "memory");
 }
 
-// Dense variant (same operand conventions, no metadata).
-__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Copy 128 rows x 128 bits from shared memory (matrix descriptor sdesc) to
-// TMEM lanes 0..127, 4 consecutive 32-bit columns from taddr.
-__device__ __forceinline__ void tc_cp_128x128b(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
-}
-
 // Each thread of the warp reads 16 consecutive 32-bit columns of its lane.
 __device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
@@ -299,26 +266,6 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 // Each thread of the warp writes 4 consecutive 32-bit columns of its lane.
 __device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t a) {
     asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(a) : "memory");
-}
-
-__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, uint32_t a, uint32_t b, uint32_t c,
-                                                  uint32_t d) {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(a),
-                 "r"(b), "r"(c), "r"(d)
-                 : "memory");
-}
-
-// Each thread of the warp writes 32 consecutive 32-bit columns of its lane.
-__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
-        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
-        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
-        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
-        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
-        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-        : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
