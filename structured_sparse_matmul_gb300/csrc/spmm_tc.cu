@@ -23,7 +23,7 @@
 //             selected B rows (4 per block, tile_n columns each) with 16-byte
 //             cp.async, coalesced along each row, straight into the
 //             128B-swizzled operand layout (zero-filled past N); the
-//             column-loc words that select the rows are loaded one stage
+//             column-loc words that select the rows are loaded four stages
 //             ahead; each thread's copies arrive on the stage's barrier by
 //             themselves when they land (cp.async.mbarrier.arrive), so every
 //             pipeline stage can be in flight; the MMA thread fences the
@@ -39,14 +39,17 @@
 //             M=tile_m, N=tile_n, K=32 per stage into an fp32 accumulator in
 //             TMEM; tcgen05.commit releases the stage, and the tile's
 //             accumulator to the epilogue. Two accumulators alternate between
-//             tiles when TMEM holds them (tile_n <= 128).
+//             tiles when TMEM holds them (tile_n <= 192).
 //   warps 6-9 epilogue: TMEM -> registers (tcgen05.ld) -> fp16 (RNE) or
 //             fp32 -> global, each thread writing whole 32-byte sectors of
 //             its row (fp32 partials to the workspace under split-K), while
 //             the other warps already run the next tile; then they release
-//             the accumulator. With M=128 row r of the tile lives in TMEM
-//             lane r; with M=64 in lane 32*(r/16) + r%16 (lanes 16..31 of
-//             each quarter stay unused).
+//             the accumulator (with a single accumulator and 64-row tiles
+//             the m-index warps drain half of its columns). With M=128 row r
+//             of the tile lives in TMEM lane r; with M=64 in lane
+//             32*(r/16) + r%16 (lanes 16..31 of each quarter stay unused).
+// Clusters (CS = 2 or 4, B by TMA): the CTAs of a cluster take consecutive
+// row tiles of one column tile and share each B tile by multicast.
 // Every mbarrier wait is bounded: on time-out the CTA records
 // VNM_ERR_TIMEOUT, drains what it already issued, frees TMEM and returns.
 #include <cuda_fp16.h>
