@@ -309,6 +309,24 @@ def test_streaming_small_n(R, K, V, M, N, c_dtype):
         check_close(got if rows is None else got[rows], ref, f"stream {R}x{K}x{N} {V}:2:{M} ws={ws}")
 
 
+@pytest.mark.parametrize("splits", [1, 2, 4, 8])
+def test_streaming_split_clusters(splits):
+    """The streaming kernel's K splits (1, 2, 4 or 8 CTAs of a V-block row in
+    one cluster, reduced in split order through distributed shared memory),
+    ragged N, both C types; the same C bit for bit on a second run."""
+    R, K, N, V, M = 192, 4096, 5, 64, 8
+    A, B, comp = _setup(R, K, N, V, M, seed=36)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    assert plan.path == vnm.VNM_PATH_SIMT, plan.as_dict()
+    plan.splits = splits
+    ref = _ref(comp, R, K, V, M, B)
+    for c_dtype in (torch.float16, torch.float32):
+        got, _ = run_spmm(A, B, c_dtype, plan=plan, workspace=False)
+        check_close(got, ref, f"stream splits {splits}")
+        again, _ = run_spmm(A, B, c_dtype, plan=plan, workspace=False)
+        assert np.array_equal(got, again)
+
+
 def test_streaming_at_n8_by_plan():
     """N = 8 runs on the tensor cores by default; a plan may ask for the
     streaming path instead, with a chosen split."""
