@@ -172,6 +172,25 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- CPU oracle
 
+def host_cpu() -> str:
+    """The host CPU's model, as the kernel reports it (Arm: implementer and part)."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    if "CPU part" in fields:
+        return f"{platform.machine()} implementer {fields.get('CPU implementer', '?')} part {fields['CPU part']}"
+    return platform.processor() or platform.machine()
+
+
 def time_oracle(case, seconds: float):
     """Time the CPU oracle (compress + fp32-accumulate SpMM, as it stands) on
     the first S V-block rows of the workload, S chosen for ~``seconds``."""
@@ -277,7 +296,8 @@ def run_reference(args, case):
         "steps": steps, "warmup": args.warmup, "ms_per_step": total / steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": config_of(case, None),
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": desc,
+                         "host_cpu": host_cpu(), "host_threads": os.cpu_count()},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -653,6 +673,8 @@ def main():
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         c = time_oracle(case, args.cpu_seconds)
         cpu = {k: c[k] for k in ("value", "unit", "cores", "kind", "sample", "row_parallel")}
+        cpu["host_cpu"] = host_cpu()
+        cpu["host_threads"] = os.cpu_count()
 
     if rank == 0:
         line = {
