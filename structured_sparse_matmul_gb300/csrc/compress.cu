@@ -15,6 +15,8 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 
 #include "vnm_internal.h"
 #include "vnm_ptx.cuh"
@@ -1022,12 +1024,14 @@ cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, 
     if (A.R == 0 || A.K == 0) return cudaSuccess;
     if (A.M == 4 && A.K % 16 == 0 && reinterpret_cast<uintptr_t>(W) % 16 == 0 && ld_w % 8 == 0) {
         // one full wave of resident CTAs, each striding over the chunks
-        static int per_sm = 0;
+        static std::atomic<int> per_sm_cache{0};  // resident CTAs per SM, once per process
+        int per_sm = per_sm_cache.load(std::memory_order_relaxed);
         if (per_sm == 0) {
             int occ = 0;
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, compress_m4_kernel, kM4Threads, 0) != cudaSuccess)
                 occ = 4;
             per_sm = std::max(1, occ);
+            per_sm_cache.store(per_sm, std::memory_order_relaxed);
         }
         const int64_t chunks = A.R * (A.K / 16);
         const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((chunks + kM4Threads - 1) / kM4Threads,
@@ -1070,7 +1074,11 @@ cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, 
         p.vec_load = (reinterpret_cast<uintptr_t>(W) % 16 == 0) && (ld_w % 8 == 0) && (p.tk % 8 == 0);
         const size_t smem = tile_bytes_aligned(A.V, p.tk) + sizeof(uint64_t) * p.tk +
                             sizeof(uint32_t) * (p.tk / A.M);
-        static size_t configured = 0;  // largest dynamic shared memory size set so far
+        // largest dynamic shared memory sizes set so far (one lock for check and set,
+        // so that concurrent calls never lower a size another call relies on)
+        static std::mutex smem_mutex;
+        static size_t configured = 0;
+        std::lock_guard<std::mutex> smem_lock(smem_mutex);
         if (smem > 48 * 1024 && smem > configured) {
             cudaError_t e = cudaFuncSetAttribute(compress_tiled_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  static_cast<int>(smem));

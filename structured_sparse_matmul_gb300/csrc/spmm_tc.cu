@@ -55,6 +55,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 
 #include "vnm_internal.h"
@@ -678,7 +679,8 @@ cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stre
         cfg.numAttrs = 1;
     }
     // co-resident CTAs (clusters), once per process (the attribute is per function)
-    static int64_t resident = 0;
+    static std::atomic<int64_t> resident_cache{0};
+    int64_t resident = resident_cache.load(std::memory_order_relaxed);
     if (resident == 0) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
         if (e != cudaSuccess) return e;
@@ -696,6 +698,7 @@ cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stre
             if (clusters < 1) return cudaErrorInvalidConfiguration;
             resident = std::min<int64_t>(resident / CS, clusters);  // in clusters
         }
+        resident_cache.store(resident, std::memory_order_relaxed);
     }
     // p.total_tiles counts tile groups of CS m-tiles
     const int64_t units = std::min<int64_t>(p.total_tiles, resident);
