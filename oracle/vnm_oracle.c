@@ -19,11 +19,12 @@
  * j*M .. j*M+M-1.
  *
  * Readings where the papers leave a step open:
- *  - "the four most significant columns" of a block: the 4 columns with the
+ *  - the 4 columns a block keeps (VENOM names them the most significant,
+ *    without a measure): the 4 columns with the
  *    largest L1 norm over the block's V rows, computed exactly (the sum is
  *    formed in double: every |fp16| is a multiple of 2^-24 below 2^16, so
  *    for V <= 4096 every partial sum is exact and the order is irrelevant);
- *  - "the two most meaningful weights" of a row of 4: the 2 largest |w|;
+ *  - the 2 weights a row keeps of its 4: the 2 largest |w|;
  *  - ties go to the lower index at both levels;
  *  - column-loc entries of a block are stored ascending; the two kept values
  *    of a row are stored in ascending slot order (as in Figure 3 and in the
