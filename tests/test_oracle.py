@@ -61,7 +61,7 @@ def check_worked_example(L):
 
 
 def check_worked_local_index(L):
-    """"slot 1 of the second group is column 4 + 1 = 5" (decompress position)."""
+    """Indices are local to their group: slot 1 of group 1 decompresses to column 5."""
     fx = read_fixture(os.path.join(GOLDEN, "worked_2x8.txt"))
     W = np.array([_floats(fx["dense_row0"]), _floats(fx["dense_row1"])], dtype=np.float16)
     values, meta, colidx = oracle.compress(W, 1, 4, L)
@@ -117,7 +117,7 @@ def check_storage_arithmetic(L):
     nv, nm, nc = oracle.sizes(R, K, V, M, L)
     assert nv == len(f3["m_indices"].split()) == R * K // M * 2
     assert nc == len(f3["column_loc"].split()) == R // V * K // M * 4
-    # "For V = 128, the overhead is ~13.28%": (2-bit m-index per value + an
+    # VENOM section 3: about 13.28 % overhead at V = 128 (2-bit m-index per value + an
     # 8-bit column-loc entry per 4 columns every V rows) over 16-bit values
     nv, nm, nc = oracle.sizes(1024, 4096, 128, 8, L)
     overhead = (nm * 8 + nc * 8) / (nv * 16)
