@@ -34,9 +34,15 @@
  *   - errors found by a kernel (non-finite weights, a bounded wait that ran
  *     out) are written to the matrix's device status word and returned by
  *     the next vnm_get_status;
- *   - the library keeps no global state and allocates device memory only in
- *     vnm_matrix_create (a 256-byte status block); one matrix handle may be
- *     used by one host thread at a time.
+ *   - device memory is allocated only by vnm_matrix_create (a 256-byte
+ *     status block); one matrix handle may be used by one host thread at a
+ *     time. The library's global state is limited to: per-process caches
+ *     filled on first use (the driver's tensor-map encoder and context
+ *     queries; per kernel instance and device, the shared-memory attribute
+ *     and the co-resident CTA count), all guarded for concurrent callers; and
+ *     the static 8 MiB (+ 256-byte) device array of vnm_spmm_noalloc, held by
+ *     every GPU that loads the library, with its address resolved once per
+ *     CUDA context.
  */
 #ifndef VNM_H
 #define VNM_H
@@ -82,12 +88,8 @@ typedef struct vnm_spmm_plan {
     int32_t splits;    /* split-K factor (1 = none): TC over the condensed K (partials go to the
                           workspace); SIMT with N <= 8 over the blocks of a row, rounded down to 1, 2,
                           4 or 8 CTAs of one cluster (no workspace) */
-    int32_t cluster;   /* TC with B loaded by TMA (M == 4): CTAs per thread-block cluster (0 or 1 =
-                          none; 2 or 4 with tile_m 128, tile_n 128, 192 or 256 and a whole number of
-                          clusters over the row tiles); the CTAs of a cluster take consecutive
-                          row tiles of one column tile and each loads 1/cluster of every B tile,
-                          multicast to all of them */
-    int32_t reserved[2];
+    int32_t reserved[3]; /* must be 0 (vnm_spmm_with_plan rejects anything else with
+                            VNM_ERR_INVALID_ARG) */
 } vnm_spmm_plan;
 
 /* Opaque handle of one compressed matrix. It records R, K, V, M and the
@@ -220,12 +222,16 @@ vnm_status vnm_spmm_with_plan(vnm_matrix A, const vnm_spmm_plan* plan, const voi
  *   B, ld_b, N, C, ld_c, c_type: as in vnm_spmm;
  *   status: optional device pointer to 3 int32 words (first error code,
  *     detail, error count) that the caller zeroed; kernel-detected errors are
- *     recorded there. NULL records them in the static status region instead,
- *     which each call clears first and the caller cannot read.
- * The first call on a device resolves the static array's address on that
- * device (cudaGetSymbolAddress); make that first call before any stream
- * capture. Every call shares the array: calls that overlap on the GPU (for
- * example on two streams) race on it; stream-ordered calls do not.
+ *     recorded there, and C is then undefined. NULL records them in the
+ *     static status region instead, which each call clears first and the
+ *     caller cannot read: such a call still returns VNM_OK, so a caller that
+ *     must know that C is valid passes a status pointer.
+ * The first call in a CUDA context (the device's primary context, or one
+ * the caller made current) resolves the static array's address in that
+ * context (cudaGetSymbolAddress) and caches it under the context's unique
+ * id; make that first call before any stream capture. Every call shares the
+ * array: calls that overlap on the GPU (for example on two streams) race on
+ * it; stream-ordered calls do not.
  * Errors: VNM_ERR_INVALID_ARG (shapes, pointers, leading dimensions, or
  * split-K partials larger than the 8 MiB scratch), VNM_ERR_CUDA.
  */

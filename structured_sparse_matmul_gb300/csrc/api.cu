@@ -150,11 +150,6 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     if (splits > 1) splits = std::min<int64_t>(splits, static_cast<int64_t>(workspace_bytes) / per_split);
     splits = std::max<int64_t>(1, splits);
     pl.splits = static_cast<int32_t>(std::max<int64_t>(1, splits));
-    // B by TMA over whole waves of tiles: pairs of CTAs on consecutive row
-    // tiles share each B tile (multicast), halving its L2 reads
-    pl.cluster = 1;
-    if (A.M == 4 && pl.tile_m == 128 && pl.tile_n >= 128 && pl.splits == 1 && ceil_div(A.R, 128) % 2 == 0)
-        pl.cluster = 2;
     return pl;
 }
 
@@ -168,6 +163,8 @@ int effective_splits(const vnm_matrix_s& A, int requested) {
 
 vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void* B, int64_t ld_b, int64_t N,
                       size_t workspace_bytes, const void* workspace) {
+    for (int32_t r : pl.reserved)
+        if (r != 0) return VNM_ERR_INVALID_ARG;
     if (pl.path == VNM_PATH_SIMT) return pl.splits < 1 ? VNM_ERR_INVALID_ARG : VNM_OK;  // no workspace
     if (pl.path != VNM_PATH_TC) return VNM_ERR_UNSUPPORTED;
     if (!tc_geometry_ok(A) || !tc_operands_ok(B, ld_b, N)) return VNM_ERR_UNSUPPORTED;
@@ -175,14 +172,6 @@ vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void
     const int depth = vnm::tc_default_stages(pl.tile_m, pl.tile_n, A.M > 4);
     if (depth == 0 || (pl.stages != 0 && pl.stages != depth)) return VNM_ERR_UNSUPPORTED;
     if (pl.splits < 1) return VNM_ERR_INVALID_ARG;
-    if (pl.cluster < 0) return VNM_ERR_INVALID_ARG;
-    if (pl.cluster > 1) {
-        // clusters share TMA-loaded B tiles between consecutive 128-row tiles
-        if (pl.cluster != 2 && pl.cluster != 4) return VNM_ERR_UNSUPPORTED;
-        if (A.M != 4 || pl.tile_m != 128) return VNM_ERR_UNSUPPORTED;
-        if (pl.tile_n != 128 && pl.tile_n != 192 && pl.tile_n != 256) return VNM_ERR_UNSUPPORTED;
-        if (ceil_div(A.R, pl.tile_m) % pl.cluster != 0) return VNM_ERR_UNSUPPORTED;
-    }
     const int s = effective_splits(A, pl.splits);
     if (s > 1) {
         const size_t need = static_cast<size_t>(s) * A.R * N * sizeof(float);
@@ -210,7 +199,6 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         L.splits = effective_splits(*A, pl.splits);
         L.gather = A->M > 4;
         L.sm_count = A->sm_count;
-        L.cluster = std::max(1, pl.cluster);
         L.skip_stage = skip_stage;
         const uint64_t vpr = static_cast<uint64_t>(values_per_row(A->K, A->M));
         const uint64_t mp = static_cast<uint64_t>(meta_pitch(A->K, A->M));
@@ -219,12 +207,10 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         ok = ok && encode_2d(&L.tm_e, CU_TENSOR_MAP_DATA_TYPE_UINT32, A->meta, mp / 4, A->R, mp, 4,
                              static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_NONE);
         // B tiles by TMA (M == 4): 64-column atoms, or exactly tile_n columns with the
-        // matching swizzle for 16- and 32-column tiles; in a cluster each CTA loads
-        // 128 / cluster rows of a stage
+        // matching swizzle for 16- and 32-column tiles
         const bool narrow = vnm::tc_narrow_b(pl.tile_n, L.gather);
         ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, A->K, ld_b * 2,
-                             narrow ? static_cast<uint32_t>(pl.tile_n) : 64,
-                             L.gather ? 1 : static_cast<uint32_t>(128 / L.cluster),
+                             narrow ? static_cast<uint32_t>(pl.tile_n) : 64, L.gather ? 1 : 128,
                              !narrow ? CU_TENSOR_MAP_SWIZZLE_128B
                                      : pl.tile_n == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
         if (!ok) return VNM_ERR_CUDA;

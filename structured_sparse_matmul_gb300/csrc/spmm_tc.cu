@@ -48,8 +48,6 @@
 //             the m-index warps drain half of its columns). With M=128 row r
 //             of the tile lives in TMEM lane r; with M=64 in lane
 //             32*(r/16) + r%16 (lanes 16..31 of each quarter stay unused).
-// Clusters (CS = 2 or 4, B by TMA): the CTAs of a cluster take consecutive
-// row tiles of one column tile and share each B tile by multicast.
 // Every mbarrier wait is bounded: on time-out the CTA records
 // VNM_ERR_TIMEOUT, drains what it already issued, frees TMEM and returns.
 #include <cuda_fp16.h>
@@ -92,14 +90,12 @@ struct TcArgs {
     int64_t nblk;
     int num_kt;              // condensed K / kKTile
     int kt_per_split;
-    int n_tiles, m_tiles;    // tile grid; CS = 1: tile t -> (n = t % n_tiles, m = t / n_tiles % m_tiles, split)
-    int total_tiles;         // tiles (CS = 1) or tile groups
+    int n_tiles, m_tiles;    // tile grid: tile t -> (n = t % n_tiles, m = t / n_tiles % m_tiles, split)
+    int total_tiles;
     int c_f32;
     int vec_store;           // C row starts 16-byte aligned
     int skip_stage;          // tests of the bounded waits: CTA 0 never issues this stage's loads (-1: none)
     int* status;
-    int m_groups;            // m_tiles / CS: group t -> n = t % n_tiles, m-group = t / n_tiles % m_groups,
-                             // split = t / n_tiles / m_groups; CTA rank r of a cluster takes m = m-group * CS + r
 };
 
 __host__ __device__ constexpr int pow2_at_least(int x) {
@@ -155,37 +151,14 @@ struct TileGeom {
     int kt0, nkt;    // first stage (of kKTile condensed columns) and stage count
 };
 
-// First tile (group) of this CTA (cluster) and the stride between its tiles.
-template <int CS>
-__device__ __forceinline__ int tile_first() {
-    if constexpr (CS == 1)
-        return static_cast<int>(blockIdx.x);
-    else
-        return static_cast<int>(cluster_index_x());
-}
-template <int CS>
-__device__ __forceinline__ int tile_step() {
-    if constexpr (CS == 1)
-        return static_cast<int>(gridDim.x);
-    else
-        return static_cast<int>(cluster_count_x());
-}
-
-template <int TM, int BN, int CS>
-__device__ __forceinline__ TileGeom tile_geom(const TcArgs& p, int t, int rank) {
+__device__ __forceinline__ TileGeom tile_geom(const TcArgs& p, int t, int tm, int bn) {
     TileGeom g;
     const int n_idx = t % p.n_tiles;
     const int rest = t / p.n_tiles;
-    int m_idx;
-    if constexpr (CS == 1) {
-        m_idx = rest % p.m_tiles;
-        g.split = rest / p.m_tiles;
-    } else {
-        m_idx = (rest % p.m_groups) * CS + rank;
-        g.split = rest / p.m_groups;
-    }
-    g.m0 = static_cast<int64_t>(m_idx) * TM;
-    g.n0 = static_cast<int64_t>(n_idx) * BN;
+    const int m_idx = rest % p.m_tiles;
+    g.split = rest / p.m_tiles;
+    g.m0 = static_cast<int64_t>(m_idx) * tm;
+    g.n0 = static_cast<int64_t>(n_idx) * bn;
     g.kt0 = g.split * p.kt_per_split;
     g.nkt = min(p.num_kt, g.kt0 + p.kt_per_split) - g.kt0;
     return g;
@@ -253,18 +226,10 @@ __device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g
 
 // Persistent: CTA b takes tiles b, b + gridDim.x, ... (all roles walk the
 // same sequence, so their stage and accumulator counters agree).
-// CS > 1 (B by TMA only): clusters of CS CTAs on CS consecutive m-tiles of
-// one column tile; cluster c takes tile groups c, c + clusters, ... Each CTA
-// loads 128/CS of the 128 B rows of a stage and multicasts them to the whole
-// cluster, so the L2 serves every B tile once per cluster instead of once
-// per CTA; a stage slot is free again only when the MMAs of every CTA of the
-// cluster are done with it (each MMA thread's commit arrives on the stage's
-// barrier in all of them).
-template <int TM, int BN, bool GATHER, int CS>
+template <int TM, int BN, bool GATHER>
 __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_e,
                    const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
-    static_assert(CS == 1 || (!GATHER && !tc_narrow_b(BN, GATHER) && (CS == 2 || CS == 4)), "clusters: TMA B tiles");
     using Cfg = TcCfg<TM, BN, tc_narrow_b(BN, GATHER)>;
     constexpr int STAGES = Cfg::kStages;
     constexpr int ACC = Cfg::kAccBufs;
@@ -297,15 +262,13 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     const uint8_t* sE_generic = smem_raw + (sE0 - smem_u32(smem_raw));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-    constexpr uint16_t kClusterMask = static_cast<uint16_t>((1u << CS) - 1u);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(smem_u32(&ae_bar[s]), 1);
             mbar_init(smem_u32(&b_bar[s]), GATHER ? kGatherThreads : 1);
             mbar_init(smem_u32(&meta_bar[s]), 4);
-            mbar_init(smem_u32(&empty_bar[s]), CS);  // one commit per CTA of the cluster
+            mbar_init(smem_u32(&empty_bar[s]), 1);
         }
         for (int b = 0; b < ACC; ++b) {
             mbar_init(smem_u32(&accf_bar[b]), 1);
@@ -326,8 +289,6 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     }
     tc_fence_before_sync();
     __syncthreads();
-    // no CTA multicasts into another before that one's barriers exist
-    if (CS > 1) cluster_sync_all();
     tc_fence_after_sync();
     const uint32_t tmem_acc = tmem_slot;           // columns [0, ACC*BN): fp32 accumulators
     const uint32_t tmem_e = tmem_slot + ACC * BN;  // then STAGES*32 columns of m-index words
@@ -340,8 +301,8 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         for (int s = 0; s < STAGES; ++s) last_it[s] = -1;
         int it = 0;
         bool run = true;
-        for (int t = tile_first<CS>(); run && t < p.total_tiles; t += tile_step<CS>()) {
-            const TileGeom g = tile_geom<TM, BN, CS>(p, t, rank);
+        for (int t = static_cast<int>(blockIdx.x); run && t < p.total_tiles; t += static_cast<int>(gridDim.x)) {
+            const TileGeom g = tile_geom(p, t, TM, BN);
             for (int k = 0; k < g.nkt; ++k, ++it) {
                 const int slot = it % STAGES;
                 const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
@@ -364,17 +325,8 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                     tma_load_2d(sE, &tm_e, kt * 4, static_cast<int32_t>(g.m0), aeb);
                     if (!GATHER) {
                         const uint32_t bb = smem_u32(&b_bar[slot]);
-                        mbar_arrive_expect_tx(bb, Cfg::kBBytes);  // from every CTA of the cluster
-                        if (CS > 1) {
-                            // rows [rank * 128/CS, (rank + 1) * 128/CS) of every 64-column atom: whole
-                            // 1024-byte groups of 8 rows, so the 128B swizzle matches the full box's
-                            constexpr int kRows = kKTile / CS;
-#pragma unroll
-                            for (int a = 0; a < Cfg::kAtoms; ++a)
-                                tma_load_2d_mc(sB + a * kKTile * 128 + rank * kRows * 128, &tm_b,
-                                               static_cast<int32_t>(g.n0 + 64 * a), kt * kKTile + rank * kRows, bb,
-                                               kClusterMask);
-                        } else if (tc_narrow_b(BN, GATHER)) {
+                        mbar_arrive_expect_tx(bb, Cfg::kBBytes);
+                        if (tc_narrow_b(BN, GATHER)) {
                             tma_load_2d(sB, &tm_b, static_cast<int32_t>(g.n0), kt * kKTile, bb);
                         } else {
 #pragma unroll
@@ -402,8 +354,8 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             constexpr uint32_t idesc = make_idesc_f16_f32(TM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/true);
             int it = 0, ti = 0;
             bool run = true;
-            for (int t = tile_first<CS>(); run && t < p.total_tiles; t += tile_step<CS>(), ++ti) {
-                const TileGeom g = tile_geom<TM, BN, CS>(p, t, rank);
+            for (int t = static_cast<int>(blockIdx.x); run && t < p.total_tiles; t += static_cast<int>(gridDim.x), ++ti) {
+                const TileGeom g = tile_geom(p, t, TM, BN);
                 const int buf = ti % ACC;
                 const uint32_t use = static_cast<uint32_t>(ti / ACC) & 1u;
                 // the epilogue must have read this accumulator out (first use passes)
@@ -439,10 +391,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                         const uint32_t te = tmem_e + slot * kMetaStageCols + s * kMetaSlotCols;
                         tc_mma_sp_f16(d, ad, bd, te, idesc, (k > 0 || s > 0) ? 1u : 0u);
                     }
-                    if (CS > 1)
-                        tc_commit_mc(smem_u32(&empty_bar[slot]), kClusterMask);
-                    else
-                        tc_commit(smem_u32(&empty_bar[slot]));
+                    tc_commit(smem_u32(&empty_bar[slot]));
                 }
                 if (run) tc_commit(smem_u32(&accf_bar[buf]));
             }
@@ -473,8 +422,8 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         };
         TileGeom prev;
         int ti = 0;
-        for (int t = tile_first<CS>(); run && t < p.total_tiles; t += tile_step<CS>(), ++ti) {
-            const TileGeom g = tile_geom<TM, BN, CS>(p, t, rank);
+        for (int t = static_cast<int>(blockIdx.x); run && t < p.total_tiles; t += static_cast<int>(gridDim.x), ++ti) {
+            const TileGeom g = tile_geom(p, t, TM, BN);
             if (kSplitEpi && ti > 0 && !drain_upper(prev, ti - 1)) {
                 run = false;
                 break;
@@ -520,8 +469,8 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         const int trow = tile_row_of_lane<TM>(q, lane);
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         int ti = 0;
-        for (int t = tile_first<CS>(); t < p.total_tiles; t += tile_step<CS>(), ++ti) {
-            const TileGeom g = tile_geom<TM, BN, CS>(p, t, rank);
+        for (int t = static_cast<int>(blockIdx.x); t < p.total_tiles; t += static_cast<int>(gridDim.x), ++ti) {
+            const TileGeom g = tile_geom(p, t, TM, BN);
             const int buf = ti % ACC;
             const uint32_t use = static_cast<uint32_t>(ti / ACC) & 1u;
             const bool ok = mbar_wait_warp(smem_u32(&accf_bar[buf]), use, abort, kSleepEpilogue) && !*abort;
@@ -558,17 +507,17 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             bool valid;
         };
         auto it_start = [&](StageIt& x) {
-            x.t = tile_first<CS>();
+            x.t = static_cast<int>(blockIdx.x);
             x.k = 0;
             x.valid = x.t < p.total_tiles;
-            if (x.valid) x.g = tile_geom<TM, BN, CS>(p, x.t, rank);
+            if (x.valid) x.g = tile_geom(p, x.t, TM, BN);
         };
         auto it_next = [&](StageIt& x) {
             if (++x.k == x.g.nkt) {
                 x.k = 0;
-                x.t += tile_step<CS>();
+                x.t += static_cast<int>(gridDim.x);
                 x.valid = x.t < p.total_tiles;
-                if (x.valid) x.g = tile_geom<TM, BN, CS>(p, x.t, rank);
+                if (x.valid) x.g = tile_geom(p, x.t, TM, BN);
             }
         };
         // Lane l holds column-loc word l (block l of the stage) of the stages
@@ -643,16 +592,6 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     // ---------------------------------------------------- teardown
     tc_fence_before_sync();
     __syncthreads();
-    if (CS > 1) {
-        // every CTA of the cluster has issued all its copies and its MMAs have
-        // all completed (so have their arrivals here); after a time-out, give
-        // copies a peer issued into this CTA's shared memory time to land
-        cluster_sync_all();
-        if (abort_flag) {
-            const uint64_t t0 = global_timer_ns();
-            while (global_timer_ns() - t0 < 200000ull) __nanosleep(1000);
-        }
-    }
     if (threadIdx.x == 0 && abort_flag) record_error(p.status, VNM_ERR_TIMEOUT, 10);
     if (warp == 1) {
         tc_fence_after_sync();
@@ -660,81 +599,46 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     }
 }
 
-template <int TM, int BN, bool GATHER, int CS>
+// Co-resident CTAs per SM of one kernel instance on one device (0: not yet
+// known). The kernel's shared-memory attribute is set on the first launch
+// of the instance on each device.
+constexpr int kMaxDevices = 64;
+
+template <int TM, int BN, bool GATHER>
 cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stream) {
     using Cfg = TcCfg<TM, BN, tc_narrow_b(BN, GATHER)>;
-    auto kern = spmm_tc_kernel<TM, BN, GATHER, CS>;
+    auto kern = spmm_tc_kernel<TM, BN, GATHER>;
     constexpr int threads = tc_threads<TM, BN, GATHER>();
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    cfg.blockDim = dim3(threads);
-    cfg.dynamicSmemBytes = Cfg::kSmemBytes;
-    cfg.stream = stream;
-    if (CS > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CS;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    // co-resident CTAs (clusters), once per process (the attribute is per function)
-    static std::atomic<int64_t> resident_cache{0};
-    int64_t resident = resident_cache.load(std::memory_order_relaxed);
-    if (resident == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
+    static std::atomic<int> per_sm_cache[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    int per_sm = per_sm_cache[dev].load(std::memory_order_relaxed);
+    if (per_sm == 0) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmemBytes);
         if (e != cudaSuccess) return e;
         int occ = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, Cfg::kSmemBytes);
         if (e != cudaSuccess) return e;
         // co-resident CTAs must find their TMEM columns free
-        const int per_sm = std::max(1, std::min(occ, 512 / Cfg::kTmemCols));
-        resident = static_cast<int64_t>(L.sm_count) * per_sm;
-        if (CS > 1) {
-            cfg.gridDim = dim3(CS);
-            int clusters = 0;
-            e = cudaOccupancyMaxActiveClusters(&clusters, reinterpret_cast<const void*>(kern), &cfg);
-            if (e != cudaSuccess) return e;
-            if (clusters < 1) return cudaErrorInvalidConfiguration;
-            resident = std::min<int64_t>(resident / CS, clusters);  // in clusters
-        }
-        resident_cache.store(resident, std::memory_order_relaxed);
+        per_sm = std::max(1, std::min(occ, 512 / Cfg::kTmemCols));
+        per_sm_cache[dev].store(per_sm, std::memory_order_relaxed);
     }
-    // p.total_tiles counts tile groups of CS m-tiles
-    const int64_t units = std::min<int64_t>(p.total_tiles, resident);
-    if constexpr (CS == 1) {
-        kern<<<static_cast<unsigned>(units), threads, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_e, L.tm_b, p);
-        return cudaGetLastError();
-    }
-    cfg.gridDim = dim3(static_cast<unsigned>(units * CS));
-    return cudaLaunchKernelEx(&cfg, kern, L.tm_a, L.tm_e, L.tm_b, p);
+    const int64_t units = std::min<int64_t>(p.total_tiles, static_cast<int64_t>(L.sm_count) * per_sm);
+    kern<<<static_cast<unsigned>(units), threads, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_e, L.tm_b, p);
+    return cudaGetLastError();
 }
 
 template <int TM, bool GATHER>
 cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, cudaStream_t stream) {
-    if (L.cluster > 1) {
-        // clusters: TMA-loaded B of 128, 192 or 256 columns, 128-row tiles
-        if constexpr (TM == 128 && !GATHER) {
-            const int key = L.tile_n * 8 + L.cluster;
-            switch (key) {
-                case 128 * 8 + 2: return launch_variant<TM, 128, false, 2>(L, p, stream);
-                case 128 * 8 + 4: return launch_variant<TM, 128, false, 4>(L, p, stream);
-                case 192 * 8 + 2: return launch_variant<TM, 192, false, 2>(L, p, stream);
-                case 192 * 8 + 4: return launch_variant<TM, 192, false, 4>(L, p, stream);
-                case 256 * 8 + 2: return launch_variant<TM, 256, false, 2>(L, p, stream);
-                case 256 * 8 + 4: return launch_variant<TM, 256, false, 4>(L, p, stream);
-                default: return cudaErrorInvalidValue;
-            }
-        }
-        return cudaErrorInvalidValue;
-    }
     switch (L.tile_n) {
-        case 16: return launch_variant<TM, 16, GATHER, 1>(L, p, stream);
-        case 32: return launch_variant<TM, 32, GATHER, 1>(L, p, stream);
-        case 64: return launch_variant<TM, 64, GATHER, 1>(L, p, stream);
-        case 128: return launch_variant<TM, 128, GATHER, 1>(L, p, stream);
-        case 192: return launch_variant<TM, 192, GATHER, 1>(L, p, stream);
-        case 256: return launch_variant<TM, 256, GATHER, 1>(L, p, stream);
+        case 16: return launch_variant<TM, 16, GATHER>(L, p, stream);
+        case 32: return launch_variant<TM, 32, GATHER>(L, p, stream);
+        case 64: return launch_variant<TM, 64, GATHER>(L, p, stream);
+        case 128: return launch_variant<TM, 128, GATHER>(L, p, stream);
+        case 192: return launch_variant<TM, 192, GATHER>(L, p, stream);
+        case 256: return launch_variant<TM, 256, GATHER>(L, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -776,10 +680,7 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
     if (splits > 1 && partial == nullptr) return cudaErrorInvalidValue;
     p.n_tiles = static_cast<int>((N + L.tile_n - 1) / L.tile_n);
     p.m_tiles = static_cast<int>((A.R + L.tile_m - 1) / L.tile_m);
-    const int cs = std::max(1, L.cluster);
-    if (p.m_tiles % cs != 0) return cudaErrorInvalidValue;
-    p.m_groups = p.m_tiles / cs;
-    const int64_t total = static_cast<int64_t>(p.n_tiles) * p.m_groups * splits;
+    const int64_t total = static_cast<int64_t>(p.n_tiles) * p.m_tiles * splits;
     if (total > INT32_MAX) return cudaErrorInvalidValue;
     p.total_tiles = static_cast<int>(total);
     cudaError_t e;

@@ -81,9 +81,6 @@ struct TcLaunch {
     int tile_m, tile_n, stages, splits;
     bool gather;        // M > 4: rows of B selected through colidx
     int sm_count;       // persistent grid: at most sm_count x resident CTAs per SM
-    int cluster;        // CTAs per cluster sharing each B tile by TMA multicast (1: none; 2, 4:
-                        // B by TMA, tile_m 128, tile_n 128/192/256, m-tiles a multiple of it);
-                        // tm_b's box is then {64, 128 / cluster}
     int skip_stage;     // tests of the bounded waits only (-1: none)
 };
 

@@ -1,7 +1,7 @@
-// Inline-PTX helpers for sm_103a: mbarriers with bounded waits, TMA tensor
-// loads (tiled, and multicast within a cluster), cluster and distributed
-// shared memory access, and the tcgen05 tensor-core instructions (TMEM
-// allocation, sparse MMA, TMEM loads and stores).
+// Inline-PTX helpers for sm_103a: mbarriers with bounded waits, tiled TMA
+// tensor loads, cluster barriers and distributed shared memory access, and
+// the tcgen05 tensor-core instructions (TMEM allocation, sparse MMA, TMEM
+// loads and stores).
 // Every wait here gives up after a time limit and raises a CTA-wide abort
 // flag instead of spinning forever.
 #pragma once
@@ -115,37 +115,7 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm,
         : "memory");
 }
 
-// The same load multicast to the CTAs of this cluster whose bit is set in
-// `cta_mask`: the box lands at offset `dst` of each one's shared memory and
-// signals the barrier at offset `bar` of each one.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* tm, int32_t x, int32_t y,
-                                               uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "h"(cta_mask)
-        : "memory");
-}
-
 // ----------------------------------------------------------------- clusters
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_index_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-    return r;
-}
-
-__device__ __forceinline__ uint32_t cluster_count_x() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-    return r;
-}
 
 // Address in the shared memory of cluster CTA `rank` of the variable at
 // shared-memory address `local` in this CTA (distributed shared memory).
@@ -225,16 +195,6 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-// The same arrival on the barrier at offset `bar` of every CTA of the
-// cluster whose bit is set in `cta_mask`.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            bar),
-        "h"(cta_mask)
-        : "memory");
 }
 
 // D[tmem] (+)= A[smem, 2:4 sparse, compressed] x B[smem], f16 inputs,

@@ -79,3 +79,24 @@ def sample_rows(R: int, V: int, count: int, seed: int = 0):
     for b in blocks:
         rows.add(int(b * V + rng.integers(0, V)))
     return sorted(r for r in rows if 0 <= r < R)
+
+
+def check_tight_f32(got: np.ndarray, comp, R: int, K: int, V: int, M: int, B: np.ndarray, rows=None,
+                    what: str = ""):
+    """fp32 C against the oracle's fp64 product within the fp32 summation
+    bound: every product of two fp16 values is exact in fp32, so only the
+    accumulation of the 2K/M kept products of a row rounds. With n terms
+    the rounding error of any summation order is at most (n - 1) ulps of
+    the running sum, i.e. below n * 2^-23 * sum |a||b| even when each
+    addition truncates instead of rounding; the bound below allows twice
+    that. A single dropped or mis-selected product (|a||b| ~ 0.02 here) is
+    far above it, unlike the 1e-2 * (1 + |C|) tolerance."""
+    values, meta, colidx = comp
+    n_terms = 2 * (K // M)
+    ref64 = oracle.spmm(values, meta, colidx, R, K, V, M, B, rows=rows, acc="f64")
+    mag = oracle.spmm(values & np.uint16(0x7FFF), meta, colidx, R, K, V, M, np.abs(B), rows=rows, acc="f64")
+    bound = n_terms * 2.0 ** -22 * mag + 1e-30
+    err = np.abs(got.astype(np.float64) - ref64)
+    bad = np.argwhere(~(err <= bound))
+    assert bad.size == 0, (f"{what}: {len(bad)} elements beyond the fp32 summation bound, first {bad[:4].tolist()}: "
+                           f"err {[err[tuple(b)] for b in bad[:4]]} bound {[bound[tuple(b)] for b in bad[:4]]}")

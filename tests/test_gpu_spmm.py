@@ -14,8 +14,8 @@ from structured_sparse_matmul_gb300 import inputs, vnm, workloads
 
 pytestmark = pytest.mark.gpu
 
-from gpu_util import (assert_compress_bitexact, check_close, device, gpu_compress, run_spmm,  # noqa: E402
-                      sample_rows, to_dev)
+from gpu_util import (assert_compress_bitexact, check_close, check_tight_f32, device, gpu_compress,  # noqa: E402
+                      run_spmm, sample_rows, to_dev)
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
 
@@ -77,6 +77,8 @@ def test_tensor_core_path(R, K, N, V, M, c_dtype):
     assert plan.path == vnm.VNM_PATH_TC, plan.as_dict()
     got, _ = run_spmm(A, B, c_dtype)
     check_close(got, _ref(comp, R, K, V, M, B), f"tc {R}x{K}x{N} {V}:2:{M}")
+    if c_dtype == torch.float32:
+        check_tight_f32(got, comp, R, K, V, M, B, what=f"tc {R}x{K}x{N} {V}:2:{M}")
 
 
 @pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 192, 256])
@@ -104,73 +106,19 @@ def test_tensor_core_tiles_plain_2to4(tile_n):
     plan.tile_n = tile_n
     plan.stages = 0
     plan.splits = 1
-    plan.cluster = 1  # one CTA per tile (the default plan pairs CTAs for wide tiles)
     got, _ = run_spmm(A, B, plan=plan)
     check_close(got, _ref(comp, R, K, V, M, B), f"plain 2:4 tile_n {tile_n}")
 
 
-@pytest.mark.parametrize("cluster", [2, 4])
-@pytest.mark.parametrize("tile_n", [128, 192, 256])
-def test_tensor_core_clusters(cluster, tile_n):
-    """M = 4 with clusters of CTAs on consecutive row tiles sharing every B
-    tile by TMA multicast: ragged rows (the last row tile half empty), ragged
-    N, both C types."""
-    R, K, N, V, M = 960, 1024, 424, 64, 4
-    A, B, comp = _setup(R, K, N, V, M, seed=31)
+def test_reserved_plan_fields_rejected():
+    """A plan whose reserved words are not zero is refused before any launch."""
+    R, K, N, V, M = 256, 512, 128, 128, 4
+    A, B, _ = _setup(R, K, N, V, M, seed=34)
     plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
-    assert plan.path == vnm.VNM_PATH_TC and plan.tile_m == 128
-    plan.tile_n = tile_n
-    plan.stages = 0
-    plan.splits = 1
-    plan.cluster = cluster
-    ref = _ref(comp, R, K, V, M, B)
-    for c_dtype in (torch.float16, torch.float32):
-        got, _ = run_spmm(A, B, c_dtype, plan=plan)
-        check_close(got, ref, f"cluster {cluster} tile_n {tile_n}")
-
-
-@pytest.mark.parametrize("cluster", [2, 4])
-def test_tensor_core_clusters_persistent(cluster):
-    """Many more tile groups than resident clusters (each cluster walks
-    several), checked on sampled rows; and clusters with split K."""
-    R, K, N, V, M = 4096, 1024, 2048, 128, 4
-    A, B, comp = _setup(R, K, N, V, M, seed=32)
-    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
-    plan.tile_n = 128
-    plan.stages = 0
-    plan.splits = 1
-    plan.cluster = cluster
-    got, _ = run_spmm(A, B, plan=plan)
-    rows = sample_rows(R, V, 40)
-    check_close(got[rows], _ref(comp, R, K, V, M, B, rows=rows), f"cluster {cluster} persistent")
-
-    R, K, N = 512, 4096, 136
-    A, B, comp = _setup(R, K, N, V, M, seed=33)
-    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
-    plan.tile_n = 128
-    plan.stages = 0
-    plan.splits = 3
-    plan.cluster = cluster
-    got, _ = run_spmm(A, B, torch.float32, plan=plan)
-    check_close(got, _ref(comp, R, K, V, M, B), f"cluster {cluster} split K")
-
-
-def test_cluster_plans_rejected():
-    """Clusters need TMA-loaded B (M = 4), 128-row tiles, tile_n >= 128 and a
-    whole number of clusters over the row tiles."""
-    cases = [((384, 512, 128, 128, 4), {"cluster": 2}),                  # 3 row tiles
-             ((512, 512, 128, 128, 4), {"cluster": 3}),
-             ((512, 512, 128, 128, 4), {"cluster": 2, "tile_n": 64}),
-             ((512, 1024, 256, 128, 8), {"cluster": 2})]                 # gathered B
-    for (R, K, N, V, M), edits in cases:
-        A, B, _ = _setup(R, K, N, V, M, seed=34)
-        plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
-        plan.stages = 0
-        for k, v in edits.items():
-            setattr(plan, k, v)
-        with pytest.raises(vnm.VnmError) as e:
-            run_spmm(A, B, plan=plan)
-        assert e.value.code == vnm.VNM_ERR_UNSUPPORTED, (R, K, N, V, M, edits)
+    plan.reserved[0] = 2
+    with pytest.raises(vnm.VnmError) as e:
+        run_spmm(A, B, plan=plan)
+    assert e.value.code == vnm.VNM_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("splits", [2, 3, 5])
@@ -183,6 +131,7 @@ def test_tensor_core_split_k(splits):
     for c_dtype in (torch.float16, torch.float32):
         got, _ = run_spmm(A, B, c_dtype, plan=plan)
         check_close(got, _ref(comp, R, K, V, M, B), f"splits {splits}")
+    check_tight_f32(got, comp, R, K, V, M, B, what=f"splits {splits}")
 
 
 @pytest.mark.parametrize("R,K,N,V,M", [(256, 1024, 200, 128, 8), (272, 256, 72, 16, 4), (96, 600, 33, 8, 5),
@@ -194,6 +143,7 @@ def test_cuda_core_path(R, K, N, V, M):
     for c_dtype in (torch.float16, torch.float32):
         got, _ = run_spmm(A, B, c_dtype, plan=plan)
         check_close(got, _ref(comp, R, K, V, M, B), f"simt {R}x{K}x{N}")
+    check_tight_f32(got, comp, R, K, V, M, B, what=f"simt {R}x{K}x{N}")
 
 
 @pytest.mark.parametrize("N", [1, 2, 3, 5, 7])
@@ -248,6 +198,9 @@ def _workload_case(case: workloads.Case, max_rows: int):
     rows = None if case.R <= max_rows else sample_rows(case.R, case.V, max_rows // 2)
     ref = _ref(comp, case.R, case.K, case.V, case.M, B, rows=rows)
     check_close(got if rows is None else got[rows], ref, case.name)
+    if case.c_f32:
+        check_tight_f32(got if rows is None else got[rows], comp, case.R, case.K, case.V, case.M, B, rows=rows,
+                        what=case.name)
     return A, Bd
 
 
@@ -257,31 +210,52 @@ def test_workloads(case):
     _workload_case(case, max_rows=256 if case.N >= 2048 else 1024)
 
 
+def _oracle_compress_parallel(W, V, M):
+    """The oracle's compress of all of W, one host thread per group of whole
+    V-block rows (each call is the same plain oracle on its rows; the C code
+    runs outside the GIL). The result equals one call on all of W: the
+    format is computed per V-block row."""
+    from concurrent.futures import ThreadPoolExecutor
+    R = W.shape[0]
+    nb = R // V
+    threads = max(1, min(nb, len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else 8))
+    bounds = [nb * q // threads * V for q in range(threads + 1)]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(lambda q: oracle.compress(W[bounds[q]:bounds[q + 1]], V, M), range(threads)))
+    return tuple(np.concatenate([p[i] for p in parts]) for i in range(3))
+
+
 @pytest.mark.parametrize("case", workloads.workload_cases(5), ids=lambda c: c.name)
 def test_workload5_full_size_sampled(case):
     """The large FFN shape at full size, through the same calls and plan the
-    bench times: the whole W is compressed and multiplied on the GPU; the
-    oracle compresses three block rows (first, middle, last) from the host W
-    and computes a sample of their rows of C, which must match the GPU's
-    arrays bit for bit and its C within the tolerance."""
+    bench times: the whole W is compressed on the GPU and its values,
+    m-indices and column-loc must match the oracle's compress of the whole W
+    bit for bit; C (computed by the GPU for all rows) is checked against the
+    oracle on a sample of rows from the first, middle and last V-block rows
+    and 40 more spread over R."""
     R, K, N, V, M = case.R, case.K, case.N, case.V, case.M
     W = inputs.normal_f16((R, K), case.seed, case.a_stream, workloads.A_SIGMA)
     B = inputs.normal_f16((K, N), case.seed, case.b_stream, workloads.B_SIGMA)
     A, st = gpu_compress(W, V, M)
     assert st == vnm.VNM_OK
     got, _ = run_spmm(A, B, torch.float16)
+    values, meta, colidx = _oracle_compress_parallel(W, V, M)
+    del W
+    gv = A.values.cpu().numpy().view(np.uint16)
+    assert np.array_equal(gv, values), f"values differ at {np.argwhere(gv != values)[:4].tolist()}"
+    del gv
+    gm = A.meta.cpu().numpy()
+    assert np.array_equal(gm, meta), f"meta differs at {np.argwhere(gm != meta)[:4].tolist()}"
+    gc = A.colidx.cpu().numpy()
+    assert np.array_equal(gc, colidx), f"column-loc differs at {np.argwhere(gc != colidx)[:4].tolist()}"
     nb = R // V
     rng = np.random.default_rng(5)
+    rows = set(sample_rows(R, V, 40))
     for i in (0, nb // 2, nb - 1):
-        Wi = W[i * V:(i + 1) * V]
-        values, meta, colidx = oracle.compress(Wi, V, M)
-        rows = slice(i * V, (i + 1) * V)
-        assert np.array_equal(A.values[rows].cpu().numpy().view(np.uint16), values), f"values, block row {i}"
-        assert np.array_equal(A.meta[rows].cpu().numpy(), meta), f"meta, block row {i}"
-        assert np.array_equal(A.colidx[i:i + 1].cpu().numpy(), colidx), f"column-loc, block row {i}"
-        local = sorted(set([0, 1, V // 2, V - 1] + rng.integers(0, V, 4).tolist()))
-        ref = oracle.spmm(values, meta, colidx, V, K, V, M, B, rows=local)
-        check_close(got[[i * V + r for r in local]], ref, f"{case.name} block row {i}")
+        rows.update(i * V + r for r in [0, 1, V // 2, V - 1] + rng.integers(0, V, 4).tolist())
+    rows = sorted(rows)
+    ref = oracle.spmm(values, meta, colidx, R, K, V, M, B, rows=rows)
+    check_close(got[rows], ref, f"{case.name} sampled rows")
 
 
 STREAM_SHAPES = [
@@ -307,6 +281,9 @@ def test_streaming_small_n(R, K, V, M, N, c_dtype):
     for ws in (True, False):
         got, _ = run_spmm(A, B, c_dtype, workspace=ws)
         check_close(got if rows is None else got[rows], ref, f"stream {R}x{K}x{N} {V}:2:{M} ws={ws}")
+        if c_dtype == torch.float32:
+            check_tight_f32(got if rows is None else got[rows], comp, R, K, V, M, B, rows=rows,
+                            what=f"stream {R}x{K}x{N} {V}:2:{M} ws={ws}")
 
 
 @pytest.mark.parametrize("splits", [1, 2, 4, 8])
