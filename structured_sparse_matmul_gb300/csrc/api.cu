@@ -130,13 +130,10 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     }
     pl.path = VNM_PATH_TC;
     pl.tile_m = tc_tile_m_ok(A, 128) ? 128 : 64;
-    // gathering (M > 4): 256-column tiles when N allows (twice the MMA work per
-    // stage for the same per-stage costs); plain 2:4: 192 for wide B (three
-    // pipeline stages of 66 KB and two accumulators), else 128 (finer waves)
-    if (A.M == 4 && N >= 1024)
-        pl.tile_n = 192;
-    else
-        pl.tile_n = (A.M > 4 && N >= 256) ? 256 : N >= 128 ? 128 : static_cast<int32_t>(ceil_div(N, 16) * 16);
+    // 256-column tiles for wide B (measured fastest on every shape: the
+    // per-stage costs are spread over the most MMA work and the fewest A
+    // re-reads); else 128, or N rounded up to a supported width
+    pl.tile_n = N >= 256 ? 256 : N >= 128 ? 128 : static_cast<int32_t>(ceil_div(N, 16) * 16);
     if (pl.tile_n > 64 && pl.tile_n < 128) pl.tile_n = 128;
     if (pl.tile_n > 32 && pl.tile_n < 64) pl.tile_n = 64;
     if (pl.tile_n > 16 && pl.tile_n < 32) pl.tile_n = 32;
@@ -201,16 +198,15 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         L.sm_count = A->sm_count;
         L.skip_stage = skip_stage;
         const uint64_t vpr = static_cast<uint64_t>(values_per_row(A->K, A->M));
-        const uint64_t mp = static_cast<uint64_t>(meta_pitch(A->K, A->M));
+        // A values: one stage (64 values per row, 4 MMA k-steps) per box, 128B swizzle
         bool ok = encode_2d(&L.tm_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A->values, vpr, A->R, vpr * 2, 64,
                             static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_128B);
-        ok = ok && encode_2d(&L.tm_e, CU_TENSOR_MAP_DATA_TYPE_UINT32, A->meta, mp / 4, A->R, mp, 4,
-                             static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_NONE);
         // B tiles by TMA (M == 4): 64-column atoms, or exactly tile_n columns with the
         // matching swizzle for 16- and 32-column tiles
         const bool narrow = vnm::tc_narrow_b(pl.tile_n, L.gather);
         ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, A->K, ld_b * 2,
-                             narrow ? static_cast<uint32_t>(pl.tile_n) : 64, L.gather ? 1 : 128,
+                             narrow ? static_cast<uint32_t>(pl.tile_n) : 64,
+                             L.gather ? 1 : static_cast<uint32_t>(vnm::kTcStageK),
                              !narrow ? CU_TENSOR_MAP_SWIZZLE_128B
                                      : pl.tile_n == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
         if (!ok) return VNM_ERR_CUDA;

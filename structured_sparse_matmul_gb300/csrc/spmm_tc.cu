@@ -7,39 +7,48 @@
 // rows (BSr = V), column-loc is fetched ahead of the B rows it selects, and
 // the output tile is written back with wide, coalesced stores.
 //
-// GB300 design: persistent CTAs (at most one per SM and TMEM share), each
-// taking tiles b, b + grid, ... of C (tile_m x tile_n over a range of the
-// condensed K; tile_m = 128, or 64 when V = 64 and column-loc differs per
-// 64-row block); n varies fastest, so the CTAs running at one time share A
-// rows in L2. Per 128-column stage of the condensed K (4 MMA k-steps):
-//   warp 0    TMA producer. Per stage: one tiled load of the A values
-//             (tile_m rows x 64 values, 128B swizzle; MMA k-step s reads bytes
-//             32s..32s+31 of each row) and one of the m-indices (tile_m rows x
-//             16 bytes), on their own barrier, and, when M == 4 (column-loc is
-//             the identity), the B rows as plain tiled loads on a second one.
-//             TMA instructions cost the SM's copy engine ~100 cycles each
-//             however small, so a stage issues as few as possible.
-//   warps 10+ (M > 4) the B gather: per stage these warps copy the 128
-//             selected B rows (4 per block, tile_n columns each) with 16-byte
-//             cp.async, coalesced along each row, straight into the
-//             128B-swizzled operand layout (zero-filled past N); the
-//             column-loc words that select the rows are loaded four stages
-//             ahead; each thread's copies arrive on the stage's barrier by
-//             themselves when they land (cp.async.mbarrier.arrive), so every
-//             pipeline stage can be in flight; the MMA thread fences the
-//             generic-proxy writes into the async proxy after acquiring the
-//             barrier.
-//   warps 2-5 per stage, as soon as A and the m-indices landed (B may still
-//             be in flight): read their rows' m-index words from shared memory,
-//             pair them the way the sparse MMA reads them (rows i and i+8 of
-//             each 16-row group share their 16-bit halves between TMEM lanes
-//             i and i+8) and write them to TMEM (tcgen05.st), each MMA's word
-//             in its own 8-column-aligned slot.
-//   warp 1    TMEM owner and MMA issuer (one thread): 4 sparse MMAs of
-//             M=tile_m, N=tile_n, K=32 per stage into an fp32 accumulator in
-//             TMEM; tcgen05.commit releases the stage, and the tile's
-//             accumulator to the epilogue. Two accumulators alternate between
-//             tiles when TMEM holds them (tile_n <= 192).
+// GB300 design: persistent CTAs (one or two per SM by shared memory and
+// TMEM), each taking tiles b, b + grid, ... of C (tile_m x tile_n over a
+// range of the condensed K; tile_m = 128, or 64 when V = 64 and column-loc
+// differs per 64-row block). Tiles are ordered in groups of group_m row
+// tiles: within a group the row tile varies fastest, so the CTAs running at
+// one time cover many row tiles of one or two column slices of B, reusing
+// each gathered slice of B from L2, and a group's A rows (sized to stay in
+// L2) are reused over all the column slices. Two shared-memory rings feed the MMAs: A values
+// and m-indices in slots of 128 condensed-K columns (4 MMA k-steps), and B
+// in slots of 64 condensed-K rows (2 MMA k-steps). A B slot is free again
+// after two MMAs, so most of the ring is always in flight: the gathered B
+// rows come from L2 with a long latency under load, and the bytes a CTA
+// keeps in flight bound its rate.
+//   warp 0    TMA producer. Per A slot: one tiled load of the A values
+//             (tile_m rows x 64 values, 128B swizzle; MMA k-step s reads
+//             bytes 32s..32s+31 of each row) and one of the m-indices
+//             (tile_m rows x 16 bytes); when M == 4 (column-loc is the
+//             identity) also the two B slots of those columns, as tiled
+//             loads of 64-column x 64-row boxes.
+//   warps 10+ (M > 4) the B gather: each warp owns whole blocks of 4
+//             selected rows per B slot; every lane reads the blocks'
+//             column-loc words (loaded eight slots ahead) and computes its
+//             own source rows, then copies 16-byte chunks with cp.async,
+//             coalesced along each row, straight into the 128B-swizzled
+//             operand layout (zero-filled past N). Each slot's copies are one
+//             cp.async group. Before it waits for the next free slot, a warp
+//             waits for the group it issued B_SLOTS-1 slots earlier
+//             (cp.async.wait_group), fences those generic-proxy writes into
+//             the async proxy, and one lane arrives on that slot's barrier:
+//             one arrival per warp and slot, all but one slot of the ring in
+//             flight, and the MMAs never wait on a slot whose copies landed.
+//   warps 2-5 per A slot, as soon as A and the m-indices landed: read their
+//             rows' m-index words from shared memory, pair them the way the
+//             sparse MMA reads them (rows i and i+8 of each 16-row group
+//             share their 16-bit halves between TMEM lanes i and i+8) and
+//             write them to TMEM (tcgen05.st), each MMA's word in its own
+//             8-column-aligned slot.
+//   warp 1    TMEM owner and MMA issuer (one thread): 2 sparse MMAs of
+//             M=tile_m, N=tile_n, K=32 per B slot into an fp32 accumulator
+//             in TMEM; tcgen05.commit frees each B slot, each A slot, and
+//             hands the tile's accumulator to the epilogue. Two accumulators
+//             alternate between tiles when TMEM holds them (tile_n <= 208).
 //   warps 6-9 epilogue: TMEM -> registers (tcgen05.ld) -> fp16 (RNE) or
 //             fp32 -> global, each thread writing whole 32-byte sectors of
 //             its row (fp32 partials to the workspace under split-K), while
@@ -62,25 +71,31 @@
 namespace vnm {
 namespace {
 
-constexpr int kTcWarpsFixed = 10;  // warps 0-9; gathering CTAs add gather warps after them
+constexpr int kTcWarpsFixed = 11;  // warps 0-10; gathering CTAs add gather warps after them
 constexpr int kEpiWarp0 = 6;       // warps 6-9: epilogue
-constexpr int kKTile = 128;        // condensed K per stage = 4 MMAs of K = 32
-constexpr int kValsPerKTile = 64;  // stored values per row per stage (128 bytes)
+constexpr int kBProducerWarp = 10; // B by TMA (M == 4)
+constexpr int kKSteps = kTcStageK / 32;        // MMA k-steps (K = 32) per stage
+constexpr int kValsPerStage = kTcStageK / 2;   // stored values per row per stage (128 bytes)
 constexpr int kMetaSlotCols = 8;   // TMEM columns between consecutive MMAs' m-index words
-constexpr int kMetaStageCols = 4 * kMetaSlotCols;
+constexpr int kMetaStageCols = kKSteps * kMetaSlotCols;
 // Sleep between polls of a barrier, per role (ns): the MMA thread polls
 // flat out; the others park so that ~20 waiting warps do not take the issue
 // slots of the ones doing work. The epilogue waits a whole tile.
 constexpr uint32_t kSleepProducer = 32;
-constexpr uint32_t kSleepMeta = 64;
-constexpr uint32_t kSleepGather = 64;
+constexpr uint32_t kSleepMeta = 32;
+constexpr uint32_t kSleepGather = 32;
 constexpr uint32_t kSleepEpilogue = 256;
 // m-index word of a row that lies beyond R: slots (0, 1) in all 8 groups
 constexpr uint32_t kPadMeta = 0x44444444u;
+// stages ahead of their use at which the m-index warps load the m-index
+// words of their rows (fewer when they also drain half of the accumulator)
+__host__ __device__ constexpr int meta_prefetch(bool split_epilogue) { return split_epilogue ? 2 : 4; }
 
 struct TcArgs {
     const uint32_t* colidx;  // [R/V][nblk] words of 4 column bytes
     const uint16_t* B;       // K x N fp16 (ld_b), read by the gather warps
+    const uint8_t* meta;     // [R][mpitch] m-indices, read by the m-index warps
+    int64_t mpitch;
     int64_t ld_b;
     void* C;
     int64_t ld_c;
@@ -88,12 +103,15 @@ struct TcArgs {
     int64_t R, N;
     int V, M;
     int64_t nblk;
-    int num_kt;              // condensed K / kKTile
-    int kt_per_split;
-    int n_tiles, m_tiles;    // tile grid: tile t -> (n = t % n_tiles, m = t / n_tiles % m_tiles, split)
+    int num_kt;              // condensed K / kTcStageK: B stages of a whole row
+    int kt_per_split;        // B stages per K split
+    int n_tiles, m_tiles;    // tile grid (see tile_geom for the order)
+    int group_m;             // row tiles per group of the tile order
     int total_tiles;
     int c_f32;
     int vec_store;           // C row starts 16-byte aligned
+    int vec32;               // C row starts 32-byte aligned (32-byte stores)
+    int part_vec32;          // split-K partial rows 32-byte aligned
     int skip_stage;          // tests of the bounded waits: CTA 0 never issues this stage's loads (-1: none)
     int* status;
 };
@@ -104,39 +122,41 @@ __host__ __device__ constexpr int pow2_at_least(int x) {
     return p;
 }
 
-template <int TM, int BN, bool NARROW>
+// Gather warps of a gathering CTA (each owns 32 / warps blocks of a stage):
+// 16 for wide tiles (one CTA per SM), 8 for tiles of at most 64 columns
+// (two CTAs per SM).
+__host__ __device__ constexpr int gather_warps(int bn) { return bn <= 64 ? 8 : 16; }
+
+template <int TM, int BN, bool GATHER>
+__host__ __device__ constexpr int tc_threads() {
+    return kTcWarpsFixed * 32 + (GATHER ? 32 * gather_warps(BN) : 0);
+}
+
+// B stages ahead of their use at which a gather warp loads their column-loc
+// words (8 words per warp in flight)
+__host__ __device__ constexpr int col_prefetch(int blocks_per_warp) { return 8 / blocks_per_warp; }
+
+template <int TM, int BN, bool GATHER>
 struct TcCfg {
-    static constexpr int kAtoms = (BN + 63) / 64;            // 64-column swizzle atoms of B
-    static constexpr int kABytes = TM * 128;                 // TM rows x 64 values, 128B swizzle
-    // per atom: 128 rows x 128 B; narrow: 128 rows x BN x 2 B
-    static constexpr int kBBytes = NARROW ? kKTile * BN * 2 : kAtoms * kKTile * 128;
-    static constexpr int kEBytes = TM * 16;                  // 4 m-index words per row
-    static constexpr int kStageBytes = kABytes + kBBytes + kEBytes;
-    static constexpr int kStages = tc_stages_for(TM, BN, NARROW);
+    static constexpr bool kNarrow = tc_narrow_b(BN, GATHER);
+    static constexpr int kAtoms = (BN + 63) / 64;      // 64-column swizzle atoms of B
+    static constexpr int kABytes = tc_a_stage_bytes(TM);
+    static constexpr int kBBytes = tc_b_stage_bytes(BN, kNarrow);
+    static constexpr int kStages = tc_stages(TM, BN, kNarrow);
+    static constexpr int kAStages = tc_a_stages(TM, kStages);
     // two accumulators (the epilogue of one tile overlaps the next tile's
     // main loop) when they fit TMEM beside the m-index slots
     static constexpr int kAccBufs = 2 * BN + kStages * kMetaStageCols <= 512 ? 2 : 1;
     static constexpr int kTmemCols = pow2_at_least(kAccBufs * BN + kStages * kMetaStageCols);
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+    static constexpr int kSmemBytes = kStages * kBBytes + kAStages * kABytes + 1024;  // + alignment
+    static constexpr int kMinBlocks = BN <= 64 ? 2 : 1;
     static_assert(kStages >= 2, "pipeline depth");
+    static_assert(kAStages >= 2 && kAStages <= kStages, "A ring depth");
     static_assert(BN + kStages * kMetaStageCols <= 512, "TMEM budget");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(TM == 64 || TM == 128, "MMA M");
+    static_assert(kBBytes % 1024 == 0 || kNarrow, "B stages keep the 1024-byte swizzle alignment");
 };
-
-// Gather threads of a gathering CTA: the gathered B tile needs many 16-byte
-// copies in flight per SM (one CTA per SM): 16 warps (measured 1-5 % faster
-// than 8 for 128-row tiles too); never more threads than 16-byte chunks per
-// stage (kKTile * BN / 8).
-__host__ __device__ constexpr int gather_threads(int tm, int bn) {
-    // 192 columns are 24 chunks a row: a multiple of 24 threads, 8 rows each
-    return (void)tm, bn == 192 ? 384 : 512 < kKTile * bn / 8 ? 512 : kKTile * bn / 8;
-}
-
-template <int TM, int BN, bool GATHER>
-__host__ __device__ constexpr int tc_threads() {
-    return kTcWarpsFixed * 32 + (GATHER ? gather_threads(TM, BN) : 0);
-}
 
 // TMEM lane quarter q (warp % 4), lane l -> row of the tile (or -1).
 template <int TM>
@@ -148,15 +168,24 @@ __device__ __forceinline__ int tile_row_of_lane(int q, int l) {
 struct TileGeom {
     int64_t m0, n0;  // first row and column of the C tile
     int split;       // K split
-    int kt0, nkt;    // first stage (of kKTile condensed columns) and stage count
+    int kt0, nkt;    // first stage (of kTcStageK condensed columns) and stage count
 };
 
+// Tile t: split = t / (m_tiles * n_tiles); within a split, groups of group_m
+// row tiles (the last group may be smaller) by n_tiles column tiles, the row
+// tile varying fastest within a group.
 __device__ __forceinline__ TileGeom tile_geom(const TcArgs& p, int t, int tm, int bn) {
     TileGeom g;
-    const int n_idx = t % p.n_tiles;
-    const int rest = t / p.n_tiles;
-    const int m_idx = rest % p.m_tiles;
-    g.split = rest / p.m_tiles;
+    const int per_split = p.m_tiles * p.n_tiles;
+    g.split = t / per_split;
+    int r = t - g.split * per_split;
+    const int group_tiles = p.group_m * p.n_tiles;
+    const int grp = r / group_tiles;
+    const int first_m = grp * p.group_m;
+    const int gm = min(p.group_m, p.m_tiles - first_m);
+    r -= grp * group_tiles;
+    const int m_idx = first_m + r % gm;
+    const int n_idx = r / gm;
     g.m0 = static_cast<int64_t>(m_idx) * tm;
     g.n0 = static_cast<int64_t>(n_idx) * bn;
     g.kt0 = g.split * p.kt_per_split;
@@ -178,7 +207,10 @@ __device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g
         const bool full = col + 16 <= p.N;
         if (p.partial != nullptr) {
             float* dst = p.partial + (static_cast<int64_t>(g.split) * p.R + row) * p.N + col;
-            if (full && (p.N % 4) == 0) {
+            if (full && p.part_vec32) {
+                st_global_v8(dst, v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+                st_global_v8(dst + 8, v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
+            } else if (full && (p.N % 4) == 0) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     reinterpret_cast<uint4*>(dst)[u] = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
@@ -187,7 +219,10 @@ __device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g
             }
         } else if (p.c_f32) {
             float* dst = static_cast<float*>(p.C) + row * p.ld_c + col;
-            if (full && p.vec_store) {
+            if (full && p.vec32) {
+                st_global_v8(dst, v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
+                st_global_v8(dst + 8, v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
+            } else if (full && p.vec_store) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     reinterpret_cast<uint4*>(dst)[u] = make_uint4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
@@ -202,7 +237,9 @@ __device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g
                 const __half2 t2 = __floats2half2_rn(__uint_as_float(v[2 * u]), __uint_as_float(v[2 * u + 1]));
                 h[u] = *reinterpret_cast<const uint32_t*>(&t2);
             }
-            if (full && p.vec_store) {
+            if (full && p.vec32) {
+                st_global_v8(dst, h[0], h[1], h[2], h[3], h[4], h[5], h[6], h[7]);
+            } else if (full && p.vec_store) {
                 reinterpret_cast<uint4*>(dst)[0] = make_uint4(h[0], h[1], h[2], h[3]);
                 reinterpret_cast<uint4*>(dst)[1] = make_uint4(h[4], h[5], h[6], h[7]);
             } else {
@@ -224,32 +261,55 @@ __device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g
     }
 }
 
-// Persistent: CTA b takes tiles b, b + gridDim.x, ... (all roles walk the
-// same sequence, so their stage and accumulator counters agree).
+// Iterator over a CTA's (tile, stage) sequence; every role walks the same
+// one, so their stage and accumulator counters agree.
+struct StageIt {
+    int t, k;
+    TileGeom g;
+    bool valid;
+};
+
+template <int TM, int BN>
+__device__ __forceinline__ void stage_start(const TcArgs& p, StageIt& x) {
+    x.t = static_cast<int>(blockIdx.x);
+    x.k = 0;
+    x.valid = x.t < p.total_tiles;
+    if (x.valid) x.g = tile_geom(p, x.t, TM, BN);
+}
+
+template <int TM, int BN>
+__device__ __forceinline__ void stage_next(const TcArgs& p, StageIt& x) {
+    if (++x.k < x.g.nkt) return;
+    x.k = 0;
+    x.t += static_cast<int>(gridDim.x);
+    x.valid = x.t < p.total_tiles;
+    if (x.valid) x.g = tile_geom(p, x.t, TM, BN);
+}
+
+// Persistent: CTA b takes tiles b, b + gridDim.x, ...
 template <int TM, int BN, bool GATHER>
-__global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
-    spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_e,
-                   const __grid_constant__ CUtensorMap tm_b, const TcArgs p) {
-    using Cfg = TcCfg<TM, BN, tc_narrow_b(BN, GATHER)>;
-    constexpr int STAGES = Cfg::kStages;
+__global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GATHER>::kMinBlocks)
+    spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const TcArgs p) {
+    using Cfg = TcCfg<TM, BN, GATHER>;
+    constexpr int ST = Cfg::kStages;
+    constexpr int AS = Cfg::kAStages;
     constexpr int ACC = Cfg::kAccBufs;
-    constexpr int kGatherThreads = gather_threads(TM, BN);
-    // With a single accumulator the next tile's MMAs wait for the whole
-    // drain, so for 64-row tiles (16 rows per warp: the drain is bound by
-    // TMEM load latency, not by the stores) the m-index warps, idle then,
-    // drain the upper half of the columns while the epilogue warps drain the
-    // lower half. (128-row tiles measured slower this way: their drain is
-    // bound by the stores, and the next tile's m-indices wait.)
-    constexpr bool kSplitEpi = ACC == 1 && BN >= 64 && TM == 64;
+    constexpr int kGatherThreads = 32 * gather_warps(BN);
+    // The m-index warps never drain the accumulator: their m-index loads run
+    // ahead of the MMAs, and a drain between tiles made them late.
+    constexpr bool kSplitEpi = false;
     constexpr int kEpiCols = kSplitEpi ? BN / 2 : BN;  // columns [0, kEpiCols) drained by the epilogue warps
     extern __shared__ uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t ae_bar[STAGES];     // A values and m-indices landed (TMA)
-    __shared__ __align__(8) uint64_t b_bar[STAGES];      // B rows landed (TMA, or every gather thread)
-    __shared__ __align__(8) uint64_t meta_bar[STAGES];   // m-indices written to TMEM (4 warps)
-    __shared__ __align__(8) uint64_t empty_bar[STAGES];  // MMAs done with the stage
-    __shared__ __align__(8) uint64_t accf_bar[ACC];      // accumulator complete (MMA commit)
-    __shared__ __align__(8) uint64_t acce_bar[ACC];      // accumulator read out (4 epilogue warps)
-    __shared__ __align__(8) uint64_t done_bar;           // every MMA of this CTA complete
+    __shared__ __align__(8) uint64_t b_full[ST];    // B landed (TMA, or every gather thread)
+    __shared__ __align__(8) uint64_t meta_bar[ST];  // the stage's m-indices written to TMEM (4 warps)
+    // b_empty[s % ST]: the MMAs of stage s (and all before it) are done, so
+    // its B rows, its m-index slot and its A stage (s % AS) may be reused
+    __shared__ __align__(8) uint64_t b_empty[ST];
+    __shared__ __align__(8) uint64_t a_full[AS];    // A stage landed (TMA)
+    __shared__ __align__(8) uint64_t accf_bar[ACC]; // accumulator complete (MMA commit)
+    __shared__ __align__(8) uint64_t acce_bar[ACC]; // accumulator read out (4 epilogue warps)
+    __shared__ __align__(8) uint64_t done_bar;      // every MMA of this CTA complete
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
 
@@ -257,19 +317,17 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     // even if its two strides were interpreted the other way round.
     const uint32_t smem_base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t sB0 = smem_base;
-    const uint32_t sA0 = sB0 + STAGES * Cfg::kBBytes;
-    const uint32_t sE0 = sA0 + STAGES * Cfg::kABytes;
-    const uint8_t* sE_generic = smem_raw + (sE0 - smem_u32(smem_raw));
+    const uint32_t sA0 = sB0 + ST * Cfg::kBBytes;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(smem_u32(&ae_bar[s]), 1);
-            mbar_init(smem_u32(&b_bar[s]), GATHER ? kGatherThreads : 1);
+        for (int s = 0; s < ST; ++s) {
+            mbar_init(smem_u32(&b_full[s]), GATHER ? kGatherThreads : 1);
             mbar_init(smem_u32(&meta_bar[s]), 4);
-            mbar_init(smem_u32(&empty_bar[s]), 1);
+            mbar_init(smem_u32(&b_empty[s]), 1);
         }
+        for (int s = 0; s < AS; ++s) mbar_init(smem_u32(&a_full[s]), 1);
         for (int b = 0; b < ACC; ++b) {
             mbar_init(smem_u32(&accf_bar[b]), 1);
             mbar_init(smem_u32(&acce_bar[b]), kSplitEpi ? 8 : 4);
@@ -280,7 +338,6 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     }
     if (threadIdx.x == 32) {
         tma_prefetch_desc(&tm_a);
-        tma_prefetch_desc(&tm_e);
         tma_prefetch_desc(&tm_b);
     }
     if (warp == 1) {
@@ -291,70 +348,105 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem_acc = tmem_slot;           // columns [0, ACC*BN): fp32 accumulators
-    const uint32_t tmem_e = tmem_slot + ACC * BN;  // then STAGES*32 columns of m-index words
+    const uint32_t tmem_e = tmem_slot + ACC * BN;  // then ST*32 columns of m-index words
     volatile int* abort = &abort_flag;
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        int last_it[STAGES];
+        // ------------------------------------------------ A producer (TMA)
+        int last_it[AS];
 #pragma unroll
-        for (int s = 0; s < STAGES; ++s) last_it[s] = -1;
-        int it = 0;
+        for (int s = 0; s < AS; ++s) last_it[s] = -1;
+        int st = 0;
         bool run = true;
         for (int t = static_cast<int>(blockIdx.x); run && t < p.total_tiles; t += static_cast<int>(gridDim.x)) {
             const TileGeom g = tile_geom(p, t, TM, BN);
-            for (int k = 0; k < g.nkt; ++k, ++it) {
-                const int slot = it % STAGES;
-                const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
-                const bool ok = mbar_wait_warp(smem_u32(&empty_bar[slot]), ph ^ 1u, abort, kSleepProducer);
-                if (!ok) {
+            for (int k = 0; k < g.nkt; ++k, ++st) {
+                const int aslot = st % AS;
+                // A stage aslot was last read by stage st - AS: free once that stage's MMAs are done
+                // (AS <= ST, and the MMAs cannot pass stage st - 1 before this load, so the phase
+                // of b_empty waited on here is unambiguous)
+                if (st >= AS && !mbar_wait_warp(smem_u32(&b_empty[(st - AS) % ST]),
+                                                static_cast<uint32_t>((st - AS) / ST) & 1u, abort, kSleepProducer)) {
                     run = false;
                     break;
                 }
-                const int kt = g.kt0 + k;
-                const uint32_t aeb = smem_u32(&ae_bar[slot]);
-                const uint32_t sA = sA0 + slot * Cfg::kABytes;
-                const uint32_t sB = sB0 + slot * Cfg::kBBytes;
-                const uint32_t sE = sE0 + slot * Cfg::kEBytes;
-                if (lane == 0 && blockIdx.x == 0 && it == p.skip_stage) {
-                    // test hook: this stage's loads stay unissued, so the waits on it run out
-                } else if (lane == 0) {
-                    // one box each for the stage's A values (64 per row) and m-index words
-                    mbar_arrive_expect_tx(aeb, Cfg::kABytes + Cfg::kEBytes);
-                    tma_load_2d(sA, &tm_a, kt * kValsPerKTile, static_cast<int32_t>(g.m0), aeb);
-                    tma_load_2d(sE, &tm_e, kt * 4, static_cast<int32_t>(g.m0), aeb);
-                    if (!GATHER) {
-                        const uint32_t bb = smem_u32(&b_bar[slot]);
-                        mbar_arrive_expect_tx(bb, Cfg::kBBytes);
-                        if (tc_narrow_b(BN, GATHER)) {
-                            tma_load_2d(sB, &tm_b, static_cast<int32_t>(g.n0), kt * kKTile, bb);
-                        } else {
-#pragma unroll
-                            for (int a = 0; a < Cfg::kAtoms; ++a)
-                                tma_load_2d(sB + a * kKTile * 128, &tm_b, static_cast<int32_t>(g.n0 + 64 * a),
-                                            kt * kKTile, bb);
-                        }
-                    }
-                    last_it[slot] = it;
+                // test hook: CTA 0 leaves this stage's A load unissued, so the wait on it runs out
+                if (lane == 0 && !(GATHER && blockIdx.x == 0 && st == p.skip_stage)) {
+                    const uint32_t fb = smem_u32(&a_full[aslot]);
+                    mbar_arrive_expect_tx(fb, Cfg::kABytes);
+                    tma_load_2d(sA0 + aslot * Cfg::kABytes, &tm_a, (g.kt0 + k) * kValsPerStage,
+                                static_cast<int32_t>(g.m0), fb);
+                    last_it[aslot] = st;
                 }
             }
         }
         if (lane == 0 && *abort) {
             // let every copy already issued land before the CTA exits
-            for (int s = 0; s < STAGES; ++s) {
-                if (last_it[s] < 0) continue;
-                const uint32_t par = static_cast<uint32_t>(last_it[s] / STAGES) & 1u;
-                mbar_drain(smem_u32(&ae_bar[s]), par);
-                if (!GATHER) mbar_drain(smem_u32(&b_bar[s]), par);
+            for (int s = 0; s < AS; ++s)
+                if (last_it[s] >= 0) mbar_drain(smem_u32(&a_full[s]), static_cast<uint32_t>(last_it[s] / AS) & 1u);
+        }
+    } else if (warp == kBProducerWarp) {
+        // ------------------------------------------------ B producer (TMA, M == 4)
+        if (!GATHER) {
+            int last_it[ST];
+#pragma unroll
+            for (int s = 0; s < ST; ++s) last_it[s] = -1;
+            int it = 0;
+            bool run = true;
+            for (int t = static_cast<int>(blockIdx.x); run && t < p.total_tiles; t += static_cast<int>(gridDim.x)) {
+                const TileGeom g = tile_geom(p, t, TM, BN);
+                for (int k = 0; k < g.nkt; ++k, ++it) {
+                    const int slot = it % ST;
+                    if (!mbar_wait_warp(smem_u32(&b_empty[slot]), (static_cast<uint32_t>(it / ST) & 1u) ^ 1u, abort,
+                                        kSleepProducer)) {
+                        run = false;
+                        break;
+                    }
+                    // test hook: CTA 0 leaves this stage's B loads unissued
+                    if (lane == 0 && !(blockIdx.x == 0 && it == p.skip_stage)) {
+                        const uint32_t fb = smem_u32(&b_full[slot]);
+                        const uint32_t sB = sB0 + slot * Cfg::kBBytes;
+                        const int32_t row = (g.kt0 + k) * kTcStageK;
+                        mbar_arrive_expect_tx(fb, Cfg::kBBytes);
+                        if (Cfg::kNarrow) {
+                            tma_load_2d(sB, &tm_b, static_cast<int32_t>(g.n0), row, fb);
+                        } else {
+#pragma unroll
+                            for (int a = 0; a < Cfg::kAtoms; ++a)
+                                tma_load_2d(sB + a * kTcStageK * 128, &tm_b, static_cast<int32_t>(g.n0 + 64 * a), row,
+                                            fb);
+                        }
+                        last_it[slot] = it;
+                    }
+                }
+            }
+            if (lane == 0 && *abort) {
+                for (int s = 0; s < ST; ++s)
+                    if (last_it[s] >= 0) mbar_drain(smem_u32(&b_full[s]), static_cast<uint32_t>(last_it[s] / ST) & 1u);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
+        // One thread; per stage one combined wait (m-indices, B, A), the four
+        // MMAs and two commits. The shared-memory descriptors are computed
+        // once and advanced by adding the (16-byte unit) offsets of the stage
+        // and the k-step to their start-address field.
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc_f16_f32(TM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/true);
+            // A: K-major, 128B swizzle, 128-byte rows (64 values), 8-row groups 1024 bytes apart;
+            // MMA k-step s takes bytes 32s .. 32s+31 of every row
+            const uint64_t adesc0 = make_smem_desc(sA0, 16, 1024, kLayoutSw128);
+            // B: N-major, 128B swizzle; 64-column atoms 128*128 bytes apart (leading dimension),
+            // 8-row groups of K 1024 bytes apart (stride dimension); narrow: BN * 2-byte rows,
+            // 32B/64B swizzle, 8-row groups 16 * BN bytes apart
+            const uint64_t bdesc0 =
+                Cfg::kNarrow ? make_smem_desc(sB0, 16, 16 * BN, BN == 16 ? kLayoutSw32 : kLayoutSw64)
+                             : make_smem_desc(sB0, Cfg::kAtoms > 1 ? kTcStageK * 128 : 1024, 1024, kLayoutSw128);
+            constexpr uint32_t kBRowBytes = Cfg::kNarrow ? BN * 2 : 128;
             int it = 0, ti = 0;
             bool run = true;
-            for (int t = static_cast<int>(blockIdx.x); run && t < p.total_tiles; t += static_cast<int>(gridDim.x), ++ti) {
+            for (int t = static_cast<int>(blockIdx.x); run && t < p.total_tiles;
+                 t += static_cast<int>(gridDim.x), ++ti) {
                 const TileGeom g = tile_geom(p, t, TM, BN);
                 const int buf = ti % ACC;
                 const uint32_t use = static_cast<uint32_t>(ti / ACC) & 1u;
@@ -362,36 +454,35 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                 if (!mbar_wait(smem_u32(&acce_bar[buf]), use ^ 1u, abort)) break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem_acc + buf * BN;
+                bool ready = false;  // this stage's barriers already seen complete
                 for (int k = 0; k < g.nkt; ++k, ++it) {
-                    const int slot = it % STAGES;
-                    const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
-                    // the m-index warps arrive only after the stage's A values and m-indices landed
-                    if (!mbar_wait(smem_u32(&meta_bar[slot]), ph, abort) ||
-                        !mbar_wait(smem_u32(&b_bar[slot]), ph, abort)) {
+                    const int slot = it % ST;
+                    const int aslot = it % AS;
+                    const uint32_t ph = static_cast<uint32_t>(it / ST) & 1u;
+                    if (!ready && !mbar_wait3(smem_u32(&meta_bar[slot]), ph, smem_u32(&b_full[slot]), ph,
+                                              smem_u32(&a_full[aslot]), static_cast<uint32_t>(it / AS) & 1u, abort)) {
                         run = false;
                         break;
                     }
                     if (GATHER) fence_proxy_async_smem();  // gathered B rows were written by cp.async
                     tc_fence_after_sync();
-                    const uint32_t sA = sA0 + slot * Cfg::kABytes;
-                    const uint32_t sB = sB0 + slot * Cfg::kBBytes;
+                    const uint64_t ad = adesc0 + ((aslot * Cfg::kABytes) >> 4);
+                    const uint64_t bd = bdesc0 + ((slot * Cfg::kBBytes) >> 4);
+                    const uint32_t te = tmem_e + slot * kMetaStageCols;
 #pragma unroll
-                    for (int s = 0; s < 4; ++s) {
-                        // A: K-major, 128B swizzle, 128-byte rows (64 values), 8-row groups 1024 bytes
-                        // apart; MMA k-step s takes bytes 32s .. 32s+31 of every row
-                        const uint64_t ad = make_smem_desc(sA + s * 32, 16, 1024, kLayoutSw128);
-                        // B: N-major, 128B swizzle; 64-column atoms kKTile*128 bytes apart (leading
-                        // dimension), 8-row groups of K 1024 bytes apart (stride dimension)
-                        // narrow: BN * 2-byte rows, 32B/64B swizzle, 8-row groups 16 * BN bytes apart
-                        const uint64_t bd =
-                            tc_narrow_b(BN, GATHER)
-                                ? make_smem_desc(sB + s * 32 * (BN * 2), 16, 16 * BN, BN == 16 ? kLayoutSw32 : kLayoutSw64)
-                                : make_smem_desc(sB + s * 32 * 128, Cfg::kAtoms > 1 ? kKTile * 128 : 1024, 1024,
-                                                 kLayoutSw128);
-                        const uint32_t te = tmem_e + slot * kMetaStageCols + s * kMetaSlotCols;
-                        tc_mma_sp_f16(d, ad, bd, te, idesc, (k > 0 || s > 0) ? 1u : 0u);
+                    for (int s = 0; s < kKSteps; ++s) {
+                        tc_mma_sp_f16(d, ad + 2 * s, bd + ((s * 32 * kBRowBytes) >> 4), te + s * kMetaSlotCols, idesc,
+                                      (k > 0 || s > 0) ? 1u : 0u);
+                        if (s == 1) {
+                            // test the next stage of this tile while these MMAs run
+                            const int nx = it + 1;
+                            const uint32_t nph = static_cast<uint32_t>(nx / ST) & 1u;
+                            ready = k + 1 < g.nkt &&
+                                    mbar_test3(smem_u32(&meta_bar[nx % ST]), nph, smem_u32(&b_full[nx % ST]), nph,
+                                               smem_u32(&a_full[nx % AS]), static_cast<uint32_t>(nx / AS) & 1u);
+                        }
                     }
-                    tc_commit(smem_u32(&empty_bar[slot]));
+                    tc_commit(smem_u32(&b_empty[slot]));
                 }
                 if (run) tc_commit(smem_u32(&accf_bar[buf]));
             }
@@ -402,11 +493,13 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
         __syncwarp();
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------ m-indices -> TMEM (warps 2-5)
+        // Each lane owns one row of the tile: it loads that row's m-index
+        // words of a stage (4 words, one per MMA k-step) from global memory
+        // kMetaPrefetch stages ahead, and once the stage's TMEM slot is free
+        // (the MMAs of its previous use are done) writes them to TMEM.
         const int q = warp & 3;  // this warp may access TMEM lanes 32q .. 32q+31
         const int trow = tile_row_of_lane<TM>(q, lane);
-        const int srow = trow >= 0 ? trow : tile_row_of_lane<TM>(q, lane & 15);  // an in-tile row to read
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
-        int it = 0;
         bool run = true;
         // upper half of tile ti's accumulator (single buffer: use ti & 1), when the split applies
         auto drain_upper = [&](const TileGeom& g, int ti) -> bool {
@@ -420,26 +513,49 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             if (lane == 0) mbar_arrive(smem_u32(&acce_bar[0]));
             return true;
         };
-        TileGeom prev;
-        int ti = 0;
-        for (int t = static_cast<int>(blockIdx.x); run && t < p.total_tiles; t += static_cast<int>(gridDim.x), ++ti) {
-            const TileGeom g = tile_geom(p, t, TM, BN);
-            if (kSplitEpi && ti > 0 && !drain_upper(prev, ti - 1)) {
-                run = false;
-                break;
-            }
-            prev = g;
-            const bool pad = trow < 0 || g.m0 + trow >= p.R;  // lanes with no row act as padding
-            for (int k = 0; k < g.nkt; ++k, ++it) {
-                const int slot = it % STAGES;
-                const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
-                const bool ok = mbar_wait_warp(smem_u32(&ae_bar[slot]), ph, abort, kSleepMeta);
-                if (!ok) {
+        // this lane's four m-index words of a stage (padding past R)
+        auto load_meta = [&](const StageIt& x) -> uint4 {
+            uint4 w = make_uint4(kPadMeta, kPadMeta, kPadMeta, kPadMeta);
+            if (x.valid && trow >= 0 && x.g.m0 + trow < p.R)
+                w = __ldg(reinterpret_cast<const uint4*>(p.meta + (x.g.m0 + trow) * p.mpitch) + (x.g.kt0 + x.k));
+            return w;
+        };
+        constexpr int kMetaPrefetch = meta_prefetch(kSplitEpi);
+        StageIt cur, ahead;
+        stage_start<TM, BN>(p, cur);
+        ahead = cur;
+        uint4 ring[kMetaPrefetch];
+#pragma unroll
+        for (int d = 0; d < kMetaPrefetch; ++d) {
+            ring[d] = load_meta(ahead);
+            if (ahead.valid) stage_next<TM, BN>(p, ahead);
+        }
+        int it = 0, ti = 0, last_t = cur.t;
+        TileGeom prev = cur.g;
+        while (run && cur.valid) {
+#pragma unroll
+            for (int d = 0; d < kMetaPrefetch; ++d) {
+                const uint4 w = ring[d];  // loaded kMetaPrefetch stages ago
+                ring[d] = load_meta(ahead);
+                if (ahead.valid) stage_next<TM, BN>(p, ahead);
+                if (cur.t != last_t) {
+                    // a new tile: with the split epilogue, drain the previous one's upper half first
+                    if (kSplitEpi && !drain_upper(prev, ti)) {
+                        run = false;
+                        break;
+                    }
+                    ++ti;
+                    last_t = cur.t;
+                    prev = cur.g;
+                }
+                const int slot = it % ST;
+                const uint32_t ph = static_cast<uint32_t>(it / ST) & 1u;
+                // the stage's TMEM m-index slot is free once the MMAs of its previous use are done
+                if (!mbar_wait_warp(smem_u32(&b_empty[slot]), ph ^ 1u, abort, kSleepMeta)) {
                     run = false;
                     break;
                 }
-                uint4 w = *reinterpret_cast<const uint4*>(sE_generic + slot * Cfg::kEBytes + srow * 16);
-                if (pad) w = make_uint4(kPadMeta, kPadMeta, kPadMeta, kPadMeta);
+                tc_fence_after_sync();
                 // lane i (i % 16 < 8) pairs its low halves with lane i+8's low halves, lane i+8
                 // its high halves with lane i's: each lane sends the four halves its partner
                 // needs, packed in two words
@@ -451,7 +567,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                 const uint32_t own[4] = {w.x, w.y, w.z, w.w};
                 const uint32_t got[4] = {got01 & 0xFFFFu, got01 >> 16, got23 & 0xFFFFu, got23 >> 16};
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
+                for (int s = 0; s < kKSteps; ++s) {
                     // low lane: [own low | partner low]; high lane: [partner high | own high]
                     const uint32_t word = hi ? (got[s] | (own[s] & 0xFFFF0000u)) : ((own[s] & 0xFFFFu) | (got[s] << 16));
                     tmem_st_32x32b_x1(tmem_e + slot * kMetaStageCols + s * kMetaSlotCols + lane_addr, word);
@@ -460,10 +576,13 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
                 tc_fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&meta_bar[slot]));
+                ++it;
+                stage_next<TM, BN>(p, cur);
+                if (!cur.valid) break;
             }
         }
-        if (kSplitEpi && run && ti > 0) drain_upper(prev, ti - 1);
-    } else if (warp < kTcWarpsFixed) {
+        if (kSplitEpi && run) drain_upper(prev, ti);
+    } else if (warp < kEpiWarp0 + 4) {
         // ------------------------------------------------ epilogue (warps 6-9)
         const int q = warp & 3;
         const int trow = tile_row_of_lane<TM>(q, lane);
@@ -483,103 +602,111 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&acce_bar[buf]));
         }
-    } else if (GATHER) {
-        // ------------------------------------------------ B gather (cp.async), warps 10+
-        constexpr int kChunksPerRow = BN / 8;                       // 16-byte chunks of a gathered row
-        constexpr int kChunks = kKTile * kChunksPerRow;             // per stage
-        static_assert(kChunks % kGatherThreads == 0, "gather split");
-        const int gt = threadIdx.x - kTcWarpsFixed * 32;
-        // Fixed thread -> (chunk, row) map: thread gt copies chunk c of the
-        // kPasses consecutive rows q = q0 * kPasses + u (whole blocks of 4
-        // rows when kPasses >= 4, so one column-loc word serves 4 rows);
-        // consecutive threads cover consecutive 16-byte chunks of a row
-        // (coalesced reads).
-        constexpr int kPasses = kChunks / kGatherThreads;
-        constexpr int kWords = kPasses >= 4 ? kPasses / 4 : 1;  // column-loc words a thread uses per stage
-        const int c = gt % kChunksPerRow;
-        const int q0 = gt / kChunksPerRow;
-        const uint32_t dst_atom = (c >> 3) * (kKTile * 128);  // 64-column atom of chunk c
-        const int cx = c & 7;                                  // chunk within the atom's 128-byte row
-        // Stage iterator over this CTA's (tile, stage) sequence.
-        struct StageIt {
-            int t, k;
-            TileGeom g;
-            bool valid;
-        };
-        auto it_start = [&](StageIt& x) {
-            x.t = static_cast<int>(blockIdx.x);
-            x.k = 0;
-            x.valid = x.t < p.total_tiles;
-            if (x.valid) x.g = tile_geom(p, x.t, TM, BN);
-        };
-        auto it_next = [&](StageIt& x) {
-            if (++x.k == x.g.nkt) {
-                x.k = 0;
-                x.t += static_cast<int>(gridDim.x);
-                x.valid = x.t < p.total_tiles;
-                if (x.valid) x.g = tile_geom(p, x.t, TM, BN);
+    } else if (GATHER && warp >= kTcWarpsFixed) {
+        // ------------------------------------------------ B gather (cp.async), warps 11+
+        // A stage holds 32 blocks of 4 selected rows of B; gather warp gw
+        // owns blocks gw*BPW .. gw*BPW+BPW-1 of every stage. A block's 4 rows
+        // are 4 * CPR 16-byte chunks, copied in P passes of the warp: in pass
+        // i lane l takes chunk q = 32i + l, i.e. chunk q % CPR of row q / CPR
+        // (consecutive lanes read consecutive chunks of a row: coalesced).
+        constexpr int GW = gather_warps(BN);
+        constexpr int kBlocks = kTcStageK / 4;
+        constexpr int BPW = kBlocks / GW;
+        constexpr int CPR = BN / 8;
+        constexpr int P = (4 * CPR + 31) / 32;
+        static_assert(kBlocks % GW == 0, "gather split");
+        const int gw = warp - kTcWarpsFixed;
+        int rb_shift[P];       // 8 * (row of the block) of this lane's chunk in pass i
+        uint32_t dst[P][BPW];  // its offset in the stage, for each of the warp's blocks
+        bool pv[P];
+        int cc[P];
+#pragma unroll
+        for (int i = 0; i < P; ++i) {
+            const int q = 32 * i + lane;
+            pv[i] = q < 4 * CPR;
+            const int rb = pv[i] ? q / CPR : 0;
+            cc[i] = pv[i] ? q % CPR : 0;
+            rb_shift[i] = 8 * rb;
+#pragma unroll
+            for (int j = 0; j < BPW; ++j) {
+                const int qq = 4 * (gw * BPW + j) + rb;  // row of the stage
+                // 128B swizzle: chunk c of row qq sits at chunk (c % 8) ^ (qq % 8) of its atom
+                dst[i][j] = static_cast<uint32_t>((cc[i] >> 3) * (kTcStageK * 128) + qq * 128 +
+                                                  (((cc[i] & 7) ^ (qq & 7)) << 4));
             }
-        };
-        // Lane l holds column-loc word l (block l of the stage) of the stages
-        // kPrefetch ahead: one coalesced 128-byte load per warp and stage, in
-        // flight for kPrefetch stages (a register ring, unrolled).
-        constexpr int kPrefetch = 4;
-        auto load_word = [&](const StageIt& x) -> uint32_t {
-            uint32_t w = 0u;
-            if (x.valid)
-                w = __ldg(p.colidx + (x.g.m0 / p.V) * p.nblk + static_cast<int64_t>(x.g.kt0 + x.k) * 32 + lane);
-            return w;
+        }
+        const int64_t ldb_bytes = p.ld_b * 2;
+        // column-loc words of this warp's blocks of a stage (every lane loads the same words)
+        auto load_words = [&](const StageIt& x, uint32_t (&w)[BPW]) {
+#pragma unroll
+            for (int j = 0; j < BPW; ++j) w[j] = 0u;
+            if (!x.valid) return;
+            const uint32_t* src =
+                p.colidx + (x.g.m0 / p.V) * p.nblk + static_cast<int64_t>(x.g.kt0 + x.k) * kBlocks + gw * BPW;
+#pragma unroll
+            for (int j = 0; j < BPW; ++j) w[j] = __ldg(src + j);
         };
         StageIt cur, ahead;
-        it_start(cur);
+        stage_start<TM, BN>(p, cur);
         ahead = cur;
-        uint32_t ring[kPrefetch];
+        constexpr int kColPrefetch = col_prefetch(BPW);
+        uint32_t ring[kColPrefetch][BPW];
 #pragma unroll
-        for (int j = 0; j < kPrefetch; ++j) {
-            ring[j] = load_word(ahead);
-            if (ahead.valid) it_next(ahead);
+        for (int d = 0; d < kColPrefetch; ++d) {
+            load_words(ahead, ring[d]);
+            if (ahead.valid) stage_next<TM, BN>(p, ahead);
         }
+        const char* bsrc[P];  // this lane's column of B in pass i for the current tile
+        uint32_t fill[P];     // bytes of that 16-byte chunk inside B (the rest is zero-filled)
+        int src_tile = -1;
         int it = 0;
         bool stop = !cur.valid;
         while (!stop) {
 #pragma unroll
-            for (int j = 0; j < kPrefetch; ++j) {
-                const uint32_t word = ring[j];  // this stage's words (loaded kPrefetch stages ago)
-                ring[j] = load_word(ahead);
-                if (ahead.valid) it_next(ahead);
+            for (int d = 0; d < kColPrefetch; ++d) {
+                uint32_t words[BPW];
+#pragma unroll
+                for (int j = 0; j < BPW; ++j) words[j] = ring[d][j];  // loaded kColPrefetch stages ago
+                load_words(ahead, ring[d]);
+                if (ahead.valid) stage_next<TM, BN>(p, ahead);
 
-                const int slot = it % STAGES;
-                const uint32_t ph = static_cast<uint32_t>(it / STAGES) & 1u;
-                const bool ok = mbar_wait_warp(smem_u32(&empty_bar[slot]), ph ^ 1u, abort, kSleepGather);
-                if (!ok) {
+                const int slot = it % ST;
+                const uint32_t ph = static_cast<uint32_t>(it / ST) & 1u;
+                if (!mbar_wait_warp(smem_u32(&b_empty[slot]), ph ^ 1u, abort, kSleepGather)) {
                     stop = true;
                     break;
                 }
                 const TileGeom& g = cur.g;
-                const int64_t col = g.n0 + 8 * c;
-                const int64_t left = p.N - col;
-                const uint32_t bytes = left >= 8 ? 16u : (left > 0 ? static_cast<uint32_t>(2 * left) : 0u);
-                const uint16_t* bcol = p.B + (bytes ? col : 0);
-                const uint32_t sB = sB0 + slot * Cfg::kBBytes + dst_atom;
-                const int64_t kbase = static_cast<int64_t>(g.kt0 + cur.k) * 32 * p.M;
-                constexpr int kRowsPerWord = kPasses >= 4 ? 4 : kPasses;
-#pragma unroll 2
-                for (int wi = 0; wi < kWords; ++wi) {
-                    // the column-loc word of the block holding rows q0*kPasses + 4*wi ..
-                    const uint32_t sel = __shfl_sync(0xFFFFFFFFu, word, ((q0 * kPasses) >> 2) + wi);
+                if (cur.t != src_tile) {
+                    src_tile = cur.t;
 #pragma unroll
-                    for (int r = 0; r < kRowsPerWord; ++r) {
-                        const int qq = q0 * kPasses + wi * 4 + r;  // row of the gathered tile: block qq/4, slot qq%4
-                        // column-loc byte, clamped so that a corrupt array cannot address past K
-                        const uint32_t cb = min((sel >> (8 * (qq & 3))) & 0xFFu, static_cast<uint32_t>(p.M - 1));
-                        const int64_t kr = kbase + (qq >> 2) * p.M + static_cast<int64_t>(cb);
-                        // 128B swizzle: chunk cx of row qq sits at chunk cx ^ (qq % 8)
-                        cp_async_16(sB + qq * 128 + ((cx ^ (qq & 7)) << 4), bcol + kr * p.ld_b, bytes);
+                    for (int i = 0; i < P; ++i) {
+                        const int64_t col = g.n0 + 8 * cc[i];
+                        const int64_t left = p.N - col;
+                        fill[i] = left >= 8 ? 16u : (left > 0 ? static_cast<uint32_t>(2 * left) : 0u);
+                        bsrc[i] = reinterpret_cast<const char*>(p.B + (fill[i] ? col : 0));
                     }
                 }
-                cp_async_arrive_noinc(smem_u32(&b_bar[slot]));
+                // test hook: CTA 0 leaves this stage's B copies unissued (the MMA's wait on it runs out)
+                if (!(blockIdx.x == 0 && it == p.skip_stage)) {
+                    const uint32_t sB = sB0 + slot * Cfg::kBBytes;
+                    // first row of B of block 0 of this stage
+                    const int64_t kbase = static_cast<int64_t>(g.kt0 + cur.k) * kBlocks * p.M;
+#pragma unroll
+                    for (int j = 0; j < BPW; ++j) {
+                        const int64_t rowbase = kbase + static_cast<int64_t>(gw * BPW + j) * p.M;
+#pragma unroll
+                        for (int i = 0; i < P; ++i) {
+                            if (!pv[i]) continue;
+                            // column-loc byte, clamped so that a corrupt array cannot address past K
+                            const uint32_t cb = min((words[j] >> rb_shift[i]) & 0xFFu, static_cast<uint32_t>(p.M - 1));
+                            cp_async_16(sB + dst[i][j], bsrc[i] + (rowbase + cb) * ldb_bytes, fill[i]);
+                        }
+                    }
+                    cp_async_arrive_noinc(smem_u32(&b_full[slot]));
+                }
                 ++it;
-                it_next(cur);
+                stage_next<TM, BN>(p, cur);
                 if (!cur.valid) {
                     stop = true;
                     break;
@@ -606,7 +733,7 @@ constexpr int kMaxDevices = 64;
 
 template <int TM, int BN, bool GATHER>
 cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stream) {
-    using Cfg = TcCfg<TM, BN, tc_narrow_b(BN, GATHER)>;
+    using Cfg = TcCfg<TM, BN, GATHER>;
     auto kern = spmm_tc_kernel<TM, BN, GATHER>;
     constexpr int threads = tc_threads<TM, BN, GATHER>();
     static std::atomic<int> per_sm_cache[kMaxDevices];
@@ -626,7 +753,7 @@ cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stre
         per_sm_cache[dev].store(per_sm, std::memory_order_relaxed);
     }
     const int64_t units = std::min<int64_t>(p.total_tiles, static_cast<int64_t>(L.sm_count) * per_sm);
-    kern<<<static_cast<unsigned>(units), threads, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_e, L.tm_b, p);
+    kern<<<static_cast<unsigned>(units), threads, Cfg::kSmemBytes, stream>>>(L.tm_a, L.tm_b, p);
     return cudaGetLastError();
 }
 
@@ -648,7 +775,7 @@ cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, cudaStream_t stream)
 int tc_default_stages(int tile_m, int tile_n, bool gather) {
     if (tile_m != 64 && tile_m != 128) return 0;
     if (tile_n != 16 && tile_n != 32 && tile_n != 64 && tile_n != 128 && tile_n != 192 && tile_n != 256) return 0;
-    return tc_stages_for(tile_m, tile_n, tc_narrow_b(tile_n, gather));
+    return tc_stages(tile_m, tile_n, tc_narrow_b(tile_n, gather));
 }
 
 cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void* B, int64_t ld_b, int64_t N, void* C,
@@ -667,19 +794,35 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
     p.V = A.V;
     p.M = A.M;
     p.nblk = A.K / A.M;
-    p.num_kt = static_cast<int>(p.nblk / 32);
-    const int splits_req = max(1, min(L.splits, p.num_kt));
-    p.kt_per_split = (p.num_kt + splits_req - 1) / splits_req;
-    const int splits = (p.num_kt + p.kt_per_split - 1) / p.kt_per_split;
+    p.meta = static_cast<const uint8_t*>(A.meta);
+    p.mpitch = meta_pitch(A.K, A.M);
+    // K splits are whole 128-column units of the condensed K (the host sizes
+    // the workspace by the same rule), one B stage each
+    static_assert(kTcStageK == 128, "one B stage per 128-column unit");
+    const int units = static_cast<int>(p.nblk / 32);
+    const int splits_req = max(1, min(L.splits, units));
+    const int units_per_split = (units + splits_req - 1) / splits_req;
+    const int splits = (units + units_per_split - 1) / units_per_split;
+    p.num_kt = units;
+    p.kt_per_split = units_per_split;
     p.partial = splits > 1 ? partial : nullptr;
     p.c_f32 = c_f32 ? 1 : 0;
     const int64_t esz = c_f32 ? 4 : 2;
     p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ld_c * esz) % 16 == 0);
+    p.vec32 = (reinterpret_cast<uintptr_t>(C) % 32 == 0) && ((ld_c * esz) % 32 == 0);
+    p.part_vec32 = (reinterpret_cast<uintptr_t>(partial) % 32 == 0) && (N % 8 == 0);
     p.status = A.status;
     p.skip_stage = L.skip_stage;
     if (splits > 1 && partial == nullptr) return cudaErrorInvalidValue;
     p.n_tiles = static_cast<int>((N + L.tile_n - 1) / L.tile_n);
     p.m_tiles = static_cast<int>((A.R + L.tile_m - 1) / L.tile_m);
+    // row tiles per group: as many as keep the group's A values and m-indices
+    // (read once per column tile) within about a third of the 126 MB L2
+    {
+        const int64_t a_tile = static_cast<int64_t>(L.tile_m) * (values_per_row(A.K, A.M) * 2 + meta_pitch(A.K, A.M));
+        const int64_t budget = int64_t(40) << 20;
+        p.group_m = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.m_tiles, budget / std::max<int64_t>(a_tile, 1))));
+    }
     const int64_t total = static_cast<int64_t>(p.n_tiles) * p.m_tiles * splits;
     if (total > INT32_MAX) return cudaErrorInvalidValue;
     p.total_tiles = static_cast<int>(total);

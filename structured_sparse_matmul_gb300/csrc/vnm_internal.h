@@ -58,25 +58,49 @@ int stream_chunk_blocks(int V);
 cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
                              int64_t ld_c, bool c_f32, cudaStream_t stream);
 
-// Shared-memory pipeline depth of the tensor-core kernel for a tile: as many
-// 128-column stages (B rows, A values, m-indices) as fit next to the staged
-// column-loc words, at most 8.
-// `narrow_b`: B rows loaded by TMA into a tile exactly tile_n wide (tile_n
-// 16 or 32, 32B/64B swizzle) instead of whole 64-column atoms.
-__host__ __device__ constexpr int tc_stages_for(int tile_m, int tile_n, bool narrow_b = false) {
-    const int b_bytes = narrow_b ? 128 * tile_n * 2 : ((tile_n + 63) / 64) * 128 * 128;
-    const int stage = b_bytes + tile_m * 128 + tile_m * 16;
-    const int budget = 227 * 1024 - 2 * 1024;  // minus 1 KB alignment slack and 1 KB for barriers
-    const int s = budget / stage;
-    return s > 8 ? 8 : s;
+// Shared-memory rings of the tensor-core kernel, in stages of 128
+// condensed-K columns (4 MMA k-steps). B: 64-column swizzle atoms of 128
+// rows x 128 bytes, or, for 16- and 32-column tiles loaded by TMA
+// ("narrow"), 128 rows of exactly tile_n columns (32B/64B swizzle); large
+// stages keep many gathered bytes in flight per barrier operation. A (tile_m
+// rows x 128 bytes, 128B swizzle) has its own, shallower ring of at most 32
+// KB (never deeper than B's). The m-indices do not pass through shared
+// memory.
+constexpr int kTcStageK = 128;        // condensed-K columns per stage
+constexpr int kTcARingBytes = 32 * 1024;
+constexpr int kTcMaxStages = 8;
+
+__host__ __device__ constexpr int tc_a_stage_bytes(int tile_m) { return tile_m * 128; }
+
+__host__ __device__ constexpr int tc_b_stage_bytes(int tile_n, bool narrow_b) {
+    return narrow_b ? kTcStageK * tile_n * 2 : ((tile_n + 63) / 64) * kTcStageK * 128;
 }
 
-// B of a tensor-core launch is loaded narrow (see tc_stages_for).
+// Dynamic shared memory a CTA may use: about all of it for wide tiles (one
+// CTA per SM); half for tiles of at most 64 columns, so that two CTAs share
+// an SM (more loads in flight per SM on the small, memory-bound products).
+__host__ __device__ constexpr int tc_smem_budget(int tile_n) {
+    return tile_n <= 64 ? 110 * 1024 : 227 * 1024 - 2 * 1024;  // minus alignment slack and barriers
+}
+
+// B stages of the tensor-core kernel for a tile: as many as fit beside the
+// A ring, at most kTcMaxStages.
+__host__ __device__ constexpr int tc_stages(int tile_m, int tile_n, bool narrow_b) {
+    const int s = (tc_smem_budget(tile_n) - kTcARingBytes) / tc_b_stage_bytes(tile_n, narrow_b);
+    return s > kTcMaxStages ? kTcMaxStages : s;
+}
+
+// A stages: as many as fit in the A ring, never more than the B stages.
+__host__ __device__ constexpr int tc_a_stages(int tile_m, int b_stages) {
+    const int s = kTcARingBytes / tc_a_stage_bytes(tile_m);
+    return s < b_stages ? s : b_stages;
+}
+
+// B of a tensor-core launch is loaded narrow (see tc_b_slot_bytes).
 __host__ __device__ constexpr bool tc_narrow_b(int tile_n, bool gather) { return !gather && tile_n < 64; }
 
 struct TcLaunch {
     CUtensorMap tm_a;   // values, box {64, tile_m}: one stage (4 MMA k-steps), 128B swizzle
-    CUtensorMap tm_e;   // m-indices as u32 words, box {4, tile_m}, no swizzle
     CUtensorMap tm_b;   // B, box {64, 128}, 128B swizzle; {tile_n, 128}, 32B/64B swizzle when narrow
     int tile_m, tile_n, stages, splits;
     bool gather;        // M > 4: rows of B selected through colidx
@@ -92,7 +116,7 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
 cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, void* C,
                                  int64_t ld_c, bool c_f32, cudaStream_t stream);
 
-// Pipeline depth the tensor-core kernel is built with for a tile (0: no such tile).
+// Pipeline stages the tensor-core kernel is built with for a tile (0: no such tile).
 int tc_default_stages(int tile_m, int tile_n, bool gather);
 
 

@@ -87,6 +87,39 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, vo
     return __all_sync(0xFFFFFFFFu, ok);
 }
 
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking test of three barrier phases (the tests are issued back to
+// back, so their latencies overlap).
+__device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2) {
+    const bool r0 = mbar_test_wait(b0, p0);
+    const bool r1 = mbar_test_wait(b1, p1);
+    const bool r2 = mbar_test_wait(b2, p2);
+    return r0 && r1 && r2;
+}
+
+// Bounded wait for three barrier phases at once: the three non-blocking
+// tests are issued back to back (their latencies overlap); only a phase that
+// is not yet complete is then waited for on its own.
+__device__ __forceinline__ bool mbar_wait3(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, uint32_t b2, uint32_t p2,
+                                           volatile int* abort) {
+    const bool r0 = mbar_test_wait(b0, p0);
+    const bool r1 = mbar_test_wait(b1, p1);
+    const bool r2 = mbar_test_wait(b2, p2);
+    if (r0 && r1 && r2) return true;
+    return (r0 || mbar_wait(b0, p0, abort)) && (r1 || mbar_wait(b1, p1, abort)) && (r2 || mbar_wait(b2, p2, abort));
+}
+
 // Same bounded wait, but it ignores the abort flag: used while draining
 // copies and MMAs that were already issued, before the CTA exits.
 __device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
@@ -140,6 +173,14 @@ __device__ __forceinline__ void cluster_sync_all() {
 // (0..16) and zero-fills the rest of the 16 bytes.
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+
+// 32-byte store (8 words) to global memory; the address must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t a4,
+                                             uint32_t a5, uint32_t a6, uint32_t a7) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
+                 "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
                  : "memory");
 }
 

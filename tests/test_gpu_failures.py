@@ -27,7 +27,7 @@ def _product(R, K, N, V, M, seed):
 # stage of its tiles; the last one gives it four tiles (persistent schedule)
 @pytest.mark.parametrize("R,K,N,V,M,skip", [(2048, 2048, 1024, 128, 4, 3),   # B by TMA
                                             (2048, 2048, 1024, 64, 8, 2),    # B gathered
-                                            (4096, 2048, 2048, 64, 8, 9)])   # second tile of four
+                                            (4096, 2048, 2048, 64, 8, 9)])   # second tile of four (8 stages each)
 def test_bounded_wait_reports_timeout_and_device_stays_usable(R, K, N, V, M, skip):
     A, B, comp = _product(R, K, N, V, M, seed=80 + M)
     Bd = torch.from_numpy(B).to(device())
