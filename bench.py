@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--no-context", action="store_true", help="skip the dense torch.matmul context timing")
     ap.add_argument("--e2e-in-streams", type=int, default=1,
                     help="streams that carry a step's host-to-device copies (row chunks of W, then B)")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload kernel table")
+    ap.add_argument("--per-config-launches", type=int, default=10,
+                    help="kernel launches per graph in the per-workload table (median of 7 replays)")
     return ap.parse_args()
 
 
@@ -356,6 +359,120 @@ def config_of(case, l2_note):
     return c
 
 
+# --------------------------------------------------------------------------- per-workload table
+
+def roofline_of(case, peaks, spmm_us, a_bytes):
+    """Roofline of one SpMM launch: the bound (tensor or HBM, by the larger
+    roofline time), the fraction achieved, and the roofline time."""
+    c_bytes = case.R * case.N * (4 if case.c_f32 else 2)
+    byts = a_bytes + 2 * case.K * case.N + c_bytes
+    t_tc = case.effective_flops() / (peaks["bf16_tflops"] * 1e12)
+    t_hbm = byts / (peaks["hbm_gbs"] * 1e9)
+    t_roof = max(t_tc, t_hbm)
+    return {"bound": "tensor" if t_tc >= t_hbm else "hbm", "t_roof_us": t_roof * 1e6,
+            "frac": t_roof / (spmm_us * 1e-6), "bytes": byts, "effective_flops": case.effective_flops()}
+
+
+def measure_per_config(dev, peaks, launches: int):
+    """Every case of workloads 1-5: SpMM and compress launch times (median of
+    7 replays of a graph of `launches` launches over rotating input sets that
+    together exceed twice the L2), the SpMM roofline, the plan, and dense
+    torch.matmul on the same shape (context). Inputs come from torch's seeded
+    device generator with the workloads' distributions (A ~ N(0, 0.02),
+    B ~ N(0, 1)); the kernels' speed does not depend on which generator
+    drew them."""
+    import torch
+
+    from structured_sparse_matmul_gb300 import vnm, workloads
+
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20))
+    cur = torch.cuda.current_stream(dev)
+    gen = torch.Generator(device=dev)
+
+    def time_graph(fn):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(cur)
+        with torch.cuda.stream(side):
+            fn(0, side)  # warm (and the kernels' one-time set-up) outside the capture
+            side.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(launches):
+                    fn(i, side)
+        torch.cuda.synchronize(dev)
+        g.replay()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(7):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(cur)
+            g.replay()
+            e1.record(cur)
+            torch.cuda.synchronize(dev)
+            ts.append(e0.elapsed_time(e1) * 1e3 / launches)
+        return statistics.median(ts)
+
+    table = {}
+    for w in range(1, 6):
+        for case in workloads.workload_cases(w):
+            gen.manual_seed(case.seed)
+            R, K, N, V, M = case.R, case.K, case.N, case.V, case.M
+            c_dtype = torch.float32 if case.c_f32 else torch.float16
+            vb, mb, cb = vnm.vnm_sizes(R, K, V, M)
+            set_bytes = 2 * R * K + vb + mb + cb + 2 * K * N + R * N * (4 if case.c_f32 else 2)
+            n_sets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+            sets = []
+            for _ in range(n_sets):
+                W = (torch.randn(R, K, device=dev, generator=gen) * workloads.A_SIGMA).half()
+                A = vnm.vnm_matrix_alloc(R, K, V, M, dev)
+                Bm = (torch.randn(K, N, device=dev, generator=gen) * workloads.B_SIGMA).half()
+                C = torch.empty(R, N, dtype=c_dtype, device=dev)
+                vnm.vnm_compress(A, W)
+                sets.append({"A": A, "W": W, "B": Bm, "C": C, "ws": vnm.workspace_for(A, N, dev)})
+            torch.cuda.synchronize(dev)
+            plan = vnm.vnm_spmm_plan_query(sets[0]["A"], sets[0]["B"], c_dtype,
+                                           0 if sets[0]["ws"] is None else sets[0]["ws"].numel() * 4)
+
+            def spmm(i, st):
+                x = sets[i % n_sets]
+                vnm.vnm_spmm(x["A"], x["B"], x["C"], workspace=x["ws"], stream=st)
+
+            def comp(i, st):
+                x = sets[i % n_sets]
+                vnm.vnm_compress(x["A"], x["W"], stream=st)
+
+            def dense(i, st):
+                x = sets[i % n_sets]
+                torch.matmul(x["W"], x["B"])
+
+            spmm_us = time_graph(spmm)
+            comp_us = time_graph(comp)
+            try:
+                dense_us = time_graph(dense)
+            except Exception as exc:  # context only
+                dense_us = f"unavailable: {exc}"
+            for x in sets:
+                st_ = vnm.vnm_get_status(x["A"])
+                if st_ != vnm.VNM_OK:
+                    raise RuntimeError(f"kernel status {vnm.status_string(st_)} in {case.name}")
+            roof = roofline_of(case, peaks, spmm_us, vb + mb + cb)
+            comp_bytes = 2 * R * K + vb + mb + cb
+            table[case.name] = {
+                "spmm_us": spmm_us, "compress_us": comp_us,
+                "spmm_effective_tflops": case.effective_flops() / (spmm_us * 1e-6) / 1e12,
+                "spmm_dense_equiv_tflops": case.dense_flops() / (spmm_us * 1e-6) / 1e12,
+                "roofline": {"bound": roof["bound"], "frac": roof["frac"], "t_roof_us": roof["t_roof_us"]},
+                "compress_hbm_frac": comp_bytes / (comp_us * 1e-6) / (peaks["hbm_gbs"] * 1e9),
+                "dense_matmul_us": dense_us, "plan": plan.as_dict(), "sets": n_sets,
+            }
+            del sets
+            torch.cuda.empty_cache()
+    return {"launches_per_graph": launches, "replays": 7, "statistic": "median",
+            "inputs": "torch seeded device generator, A ~ N(0, 0.02), B ~ N(0, 1)",
+            "l2_eviction": "rotating input sets of more than twice the L2 in each graph", "cases": table}
+
+
 # --------------------------------------------------------------------------- main arm
 
 def main():
@@ -507,8 +624,9 @@ def main():
     elapsed_ms = timed(graph)
     dist_barrier(world, dev)
     serial_ms = timed(graph_serial) / steps
-    spmm_ms = timed(graph_spmm) / steps
-    comp_ms = timed(graph_comp) / steps
+    # each kernel's average launch duration: median of 5 replays of its graph
+    spmm_ms = statistics.median(timed(graph_spmm) for _ in range(5)) / steps
+    comp_ms = statistics.median(timed(graph_comp) for _ in range(5)) / steps
     # launch floor: K empty kernels (a sleep of zero cycles), captured and
     # timed the same way
     empty_ms = None
@@ -669,6 +787,10 @@ def main():
     except Exception as exc:  # context only
         ctx["torch_matmul_dense_tflops"] = f"unavailable: {exc}"
 
+    per_config = None
+    if not args.no_per_config:
+        per_config = measure_per_config(dev, peaks, max(2, args.per_config_launches))
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         c = time_oracle(case, args.cpu_seconds)
@@ -692,7 +814,7 @@ def main():
                         "spmm_effective_tflops": eff_flops / (spmm_ms * 1e-3) / 1e12,
                         "compress_gbs": comp_bytes / (comp_ms * 1e-3) / 1e9,
                         "plan": plan.as_dict()},
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks, "per_config": per_config,
             "gpu_launches": steps * kernels_per_step, "context": ctx,
             "gpu": props.name, "sm_count": props.multi_processor_count,
         }
