@@ -23,6 +23,7 @@ this path here) on a bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import math
 import os
@@ -48,6 +49,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["vnm", "reference"], default="vnm")
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--case", type=int, default=0)
+    ap.add_argument("--rows", type=int, default=0,
+                    help="override R of the chosen case (a smaller case of the same kernels, e.g. for ncu)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle timing")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target seconds of oracle work")
@@ -479,6 +482,10 @@ def main():
     args = parse_args()
     from structured_sparse_matmul_gb300 import workloads
     case = workloads.workload_cases(args.workload)[args.case]
+    if args.rows:
+        if args.rows % 128 or args.rows % case.V:
+            raise SystemExit(f"--rows must be a multiple of 128 and of V={case.V}")
+        case = dataclasses.replace(case, R=args.rows)
     if args.impl == "reference":
         world, _, _ = dist_env()
         dist_init(world, "gloo")

@@ -85,10 +85,19 @@ typedef struct vnm_spmm_plan {
     int32_t tile_n;    /* TC: columns of C per CTA tile = MMA N (16, 32, 64, 128, 192 or 256) */
     int32_t stages;    /* TC: depth of the shared-memory pipeline (one depth is built per tile;
                           0 in a plan passed to vnm_spmm_with_plan means that depth) */
-    int32_t splits;    /* split-K factor (1 = none): TC over the condensed K (partials go to the
+    int32_t splits;    /* split-K factor (1 = none): TC over the MMAs' K (partials go to the
                           workspace); SIMT with N <= 8 over the blocks of a row, rounded down to 1, 2,
                           4 or 8 CTAs of one cluster (no workspace) */
-    int32_t reserved[3]; /* must be 0 (vnm_spmm_with_plan rejects anything else with
+    int32_t lift;      /* TC, M == 8 only: 1 = the MMAs run over the whole K, B loaded in tiles
+                          (no gather); each block's two kept values of a row are re-encoded on
+                          chip as 2:4 over the block's 8 columns (a row never keeps more than 2
+                          of a group of 4), zeros filling the free slots: twice the MMA work of
+                          the condensed K, 128-row tiles for any V % 16 == 0, K % 128 == 0.
+                          0 = the default path for M (M == 4: B in tiles; M > 4: the selected
+                          rows of B gathered, V % 64 == 0). Ignored outside the TC path. Any
+                          value but 0 or 1: VNM_ERR_INVALID_ARG; 1 where the shape does not
+                          allow it (or with tile_m != 128): VNM_ERR_UNSUPPORTED. */
+    int32_t reserved[2]; /* must be 0 (vnm_spmm_with_plan rejects anything else with
                             VNM_ERR_INVALID_ARG) */
 } vnm_spmm_plan;
 
@@ -188,7 +197,9 @@ vnm_status vnm_spmm_workspace_size(vnm_matrix A, int64_t N, size_t* bytes);
  * The plan vnm_spmm would use for this product (host only; reads the current
  * device's SM count). B and C alignment decide whether the tensor-core path
  * is allowed: it needs B 16-byte aligned with ld_b % 8 == 0 and N >= 8, and
- * a block geometry it serves (K/M % 32 == 0, and V % 64 == 0 or M == 4);
+ * a block geometry it serves (K/M % 32 == 0, and V % 64 == 0 or M == 4; or
+ * M == 8 with V % 16 == 0 and K % 128 == 0, which it serves with lift = 1
+ * when the gather cannot: a plan may ask for lift = 1 wherever it applies);
  * everything else takes the CUDA-core path (N <= 8: the streaming kernel,
  * which splits K over a cluster of CTAs without a workspace).
  * Errors: VNM_ERR_INVALID_ARG.

@@ -79,6 +79,11 @@ bool tc_geometry_ok(const vnm_matrix_s& A) {
     return A.M == 4 || A.V % 64 == 0;
 }
 
+// The re-encoded path (M == 8 as 2:4 over the whole K) serves any V that
+// is a multiple of 16 (the 16 rows of a half-warp share column-loc words)
+// with K a whole number of 128-column stages; tiles of 128 rows.
+bool lift_ok(const vnm_matrix_s& A) { return A.M == 8 && A.V % 16 == 0 && A.K > 0 && A.K % vnm::kTcStageK == 0; }
+
 bool tc_tile_m_ok(const vnm_matrix_s& A, int tile_m) {
     if (tile_m == 128) return A.M == 4 || A.V % 128 == 0;
     if (tile_m == 64) return A.M == 4 || A.V % 64 == 0;
@@ -123,13 +128,18 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
         pl.path = VNM_PATH_NONE;
         return pl;
     }
-    if (!(tc_geometry_ok(A) && tc_operands_ok(B, ld_b, N))) {
+    if (!((tc_geometry_ok(A) || lift_ok(A)) && tc_operands_ok(B, ld_b, N))) {
         pl.path = VNM_PATH_SIMT;
         pl.splits = static_cast<int32_t>(stream_splits(A, N));
         return pl;
     }
     pl.path = VNM_PATH_TC;
-    pl.tile_m = tc_tile_m_ok(A, 128) ? 128 : 64;
+    // M == 8 where the gather cannot run (V % 64 != 0): the MMAs over the
+    // whole K with A re-encoded on chip. Where both run the gather is kept:
+    // measured as fast or faster (the re-encoded A's shared-memory stores
+    // contend with the MMAs' operand reads)
+    pl.lift = !tc_geometry_ok(A) && lift_ok(A) ? 1 : 0;
+    pl.tile_m = pl.lift || tc_tile_m_ok(A, 128) ? 128 : 64;
     // 256-column tiles for wide B (measured fastest on every shape: the
     // per-stage costs are spread over the most MMA work and the fewest A
     // re-reads); else 128, or N rounded up to a supported width
@@ -137,10 +147,10 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     if (pl.tile_n > 64 && pl.tile_n < 128) pl.tile_n = 128;
     if (pl.tile_n > 32 && pl.tile_n < 64) pl.tile_n = 64;
     if (pl.tile_n > 16 && pl.tile_n < 32) pl.tile_n = 32;
-    pl.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n, A.M > 4);
+    pl.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n, A.M > 4 && !pl.lift);
     // split K when the tiles alone cannot fill the GPU
     const int64_t tiles = ceil_div(A.R, pl.tile_m) * ceil_div(N, pl.tile_n);
-    const int64_t num_kt = (A.K / A.M) / 32;
+    const int64_t num_kt = vnm::tc_k_units(A.K, A.M, pl.lift != 0);
     int64_t splits = 1;
     if (tiles < A.sm_count) splits = std::min<int64_t>(num_kt, std::max<int64_t>(1, A.sm_count / tiles));
     const int64_t per_split = A.R * N * static_cast<int64_t>(sizeof(float));
@@ -151,8 +161,8 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
 }
 
 // The split the kernels will actually use (no empty split).
-int effective_splits(const vnm_matrix_s& A, int requested) {
-    const int num_kt = static_cast<int>((A.K / A.M) / 32);
+int effective_splits(const vnm_matrix_s& A, int requested, bool lift) {
+    const int num_kt = static_cast<int>(vnm::tc_k_units(A.K, A.M, lift));
     const int req = std::max(1, std::min(requested, num_kt));
     const int per = (num_kt + req - 1) / req;
     return (num_kt + per - 1) / per;
@@ -162,14 +172,19 @@ vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void
                       size_t workspace_bytes, const void* workspace) {
     for (int32_t r : pl.reserved)
         if (r != 0) return VNM_ERR_INVALID_ARG;
+    if (pl.lift != 0 && pl.lift != 1) return VNM_ERR_INVALID_ARG;  // read by the TC path only
     if (pl.path == VNM_PATH_SIMT) return pl.splits < 1 ? VNM_ERR_INVALID_ARG : VNM_OK;  // no workspace
     if (pl.path != VNM_PATH_TC) return VNM_ERR_UNSUPPORTED;
-    if (!tc_geometry_ok(A) || !tc_operands_ok(B, ld_b, N)) return VNM_ERR_UNSUPPORTED;
-    if (!tc_tile_m_ok(A, pl.tile_m)) return VNM_ERR_UNSUPPORTED;
-    const int depth = vnm::tc_default_stages(pl.tile_m, pl.tile_n, A.M > 4);
+    if (!tc_operands_ok(B, ld_b, N)) return VNM_ERR_UNSUPPORTED;
+    if (pl.lift) {
+        if (!lift_ok(A) || pl.tile_m != 128) return VNM_ERR_UNSUPPORTED;
+    } else if (!tc_geometry_ok(A) || !tc_tile_m_ok(A, pl.tile_m)) {
+        return VNM_ERR_UNSUPPORTED;
+    }
+    const int depth = vnm::tc_default_stages(pl.tile_m, pl.tile_n, A.M > 4 && !pl.lift);
     if (depth == 0 || (pl.stages != 0 && pl.stages != depth)) return VNM_ERR_UNSUPPORTED;
     if (pl.splits < 1) return VNM_ERR_INVALID_ARG;
-    const int s = effective_splits(A, pl.splits);
+    const int s = effective_splits(A, pl.splits, pl.lift != 0);
     if (s > 1) {
         const size_t need = static_cast<size_t>(s) * A.R * N * sizeof(float);
         if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)) return VNM_ERR_INVALID_ARG;
@@ -192,9 +207,10 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         std::memset(&L, 0, sizeof(L));
         L.tile_m = pl.tile_m;
         L.tile_n = pl.tile_n;
-        L.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n, A->M > 4);
-        L.splits = effective_splits(*A, pl.splits);
-        L.gather = A->M > 4;
+        L.mode = A->M == 4 ? vnm::kTcTiled : pl.lift ? vnm::kTcLift : vnm::kTcGather;
+        const bool gather = L.mode == vnm::kTcGather;
+        L.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n, gather);
+        L.splits = effective_splits(*A, pl.splits, pl.lift != 0);
         L.sm_count = A->sm_count;
         L.skip_stage = skip_stage;
         const uint64_t vpr = static_cast<uint64_t>(values_per_row(A->K, A->M));
@@ -203,10 +219,10 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
                             static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_128B);
         // B tiles by TMA (M == 4): 64-column atoms, or exactly tile_n columns with the
         // matching swizzle for 16- and 32-column tiles
-        const bool narrow = vnm::tc_narrow_b(pl.tile_n, L.gather);
+        const bool narrow = vnm::tc_narrow_b(pl.tile_n, gather);
         ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, A->K, ld_b * 2,
                              narrow ? static_cast<uint32_t>(pl.tile_n) : 64,
-                             L.gather ? 1 : static_cast<uint32_t>(vnm::kTcStageK),
+                             gather ? 1 : static_cast<uint32_t>(vnm::kTcStageK),
                              !narrow ? CU_TENSOR_MAP_SWIZZLE_128B
                                      : pl.tile_n == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
         if (!ok) return VNM_ERR_CUDA;
@@ -342,7 +358,7 @@ vnm_status vnm_spmm_workspace_size(vnm_matrix A, int64_t N, size_t* bytes) {
     vnm_spmm_plan pl = make_plan(*A, aligned_b, ((std::max<int64_t>(N, 1) + 7) / 8) * 8, N, SIZE_MAX / 2);
     *bytes = 0;
     int s = 1;
-    if (pl.path == VNM_PATH_TC) s = effective_splits(*A, pl.splits);
+    if (pl.path == VNM_PATH_TC) s = effective_splits(*A, pl.splits, pl.lift != 0);
     if (s > 1) *bytes = static_cast<size_t>(s) * A->R * N * sizeof(float);
     return VNM_OK;
 }

@@ -9,54 +9,53 @@
 //
 // GB300 design: persistent CTAs (one or two per SM by shared memory and
 // TMEM), each taking tiles b, b + grid, ... of C (tile_m x tile_n over a
-// range of the condensed K; tile_m = 128, or 64 when V = 64 and column-loc
+// range of the MMAs' K; tile_m = 128, or 64 when V = 64 and column-loc
 // differs per 64-row block). Tiles are ordered in groups of group_m row
 // tiles: within a group the row tile varies fastest, so the CTAs running at
 // one time cover many row tiles of one or two column slices of B, reusing
-// each gathered slice of B from L2, and a group's A rows (sized to stay in
-// L2) are reused over all the column slices. Two shared-memory rings feed the MMAs: A values
-// and m-indices in slots of 128 condensed-K columns (4 MMA k-steps), and B
-// in slots of 64 condensed-K rows (2 MMA k-steps). A B slot is free again
-// after two MMAs, so most of the ring is always in flight: the gathered B
-// rows come from L2 with a long latency under load, and the bytes a CTA
-// keeps in flight bound its rate.
-//   warp 0    TMA producer. Per A slot: one tiled load of the A values
-//             (tile_m rows x 64 values, 128B swizzle; MMA k-step s reads
-//             bytes 32s..32s+31 of each row) and one of the m-indices
-//             (tile_m rows x 16 bytes); when M == 4 (column-loc is the
-//             identity) also the two B slots of those columns, as tiled
-//             loads of 64-column x 64-row boxes.
-//   warps 10+ (M > 4) the B gather: each warp owns whole blocks of 4
-//             selected rows per B slot; every lane reads the blocks'
-//             column-loc words (loaded eight slots ahead) and computes its
-//             own source rows, then copies 16-byte chunks with cp.async,
-//             coalesced along each row, straight into the 128B-swizzled
-//             operand layout (zero-filled past N). Each slot's copies are one
-//             cp.async group. Before it waits for the next free slot, a warp
-//             waits for the group it issued B_SLOTS-1 slots earlier
-//             (cp.async.wait_group), fences those generic-proxy writes into
-//             the async proxy, and one lane arrives on that slot's barrier:
-//             one arrival per warp and slot, all but one slot of the ring in
-//             flight, and the MMAs never wait on a slot whose copies landed.
-//   warps 2-5 per A slot, as soon as A and the m-indices landed: read their
-//             rows' m-index words from shared memory, pair them the way the
-//             sparse MMA reads them (rows i and i+8 of each 16-row group
-//             share their 16-bit halves between TMEM lanes i and i+8) and
-//             write them to TMEM (tcgen05.st), each MMA's word in its own
-//             8-column-aligned slot.
-//   warp 1    TMEM owner and MMA issuer (one thread): 2 sparse MMAs of
-//             M=tile_m, N=tile_n, K=32 per B slot into an fp32 accumulator
-//             in TMEM; tcgen05.commit frees each B slot, each A slot, and
-//             hands the tile's accumulator to the epilogue. Two accumulators
-//             alternate between tiles when TMEM holds them (tile_n <= 208).
+// each slice of B from L2, and a group's A rows (sized to stay in L2) are
+// reused over all the column slices. A stage is 128 columns of the MMAs' K
+// (4 MMA k-steps): a B ring of stages (the 128 rows of B the stage needs,
+// tile_n wide) and a shallower A ring (tile_m rows x 64 stored values,
+// 128B swizzle) feed the MMAs; the m-indices go to TMEM. Three ways to form
+// the operands (TcMode):
+//   kTcTiled  (M == 4): A values by TMA, B in TMA tiles.
+//   kTcGather (M > 4): A values by TMA; the MMAs run over the condensed K,
+//             B's 4 selected rows of every block copied in by gather warps.
+//   kTcLift   (M == 8): the MMAs run over the whole K, B in TMA tiles; a
+//             row keeps 2 values of 8 columns, never more than 2 of a group
+//             of 4, so warps re-encode each block as 2:4 over its columns
+//             and write A to shared memory themselves.
+// Warp roles:
+//   warp 0    A producer: one tiled TMA load per A stage (idle for kTcLift).
+//   warp 1    TMEM owner and MMA issuer (one thread): per stage one
+//             combined wait, 4 sparse MMAs of M = tile_m, N = tile_n, K = 32
+//             into an fp32 accumulator in TMEM, and one commit that frees
+//             the stage's B slot, A slot and m-index slot; a commit per tile
+//             hands the accumulator to the epilogue. Two accumulators
+//             alternate when TMEM holds them beside the m-index slots.
+//   warps 2-5 m-index warps, one lane per row: each loads its row's four
+//             m-index words of a stage from global memory a few stages
+//             ahead, pairs them the way the sparse MMA reads them (rows i
+//             and i+8 of each 16-row group share 16-bit halves between TMEM
+//             lanes i and i+8) and writes them to the stage's TMEM slot (each
+//             MMA's word 8-column aligned). With kTcLift they, and two more
+//             groups of four warps (11+), re-encode A instead (see there).
 //   warps 6-9 epilogue: TMEM -> registers (tcgen05.ld) -> fp16 (RNE) or
 //             fp32 -> global, each thread writing whole 32-byte sectors of
-//             its row (fp32 partials to the workspace under split-K), while
-//             the other warps already run the next tile; then they release
-//             the accumulator (with a single accumulator and 64-row tiles
-//             the m-index warps drain half of its columns). With M=128 row r
-//             of the tile lives in TMEM lane r; with M=64 in lane
-//             32*(r/16) + r%16 (lanes 16..31 of each quarter stay unused).
+//             its row (fp32 partials to the workspace under split-K); with
+//             M = 128 row r of the tile lives in TMEM lane r, with M = 64 in
+//             lane 32*(r/16) + r%16 (lanes 16..31 of each quarter unused).
+//   warp 10   B producer (kTcTiled, kTcLift): TMA tiles of 64 columns x 128
+//             rows, or one tile_n-wide box for 16- and 32-column tiles.
+//   warps 11+ (kTcGather) the B gather: each warp owns whole blocks of 4
+//             selected rows of every stage; every lane reads the blocks'
+//             column-loc words (loaded a few stages ahead) and copies
+//             16-byte chunks with cp.async, coalesced along each row,
+//             straight into the 128B-swizzled operand layout (zero-filled
+//             past N); each thread's copies arrive on the stage's barrier
+//             (cp.async.mbarrier.arrive.noinc) and the MMA thread fences the
+//             generic-proxy writes into the async proxy after its wait.
 // Every mbarrier wait is bounded: on time-out the CTA records
 // VNM_ERR_TIMEOUT, drains what it already issued, frees TMEM and returns.
 #include <cuda_fp16.h>
@@ -93,6 +92,8 @@ __host__ __device__ constexpr int meta_prefetch(bool split_epilogue) { return sp
 
 struct TcArgs {
     const uint32_t* colidx;  // [R/V][nblk] words of 4 column bytes
+    const uint32_t* values;  // [R][vpr_words] words of 2 values, read by the re-encoding warps (kTcLift)
+    int64_t vpr_words;
     const uint16_t* B;       // K x N fp16 (ld_b), read by the gather warps
     const uint8_t* meta;     // [R][mpitch] m-indices, read by the m-index warps
     int64_t mpitch;
@@ -103,7 +104,7 @@ struct TcArgs {
     int64_t R, N;
     int V, M;
     int64_t nblk;
-    int num_kt;              // condensed K / kTcStageK: B stages of a whole row
+    int num_kt;              // MMA K / kTcStageK: B stages of a whole row
     int kt_per_split;        // B stages per K split
     int n_tiles, m_tiles;    // tile grid (see tile_geom for the order)
     int group_m;             // row tiles per group of the tile order
@@ -127,18 +128,23 @@ __host__ __device__ constexpr int pow2_at_least(int x) {
 // (two CTAs per SM).
 __host__ __device__ constexpr int gather_warps(int bn) { return bn <= 64 ? 8 : 16; }
 
-template <int TM, int BN, bool GATHER>
+// Groups of 4 warps that re-encode A (kTcLift), each taking every
+// kLiftGroups-th stage (at most the B stages: see the lift warps' waits).
+constexpr int kLiftGroups = 3;
+
+template <int TM, int BN, int MODE>
 __host__ __device__ constexpr int tc_threads() {
-    return kTcWarpsFixed * 32 + (GATHER ? 32 * gather_warps(BN) : 0);
+    return kTcWarpsFixed * 32 +
+           (MODE == kTcGather ? 32 * gather_warps(BN) : MODE == kTcLift ? 32 * 4 * (kLiftGroups - 1) : 0);
 }
 
 // B stages ahead of their use at which a gather warp loads their column-loc
 // words (8 words per warp in flight)
 __host__ __device__ constexpr int col_prefetch(int blocks_per_warp) { return 8 / blocks_per_warp; }
 
-template <int TM, int BN, bool GATHER>
+template <int TM, int BN, int MODE>
 struct TcCfg {
-    static constexpr bool kNarrow = tc_narrow_b(BN, GATHER);
+    static constexpr bool kNarrow = tc_narrow_b(BN, MODE == kTcGather);
     static constexpr int kAtoms = (BN + 63) / 64;      // 64-column swizzle atoms of B
     static constexpr int kABytes = tc_a_stage_bytes(TM);
     static constexpr int kBBytes = tc_b_stage_bytes(BN, kNarrow);
@@ -149,12 +155,15 @@ struct TcCfg {
     static constexpr int kAccBufs = 2 * BN + kStages * kMetaStageCols <= 512 ? 2 : 1;
     static constexpr int kTmemCols = pow2_at_least(kAccBufs * BN + kStages * kMetaStageCols);
     static constexpr int kSmemBytes = kStages * kBBytes + kAStages * kABytes + 1024;  // + alignment
-    static constexpr int kMinBlocks = BN <= 64 ? 2 : 1;
+    static constexpr int kMinBlocks = BN <= 64 && MODE != kTcLift ? 2 : 1;
     static_assert(kStages >= 2, "pipeline depth");
     static_assert(kAStages >= 2 && kAStages <= kStages, "A ring depth");
     static_assert(BN + kStages * kMetaStageCols <= 512, "TMEM budget");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N");
     static_assert(TM == 64 || TM == 128, "MMA M");
+    // a lift group waits on b_empty of stage it - AS having last waited on stage
+    // it - kLiftGroups - AS: the barrier cannot be two phases behind
+    static_assert(MODE != kTcLift || kLiftGroups <= kStages, "lift groups");
     static_assert(kBBytes % 1024 == 0 || kNarrow, "B stages keep the 1024-byte swizzle alignment");
 };
 
@@ -163,6 +172,54 @@ template <int TM>
 __device__ __forceinline__ int tile_row_of_lane(int q, int l) {
     if (TM == 128) return 32 * q + l;
     return l < 16 ? 16 * q + l : -1;
+}
+
+// Write a row's four m-index words of a stage (one per MMA k-step) to the
+// stage's TMEM slot `te` in this warp's lane quarter (`lane_addr`), paired
+// the way the sparse MMA reads them: rows i and i+8 of each 16-row group
+// share 16-bit halves, TMEM lane i taking both rows' low halves and lane i+8
+// both rows' high halves. Each lane sends its partner the four halves the
+// partner needs, packed in two words. Whole warp.
+__device__ __forceinline__ void store_meta_words(uint32_t te, uint32_t lane_addr, int lane, const uint32_t (&own)[4]) {
+    const bool hi = (lane & 8) != 0;
+    const uint32_t send01 = hi ? ((own[0] & 0xFFFFu) | (own[1] << 16)) : ((own[0] >> 16) | (own[1] & 0xFFFF0000u));
+    const uint32_t send23 = hi ? ((own[2] & 0xFFFFu) | (own[3] << 16)) : ((own[2] >> 16) | (own[3] & 0xFFFF0000u));
+    const uint32_t got01 = __shfl_xor_sync(0xFFFFFFFFu, send01, 8);
+    const uint32_t got23 = __shfl_xor_sync(0xFFFFFFFFu, send23, 8);
+    const uint32_t got[4] = {got01 & 0xFFFFu, got01 >> 16, got23 & 0xFFFFu, got23 >> 16};
+#pragma unroll
+    for (int s = 0; s < kKSteps; ++s) {
+        // low lane: [own low | partner low]; high lane: [partner high | own high]
+        const uint32_t word = hi ? (got[s] | (own[s] & 0xFFFF0000u)) : ((own[s] & 0xFFFFu) | (got[s] << 16));
+        tmem_st_32x32b_x1(te + s * kMetaSlotCols + lane_addr, word);
+    }
+}
+
+// 2:4 form of one block of 8 columns (kTcLift) that keeps columns d0 < d1,
+// for the block's values word u (value of column d0 in the low half, of d1
+// in the high half): .x holds two byte-permute selectors, applied to
+// (u, 0), that give the 2-value words of the block's two groups of 4
+// columns (low 16 bits: columns 0-3; high: columns 4-7); .y the two groups'
+// 4-bit slot codes (lower slot in the low 2 bits; columns 0-3 in the low
+// nibble). A group that holds one kept column pairs it with a zero in slot
+// 0, or in slot 1 when the kept column is column 0 of the group; a group
+// that holds none takes zeros in slots 0 and 1. A pair with d0 >= d1 (which
+// vnm_compress never writes) gives zeros.
+__host__ __device__ constexpr uint2 lift_entry(uint32_t d0, uint32_t d1) {
+    constexpr uint32_t kBoth = 0x3210u;     // (u.lo, u.hi)
+    constexpr uint32_t kNone = 0x4444u;     // (0, 0)
+    constexpr uint32_t kLoZero = 0x4410u;   // (u.lo, 0)
+    constexpr uint32_t kZeroLo = 0x1044u;   // (0, u.lo)
+    constexpr uint32_t kHiZero = 0x4432u;   // (u.hi, 0)
+    constexpr uint32_t kZeroHi = 0x3244u;   // (0, u.hi)
+    constexpr uint32_t kPad = 0x4u;         // slots 0 and 1
+    if (d0 >= d1 || d1 > 7) return uint2{kNone | (kNone << 16), kPad | (kPad << 4)};
+    if (d1 < 4) return uint2{kBoth | (kNone << 16), (d0 | (d1 << 2)) | (kPad << 4)};
+    if (d0 >= 4) return uint2{kNone | (kBoth << 16), kPad | (((d0 - 4) | ((d1 - 4) << 2)) << 4)};
+    const uint32_t e = d1 - 4;
+    const uint32_t sel0 = d0 == 0 ? kLoZero : kZeroLo, code0 = d0 == 0 ? kPad : (d0 << 2);
+    const uint32_t sel1 = e == 0 ? kHiZero : kZeroHi, code1 = e == 0 ? kPad : (e << 2);
+    return uint2{sel0 | (sel1 << 16), code0 | (code1 << 4)};
 }
 
 struct TileGeom {
@@ -287,11 +344,13 @@ __device__ __forceinline__ void stage_next(const TcArgs& p, StageIt& x) {
 }
 
 // Persistent: CTA b takes tiles b, b + gridDim.x, ...
-template <int TM, int BN, bool GATHER>
-__global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GATHER>::kMinBlocks)
+template <int TM, int BN, int MODE>
+__global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE>::kMinBlocks)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const TcArgs p) {
-    using Cfg = TcCfg<TM, BN, GATHER>;
+    constexpr bool GATHER = MODE == kTcGather;
+    constexpr bool LIFT = MODE == kTcLift;
+    using Cfg = TcCfg<TM, BN, MODE>;
     constexpr int ST = Cfg::kStages;
     constexpr int AS = Cfg::kAStages;
     constexpr int ACC = Cfg::kAccBufs;
@@ -312,6 +371,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
     __shared__ __align__(8) uint64_t done_bar;      // every MMA of this CTA complete
     __shared__ uint32_t tmem_slot;
     __shared__ int abort_flag;
+    __shared__ uint2 lift_tab[LIFT ? 64 : 1];       // lift_entry(d0, d1) at 8 * d0 + d1
 
     // B stages first: a B descriptor read stays inside this CTA's allocation
     // even if its two strides were interpreted the other way round.
@@ -337,9 +397,10 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
         fence_barrier_init();
     }
     if (threadIdx.x == 32) {
-        tma_prefetch_desc(&tm_a);
+        if (!LIFT) tma_prefetch_desc(&tm_a);
         tma_prefetch_desc(&tm_b);
     }
+    if (LIFT && threadIdx.x < 64) lift_tab[threadIdx.x] = lift_entry(threadIdx.x >> 3, threadIdx.x & 7u);
     if (warp == 1) {
         tmem_alloc(smem_u32(&tmem_slot), Cfg::kTmemCols);
         tmem_relinquish();
@@ -352,7 +413,10 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
     volatile int* abort = &abort_flag;
 
     if (warp == 0) {
-        // ------------------------------------------------ A producer (TMA)
+        // ------------------------------------------------ A producer (TMA; none when A is re-encoded)
+        if (LIFT) {
+            // idle
+        } else {
         int last_it[AS];
 #pragma unroll
         for (int s = 0; s < AS; ++s) last_it[s] = -1;
@@ -385,8 +449,9 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
             for (int s = 0; s < AS; ++s)
                 if (last_it[s] >= 0) mbar_drain(smem_u32(&a_full[s]), static_cast<uint32_t>(last_it[s] / AS) & 1u);
         }
+        }
     } else if (warp == kBProducerWarp) {
-        // ------------------------------------------------ B producer (TMA, M == 4)
+        // ------------------------------------------------ B producer (TMA tiles: kTcTiled, kTcLift)
         if (!GATHER) {
             int last_it[ST];
 #pragma unroll
@@ -459,12 +524,16 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
                     const int slot = it % ST;
                     const int aslot = it % AS;
                     const uint32_t ph = static_cast<uint32_t>(it / ST) & 1u;
-                    if (!ready && !mbar_wait3(smem_u32(&meta_bar[slot]), ph, smem_u32(&b_full[slot]), ph,
-                                              smem_u32(&a_full[aslot]), static_cast<uint32_t>(it / AS) & 1u, abort)) {
+                    // (re-encoded A is written together with the m-indices: one barrier)
+                    if (!ready && !(LIFT ? mbar_wait2(smem_u32(&meta_bar[slot]), ph, smem_u32(&b_full[slot]), ph, abort)
+                                         : mbar_wait3(smem_u32(&meta_bar[slot]), ph, smem_u32(&b_full[slot]), ph,
+                                                      smem_u32(&a_full[aslot]), static_cast<uint32_t>(it / AS) & 1u,
+                                                      abort))) {
                         run = false;
                         break;
                     }
-                    if (GATHER) fence_proxy_async_smem();  // gathered B rows were written by cp.async
+                    // gathered B rows (cp.async) and re-encoded A (st.shared) came through the generic proxy
+                    if (GATHER || LIFT) fence_proxy_async_smem();
                     tc_fence_after_sync();
                     const uint64_t ad = adesc0 + ((aslot * Cfg::kABytes) >> 4);
                     const uint64_t bd = bdesc0 + ((slot * Cfg::kBBytes) >> 4);
@@ -478,8 +547,10 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
                             const int nx = it + 1;
                             const uint32_t nph = static_cast<uint32_t>(nx / ST) & 1u;
                             ready = k + 1 < g.nkt &&
-                                    mbar_test3(smem_u32(&meta_bar[nx % ST]), nph, smem_u32(&b_full[nx % ST]), nph,
-                                               smem_u32(&a_full[nx % AS]), static_cast<uint32_t>(nx / AS) & 1u);
+                                    (LIFT ? mbar_test2(smem_u32(&meta_bar[nx % ST]), nph, smem_u32(&b_full[nx % ST]), nph)
+                                          : mbar_test3(smem_u32(&meta_bar[nx % ST]), nph, smem_u32(&b_full[nx % ST]),
+                                                       nph, smem_u32(&a_full[nx % AS]),
+                                                       static_cast<uint32_t>(nx / AS) & 1u));
                         }
                     }
                     tc_commit(smem_u32(&b_empty[slot]));
@@ -491,6 +562,106 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
             mbar_drain(smem_u32(&done_bar), 0);
         }
         __syncwarp();
+    } else if (LIFT && (warp < kEpiWarp0 || warp >= kTcWarpsFixed)) {
+        // ------------------------------------------------ A re-encoded as 2:4 (kTcLift)
+        // kLiftGroups groups of 4 warps (warps 2-5, then 11-14, 15-18, ...);
+        // group g prepares the stages it with it % kLiftGroups == g, each
+        // lane one row of the tile, so that every warp has kLiftGroups
+        // stage-times for the re-encoding and for its loads to land. A stage
+        // is 16 blocks of 8 columns: the lane loads the row's 32 values of
+        // the stage (16 words), its 64 bits of m-indices and one column-loc
+        // word of its V-block (lane l: block l % 16; the 16 rows of a
+        // half-warp lie in one V-block); re-encodes every block as 2:4 over
+        // the block's 8 columns (lift_entry); issues the loads of its next
+        // stage; and, once the stage's A slot and TMEM slot are free, writes
+        // the row's 64 values into the A slot in the layout a 128B-swizzled
+        // TMA box would have, and its four m-index words to TMEM.
+        const int grp = warp < kEpiWarp0 ? 0 : 1 + (warp - kTcWarpsFixed) / 4;
+        const int q = warp & 3;
+        const int trow = tile_row_of_lane<TM>(q, lane);
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+        struct Raw {
+            uint4 v[4];   // the row's 32 values of the stage
+            uint2 m;      // their 2-bit slots (block b at bits 4b)
+            uint32_t c;   // column-loc word of block lane % 16 of the stage
+        };
+        int col_t = -1;         // tile whose column-loc row base is cached
+        int64_t col_base = 0;   // first column-loc word of this lane's V-block row
+        auto load_raw = [&](const StageIt& x, Raw& r) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) r.v[j] = make_uint4(0u, 0u, 0u, 0u);
+            r.m = make_uint2(0u, 0u);  // rows past R: slots (0, 0) in every block encode zeros
+            r.c = 0u;
+            if (!x.valid || trow < 0) return;
+            const int64_t row = x.g.m0 + trow;
+            if (row >= p.R) return;
+            if (x.t != col_t) {
+                col_t = x.t;
+                col_base = (row / p.V) * p.nblk;
+            }
+            const int kt = x.g.kt0 + x.k;
+            const uint4* vs = reinterpret_cast<const uint4*>(p.values + row * p.vpr_words) + 4 * kt;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) r.v[j] = __ldg(vs + j);
+            r.m = __ldg(reinterpret_cast<const uint2*>(p.meta + row * p.mpitch) + kt);
+            r.c = __ldg(p.colidx + col_base + 16 * static_cast<int64_t>(kt) + (lane & 15));
+        };
+        auto advance = [&](StageIt& x, int n) {
+            for (int i = 0; i < n && x.valid; ++i) stage_next<TM, BN>(p, x);
+        };
+        StageIt cur;
+        stage_start<TM, BN>(p, cur);
+        advance(cur, grp);
+        StageIt ahead = cur;
+        advance(ahead, kLiftGroups);
+        Raw r;
+        load_raw(cur, r);
+        int it = grp;
+        while (cur.valid) {
+            uint32_t aw[32];  // the row's 64 values of the stage, 2 per word
+            uint32_t mw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int b = 0; b < 16; ++b) {
+                const uint32_t cw = __shfl_sync(0xFFFFFFFFu, r.c, (lane & 16) | b);
+                const uint4& v4 = r.v[b >> 2];
+                const uint32_t u = (b & 3) == 0 ? v4.x : (b & 3) == 1 ? v4.y : (b & 3) == 2 ? v4.z : v4.w;
+                const uint32_t nib = ((b < 8 ? r.m.x : r.m.y) >> (4 * (b & 7))) & 15u;
+                const uint32_t d0 = (cw >> ((nib & 3u) << 3)) & 7u;
+                const uint32_t d1 = (cw >> ((nib >> 2) << 3)) & 7u;
+                const uint2 e = lift_tab[8 * d0 + d1];
+                aw[2 * b] = __byte_perm(u, 0u, e.x);
+                aw[2 * b + 1] = __byte_perm(u, 0u, e.x >> 16);
+                mw[b >> 2] |= e.y << (8 * (b & 3));
+            }
+            // the next stage's loads only now: a wait for this stage's words never covers them
+            asm volatile("" ::: "memory");
+            load_raw(ahead, r);
+            advance(ahead, kLiftGroups);
+            const int slot = it % ST;
+            const int aslot = it % AS;
+            // A slot aslot was last read by stage it - AS, TMEM slot `slot` by stage
+            // it - ST <= it - AS: both free once the MMAs of stage it - AS are done
+            if (it >= AS && !mbar_wait_warp(smem_u32(&b_empty[(it - AS) % ST]),
+                                            static_cast<uint32_t>((it - AS) / ST) & 1u, abort, kSleepMeta))
+                break;
+            tc_fence_after_sync();
+            if (trow >= 0) {
+                // 128B swizzle: 16-byte chunk c of row trow at chunk c ^ (trow % 8)
+                const uint32_t rowa = sA0 + aslot * Cfg::kABytes + static_cast<uint32_t>(trow) * 128u;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    st_shared_v4(rowa + ((static_cast<uint32_t>(c) ^ (trow & 7u)) << 4), aw[4 * c], aw[4 * c + 1],
+                                 aw[4 * c + 2], aw[4 * c + 3]);
+            }
+            fence_proxy_async_smem();  // these generic-proxy writes are read by the MMAs
+            store_meta_words(tmem_e + slot * kMetaStageCols, lane_addr, lane, mw);
+            tmem_wait_st();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&meta_bar[slot]));
+            it += kLiftGroups;
+            advance(cur, kLiftGroups);
+        }
     } else if (warp < kEpiWarp0) {
         // ------------------------------------------------ m-indices -> TMEM (warps 2-5)
         // Each lane owns one row of the tile: it loads that row's m-index
@@ -536,8 +707,6 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
 #pragma unroll
             for (int d = 0; d < kMetaPrefetch; ++d) {
                 const uint4 w = ring[d];  // loaded kMetaPrefetch stages ago
-                ring[d] = load_meta(ahead);
-                if (ahead.valid) stage_next<TM, BN>(p, ahead);
                 if (cur.t != last_t) {
                     // a new tile: with the split epilogue, drain the previous one's upper half first
                     if (kSplitEpi && !drain_upper(prev, ti)) {
@@ -556,22 +725,13 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
                     break;
                 }
                 tc_fence_after_sync();
-                // lane i (i % 16 < 8) pairs its low halves with lane i+8's low halves, lane i+8
-                // its high halves with lane i's: each lane sends the four halves its partner
-                // needs, packed in two words
-                const bool hi = (lane & 8) != 0;
-                const uint32_t send01 = hi ? ((w.x & 0xFFFFu) | (w.y << 16)) : ((w.x >> 16) | (w.y & 0xFFFF0000u));
-                const uint32_t send23 = hi ? ((w.z & 0xFFFFu) | (w.w << 16)) : ((w.z >> 16) | (w.w & 0xFFFF0000u));
-                const uint32_t got01 = __shfl_xor_sync(0xFFFFFFFFu, send01, 8);
-                const uint32_t got23 = __shfl_xor_sync(0xFFFFFFFFu, send23, 8);
                 const uint32_t own[4] = {w.x, w.y, w.z, w.w};
-                const uint32_t got[4] = {got01 & 0xFFFFu, got01 >> 16, got23 & 0xFFFFu, got23 >> 16};
-#pragma unroll
-                for (int s = 0; s < kKSteps; ++s) {
-                    // low lane: [own low | partner low]; high lane: [partner high | own high]
-                    const uint32_t word = hi ? (got[s] | (own[s] & 0xFFFF0000u)) : ((own[s] & 0xFFFFu) | (got[s] << 16));
-                    tmem_st_32x32b_x1(tmem_e + slot * kMetaStageCols + s * kMetaSlotCols + lane_addr, word);
-                }
+                store_meta_words(tmem_e + slot * kMetaStageCols, lane_addr, lane, own);
+                // the ring slot is reused only after its words were used: a wait for them then
+                // never covers the load issued for a later stage
+                asm volatile("" ::: "memory");
+                ring[d] = load_meta(ahead);
+                if (ahead.valid) stage_next<TM, BN>(p, ahead);
                 tmem_wait_st();
                 tc_fence_before_sync();
                 __syncwarp();
@@ -637,12 +797,17 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
         }
         const int64_t ldb_bytes = p.ld_b * 2;
         // column-loc words of this warp's blocks of a stage (every lane loads the same words)
+        int col_t = -1;        // tile whose column-loc row base is cached
+        int64_t col_base = 0;  // its first column-loc word
         auto load_words = [&](const StageIt& x, uint32_t (&w)[BPW]) {
 #pragma unroll
             for (int j = 0; j < BPW; ++j) w[j] = 0u;
             if (!x.valid) return;
-            const uint32_t* src =
-                p.colidx + (x.g.m0 / p.V) * p.nblk + static_cast<int64_t>(x.g.kt0 + x.k) * kBlocks + gw * BPW;
+            if (x.t != col_t) {
+                col_t = x.t;
+                col_base = (x.g.m0 / p.V) * p.nblk;
+            }
+            const uint32_t* src = p.colidx + col_base + static_cast<int64_t>(x.g.kt0 + x.k) * kBlocks + gw * BPW;
 #pragma unroll
             for (int j = 0; j < BPW; ++j) w[j] = __ldg(src + j);
         };
@@ -664,11 +829,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
         while (!stop) {
 #pragma unroll
             for (int d = 0; d < kColPrefetch; ++d) {
-                uint32_t words[BPW];
-#pragma unroll
-                for (int j = 0; j < BPW; ++j) words[j] = ring[d][j];  // loaded kColPrefetch stages ago
-                load_words(ahead, ring[d]);
-                if (ahead.valid) stage_next<TM, BN>(p, ahead);
+                const uint32_t (&words)[BPW] = ring[d];  // loaded kColPrefetch stages ago
 
                 const int slot = it % ST;
                 const uint32_t ph = static_cast<uint32_t>(it / ST) & 1u;
@@ -705,6 +866,10 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
                     }
                     cp_async_arrive_noinc(smem_u32(&b_full[slot]));
                 }
+                // the ring slot is reused only after its words were used (see the m-index warps)
+                asm volatile("" ::: "memory");
+                load_words(ahead, ring[d]);
+                if (ahead.valid) stage_next<TM, BN>(p, ahead);
                 ++it;
                 stage_next<TM, BN>(p, cur);
                 if (!cur.valid) {
@@ -731,11 +896,11 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, GATHER>(), TcCfg<TM, BN, GA
 // of the instance on each device.
 constexpr int kMaxDevices = 64;
 
-template <int TM, int BN, bool GATHER>
+template <int TM, int BN, int MODE>
 cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stream) {
-    using Cfg = TcCfg<TM, BN, GATHER>;
-    auto kern = spmm_tc_kernel<TM, BN, GATHER>;
-    constexpr int threads = tc_threads<TM, BN, GATHER>();
+    using Cfg = TcCfg<TM, BN, MODE>;
+    auto kern = spmm_tc_kernel<TM, BN, MODE>;
+    constexpr int threads = tc_threads<TM, BN, MODE>();
     static std::atomic<int> per_sm_cache[kMaxDevices];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -757,15 +922,15 @@ cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stre
     return cudaGetLastError();
 }
 
-template <int TM, bool GATHER>
+template <int TM, int MODE>
 cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, cudaStream_t stream) {
     switch (L.tile_n) {
-        case 16: return launch_variant<TM, 16, GATHER>(L, p, stream);
-        case 32: return launch_variant<TM, 32, GATHER>(L, p, stream);
-        case 64: return launch_variant<TM, 64, GATHER>(L, p, stream);
-        case 128: return launch_variant<TM, 128, GATHER>(L, p, stream);
-        case 192: return launch_variant<TM, 192, GATHER>(L, p, stream);
-        case 256: return launch_variant<TM, 256, GATHER>(L, p, stream);
+        case 16: return launch_variant<TM, 16, MODE>(L, p, stream);
+        case 32: return launch_variant<TM, 32, MODE>(L, p, stream);
+        case 64: return launch_variant<TM, 64, MODE>(L, p, stream);
+        case 128: return launch_variant<TM, 128, MODE>(L, p, stream);
+        case 192: return launch_variant<TM, 192, MODE>(L, p, stream);
+        case 256: return launch_variant<TM, 256, MODE>(L, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -780,11 +945,16 @@ int tc_default_stages(int tile_m, int tile_n, bool gather) {
 
 cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void* B, int64_t ld_b, int64_t N, void* C,
                            int64_t ld_c, bool c_f32, float* partial, cudaStream_t stream) {
-    if (tc_default_stages(L.tile_m, L.tile_n, L.gather) == 0 ||
-        L.stages != tc_default_stages(L.tile_m, L.tile_n, L.gather))
+    const bool gather = L.mode == kTcGather;
+    const bool lift = L.mode == kTcLift;
+    if (L.mode != kTcTiled && L.mode != kTcGather && L.mode != kTcLift) return cudaErrorInvalidValue;
+    if (lift && (A.M != 8 || L.tile_m != 128)) return cudaErrorInvalidValue;
+    if (tc_default_stages(L.tile_m, L.tile_n, gather) == 0 || L.stages != tc_default_stages(L.tile_m, L.tile_n, gather))
         return cudaErrorInvalidValue;
     TcArgs p;
     p.colidx = static_cast<const uint32_t*>(A.colidx);
+    p.values = static_cast<const uint32_t*>(A.values);
+    p.vpr_words = values_per_row(A.K, A.M) / 2;
     p.B = static_cast<const uint16_t*>(B);
     p.ld_b = ld_b;
     p.C = C;
@@ -796,10 +966,10 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
     p.nblk = A.K / A.M;
     p.meta = static_cast<const uint8_t*>(A.meta);
     p.mpitch = meta_pitch(A.K, A.M);
-    // K splits are whole 128-column units of the condensed K (the host sizes
-    // the workspace by the same rule), one B stage each
+    // K splits are whole 128-column units of the MMAs' K (the host sizes the
+    // workspace by the same rule), one B stage each
     static_assert(kTcStageK == 128, "one B stage per 128-column unit");
-    const int units = static_cast<int>(p.nblk / 32);
+    const int units = static_cast<int>(tc_k_units(A.K, A.M, lift));
     const int splits_req = max(1, min(L.splits, units));
     const int units_per_split = (units + splits_req - 1) / splits_req;
     const int splits = (units + units_per_split - 1) / units_per_split;
@@ -827,10 +997,12 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
     if (total > INT32_MAX) return cudaErrorInvalidValue;
     p.total_tiles = static_cast<int>(total);
     cudaError_t e;
-    if (L.tile_m == 128)
-        e = L.gather ? dispatch_bn<128, true>(L, p, stream) : dispatch_bn<128, false>(L, p, stream);
+    if (lift)
+        e = dispatch_bn<128, kTcLift>(L, p, stream);
+    else if (L.tile_m == 128)
+        e = gather ? dispatch_bn<128, kTcGather>(L, p, stream) : dispatch_bn<128, kTcTiled>(L, p, stream);
     else
-        e = L.gather ? dispatch_bn<64, true>(L, p, stream) : dispatch_bn<64, false>(L, p, stream);
+        e = gather ? dispatch_bn<64, kTcGather>(L, p, stream) : dispatch_bn<64, kTcTiled>(L, p, stream);
     if (e != cudaSuccess) return e;
     if (splits > 1) return launch_splitk_reduce(partial, splits, A.R, N, C, ld_c, c_f32, stream);
     return cudaSuccess;

@@ -58,15 +58,14 @@ int stream_chunk_blocks(int V);
 cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
                              int64_t ld_c, bool c_f32, cudaStream_t stream);
 
-// Shared-memory rings of the tensor-core kernel, in stages of 128
-// condensed-K columns (4 MMA k-steps). B: 64-column swizzle atoms of 128
-// rows x 128 bytes, or, for 16- and 32-column tiles loaded by TMA
-// ("narrow"), 128 rows of exactly tile_n columns (32B/64B swizzle); large
-// stages keep many gathered bytes in flight per barrier operation. A (tile_m
-// rows x 128 bytes, 128B swizzle) has its own, shallower ring of at most 32
-// KB (never deeper than B's). The m-indices do not pass through shared
-// memory.
-constexpr int kTcStageK = 128;        // condensed-K columns per stage
+// Shared-memory rings of the tensor-core kernel, in stages of 128 columns
+// of the MMAs' K (4 MMA k-steps). B: 64-column swizzle atoms of 128 rows x
+// 128 bytes, or, for 16- and 32-column tiles loaded by TMA ("narrow"), 128
+// rows of exactly tile_n columns (32B/64B swizzle); large stages keep many
+// gathered bytes in flight per barrier operation. A (tile_m rows x 128
+// bytes, 128B swizzle) has its own, shallower ring of at most 32 KB (never
+// deeper than B's). The m-indices do not pass through shared memory.
+constexpr int kTcStageK = 128;        // MMA-K columns (rows of B) per stage
 constexpr int kTcARingBytes = 32 * 1024;
 constexpr int kTcMaxStages = 8;
 
@@ -99,11 +98,31 @@ __host__ __device__ constexpr int tc_a_stages(int tile_m, int b_stages) {
 // B of a tensor-core launch is loaded narrow (see tc_b_slot_bytes).
 __host__ __device__ constexpr bool tc_narrow_b(int tile_n, bool gather) { return !gather && tile_n < 64; }
 
+// How the tensor-core kernel forms its operands.
+enum TcMode : int {
+    // M == 4: A is plain 2:4; A values by TMA, B in TMA tiles over K
+    kTcTiled = 0,
+    // M > 4: the MMAs run over the condensed K; A values by TMA, the 4
+    // selected rows of B per block gathered through column-loc
+    kTcGather = 1,
+    // M == 8: the MMAs run over the whole K. A row keeps 2 values in a block
+    // of 8 columns, so it never has more than 2 in a group of 4: the kernel
+    // re-encodes each block's two values as 2:4 over the block's columns
+    // (zeros fill the groups' free slots) and writes A to shared memory
+    // itself; B in TMA tiles over K as for M == 4
+    kTcLift = 2,
+};
+
+// The tensor-core kernel's K runs over units of kTcStageK columns: of the
+// condensed K (kTcTiled, kTcGather) or of the whole K (kTcLift); both equal
+// K / 128 when M == 4.
+inline int64_t tc_k_units(int64_t K, int32_t M, bool lift) { return lift ? K / kTcStageK : (K / M) / 32; }
+
 struct TcLaunch {
-    CUtensorMap tm_a;   // values, box {64, tile_m}: one stage (4 MMA k-steps), 128B swizzle
+    CUtensorMap tm_a;   // values, box {64, tile_m}: one stage (4 MMA k-steps), 128B swizzle (not read by kTcLift)
     CUtensorMap tm_b;   // B, box {64, 128}, 128B swizzle; {tile_n, 128}, 32B/64B swizzle when narrow
     int tile_m, tile_n, stages, splits;
-    bool gather;        // M > 4: rows of B selected through colidx
+    int mode;           // a TcMode
     int sm_count;       // persistent grid: at most sm_count x resident CTAs per SM
     int skip_stage;     // tests of the bounded waits only (-1: none)
 };

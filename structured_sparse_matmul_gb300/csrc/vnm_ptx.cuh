@@ -108,6 +108,12 @@ __device__ __forceinline__ bool mbar_test3(uint32_t b0, uint32_t p0, uint32_t b1
     return r0 && r1 && r2;
 }
 
+__device__ __forceinline__ bool mbar_test2(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1) {
+    const bool r0 = mbar_test_wait(b0, p0);
+    const bool r1 = mbar_test_wait(b1, p1);
+    return r0 && r1;
+}
+
 // Bounded wait for three barrier phases at once: the three non-blocking
 // tests are issued back to back (their latencies overlap); only a phase that
 // is not yet complete is then waited for on its own.
@@ -118,6 +124,13 @@ __device__ __forceinline__ bool mbar_wait3(uint32_t b0, uint32_t p0, uint32_t b1
     const bool r2 = mbar_test_wait(b2, p2);
     if (r0 && r1 && r2) return true;
     return (r0 || mbar_wait(b0, p0, abort)) && (r1 || mbar_wait(b1, p1, abort)) && (r2 || mbar_wait(b2, p2, abort));
+}
+
+__device__ __forceinline__ bool mbar_wait2(uint32_t b0, uint32_t p0, uint32_t b1, uint32_t p1, volatile int* abort) {
+    const bool r0 = mbar_test_wait(b0, p0);
+    const bool r1 = mbar_test_wait(b1, p1);
+    if (r0 && r1) return true;
+    return (r0 || mbar_wait(b0, p0, abort)) && (r1 || mbar_wait(b1, p1, abort));
 }
 
 // Same bounded wait, but it ignores the abort flag: used while draining
@@ -181,6 +194,11 @@ __device__ __forceinline__ void st_global_v8(void* p, uint32_t a0, uint32_t a1, 
                                              uint32_t a5, uint32_t a6, uint32_t a7) {
     asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a0), "r"(a1), "r"(a2),
                  "r"(a3), "r"(a4), "r"(a5), "r"(a6), "r"(a7)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
 }
 

@@ -43,10 +43,11 @@ class VnmError(RuntimeError):
 
 class vnm_spmm_plan(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("tile_m", ctypes.c_int32), ("tile_n", ctypes.c_int32),
-                ("stages", ctypes.c_int32), ("splits", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("stages", ctypes.c_int32), ("splits", ctypes.c_int32), ("lift", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
     def as_dict(self):
-        return {k: getattr(self, k) for k in ("path", "tile_m", "tile_n", "stages", "splits")}
+        return {k: getattr(self, k) for k in ("path", "tile_m", "tile_n", "stages", "splits", "lift")}
 
 
 def _declare(L: ctypes.CDLL) -> ctypes.CDLL:

@@ -24,10 +24,12 @@ def _product(R, K, N, V, M, seed):
 
 
 # shapes with enough tiles that K is not split, so the first CTA runs every
-# stage of its tiles; the last one gives it four tiles (persistent schedule)
-@pytest.mark.parametrize("R,K,N,V,M,skip", [(2048, 2048, 1024, 128, 4, 3),   # B by TMA
-                                            (2048, 2048, 1024, 64, 8, 2),    # B gathered
-                                            (4096, 2048, 2048, 64, 8, 9)])   # second tile of four (8 stages each)
+# stage of its tiles (persistent schedule: CTA 0 takes tiles 0, 152, ...)
+@pytest.mark.parametrize("R,K,N,V,M,skip", [(2048, 2048, 1024, 128, 4, 3),    # B by TMA
+                                            (2048, 2048, 1024, 64, 16, 2),    # B gathered
+                                            (4096, 2048, 2048, 64, 16, 9),    # third tile of four (4 stages each)
+                                            (4096, 2048, 2048, 32, 8, 2),     # A re-encoded as 2:4 (lift)
+                                            (4096, 2048, 2048, 32, 8, 20)])   # second tile of two (16 stages each)
 def test_bounded_wait_reports_timeout_and_device_stays_usable(R, K, N, V, M, skip):
     A, B, comp = _product(R, K, N, V, M, seed=80 + M)
     Bd = torch.from_numpy(B).to(device())
@@ -55,7 +57,8 @@ def test_skip_stage_needs_the_tensor_core_path():
 
 
 @pytest.mark.parametrize("R,K,N,V,M", [(272, 256, 72, 16, 4),     # tensor cores, ragged rows and columns
-                                       (256, 1024, 296, 64, 8),   # gather, ragged against the tile
+                                       (256, 1024, 296, 64, 16),  # gather, ragged against the tile
+                                       (144, 1024, 296, 16, 8),   # lift, ragged rows and columns
                                        (192, 768, 5, 64, 8),      # streaming small N
                                        (96, 600, 33, 8, 5)])      # CUDA-core rows
 def test_outputs_stay_inside_c(R, K, N, V, M):

@@ -62,7 +62,9 @@ TC_SHAPES = [
     (272, 256, 72, 16, 4),     # ragged rows (R % 128 != 0), plain 2:4
     (256, 1024, 24, 256, 8),   # V = 256: two tiles per block row
     (128, 512, 8, 128, 4),     # N = 8: one MMA of N = 16 with zero-filled columns
-    (256, 1024, 128, 64, 8),   # V = 64: 64-row tiles (M = 64 MMA)
+    (256, 1024, 128, 64, 16),  # V = 64: 64-row tiles (M = 64 MMA), gathered B
+    (256, 1024, 128, 64, 8),
+    (272, 1024, 88, 16, 8),    # V = 16, M = 8: A re-encoded as 2:4 (lift), ragged rows
     (192, 2048, 40, 64, 16),
     (64, 4096, 256, 64, 32),
     (320, 512, 72, 64, 4),     # V = 64 with M = 4: 128-row tiles, ragged rows
@@ -84,10 +86,11 @@ def test_tensor_core_path(R, K, N, V, M, c_dtype):
 @pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 192, 256])
 @pytest.mark.parametrize("V,tile_m", [(128, 128), (64, 64), (128, 64)])
 def test_tensor_core_tiles(tile_n, V, tile_m):
+    """Gathered B (lift = 0) at every tile width and both MMA heights."""
     R, K, N, M = 256, 1024, 296, 8  # N % 8 == 0 (TMA rows), ragged against every tile_n
     A, B, comp = _setup(R, K, N, V, M, seed=22)
     plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
-    assert plan.path == vnm.VNM_PATH_TC
+    assert plan.path == vnm.VNM_PATH_TC and plan.lift == 0
     plan.tile_m = tile_m
     plan.tile_n = tile_n
     plan.stages = 0  # the default depth for this tile
@@ -108,6 +111,133 @@ def test_tensor_core_tiles_plain_2to4(tile_n):
     plan.splits = 1
     got, _ = run_spmm(A, B, plan=plan)
     check_close(got, _ref(comp, R, K, V, M, B), f"plain 2:4 tile_n {tile_n}")
+
+
+# ---------------------------------------------------------------- M = 8 re-encoded as 2:4 (lift)
+
+def _lift_plan(A, B, c_dtype=torch.float16):
+    """The plan vnm_spmm would use, asked for the re-encoded path (the
+    default only where the gather cannot run)."""
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B), c_dtype)
+    assert plan.path == vnm.VNM_PATH_TC, plan.as_dict()
+    plan.lift = 1
+    plan.tile_m = 128
+    plan.stages = 0
+    return plan
+
+
+def _all_pairs_weights(R, K, V, seed):
+    """W (R x K, M = 8) in which every V-block row keeps, in block j, the
+    pair of columns PAIRS[(j + 3 * vb) % 28]: all rows of the V-block are
+    non-zero there (with random signs and magnitudes) and zero elsewhere, so
+    the column selection takes those two columns first and every row keeps
+    both. Every one of the 28 pairs d0 < d1 of an 8-column block appears,
+    in every position of a 16-block stage."""
+    pairs = [(a, b) for a in range(8) for b in range(a + 1, 8)]
+    rng = np.random.default_rng(seed)
+    W = np.zeros((R, K), dtype=np.float16)
+    for vb in range(R // V):
+        for j in range(K // 8):
+            d0, d1 = pairs[(j + 3 * vb) % 28]
+            rows = slice(vb * V, (vb + 1) * V)
+            W[rows, 8 * j + d0] = (rng.uniform(0.5, 2.0, V) * rng.choice([-1, 1], V)).astype(np.float16)
+            W[rows, 8 * j + d1] = (rng.uniform(0.5, 2.0, V) * rng.choice([-1, 1], V)).astype(np.float16)
+    return W
+
+
+@pytest.mark.parametrize("V", [16, 64, 128])
+def test_lift_every_column_pair(V):
+    """Every (d0, d1) placement of a row's two kept values in an 8-column
+    block: the 2:4 re-encoding (both in the first group, both in the second,
+    one in each, with column 0 or 4 among them or not) against the oracle,
+    with the fp32 summation bound."""
+    R, K, N = 256, 2048, 136
+    W = _all_pairs_weights(R, K, V, seed=61)
+    B = inputs.normal_f16((K, N), 61, 1, 1.0)
+    A, st = gpu_compress(W, V, 8)
+    assert st == vnm.VNM_OK
+    comp = assert_compress_bitexact(A, W, V, 8)
+    plan = _lift_plan(A, B, torch.float32)
+    got, _ = run_spmm(A, B, torch.float32, plan=plan)
+    check_close(got, _ref(comp, R, K, V, 8, B), f"all pairs V={V}")
+    check_tight_f32(got, comp, R, K, V, 8, B, what=f"all pairs V={V}")
+
+
+@pytest.mark.parametrize("R,K,N,V", [(128, 128, 16, 16),     # one tile, one stage
+                                     (144, 384, 40, 16),     # ragged rows (R % 128 = 16) and columns
+                                     (320, 1024, 296, 32),   # V = 32
+                                     (384, 1152, 520, 64),   # three row tiles, N over two 256-column tiles
+                                     (512, 1024, 64, 256)])  # V = 256: two row tiles share column-loc
+@pytest.mark.parametrize("c_dtype", [torch.float16, torch.float32], ids=["f16", "f32"])
+def test_lift_shapes(R, K, N, V, c_dtype):
+    A, B, comp = _setup(R, K, N, V, 8, seed=62)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B), c_dtype)
+    assert plan.path == vnm.VNM_PATH_TC and plan.lift == (1 if V % 64 or (K // 8) % 32 else 0), plan.as_dict()
+    got, _ = run_spmm(A, B, c_dtype, plan=_lift_plan(A, B, c_dtype))
+    check_close(got, _ref(comp, R, K, V, 8, B), f"lift {R}x{K}x{N} V={V}")
+    if c_dtype == torch.float32:
+        check_tight_f32(got, comp, R, K, V, 8, B, what=f"lift {R}x{K}x{N} V={V}")
+
+
+@pytest.mark.parametrize("tile_n", [16, 32, 64, 128, 192, 256])
+def test_lift_tiles(tile_n):
+    R, K, N, V = 256, 1024, 296, 64
+    A, B, comp = _setup(R, K, N, V, 8, seed=63)
+    plan = _lift_plan(A, B)
+    plan.tile_n = tile_n
+    plan.stages = 0
+    plan.splits = 1
+    got, _ = run_spmm(A, B, torch.float32, plan=plan)
+    check_close(got, _ref(comp, R, K, V, 8, B), f"lift tile_n {tile_n}")
+    check_tight_f32(got, comp, R, K, V, 8, B, what=f"lift tile_n {tile_n}")
+
+
+@pytest.mark.parametrize("splits", [2, 3, 7])
+def test_lift_split_k(splits):
+    R, K, N, V = 256, 2560, 40, 128
+    A, B, comp = _setup(R, K, N, V, 8, seed=64)
+    plan = _lift_plan(A, B)
+    plan.splits = splits
+    for c_dtype in (torch.float16, torch.float32):
+        got, _ = run_spmm(A, B, c_dtype, plan=plan)
+        check_close(got, _ref(comp, R, K, V, 8, B), f"lift splits {splits}")
+    check_tight_f32(got, comp, R, K, V, 8, B, what=f"lift splits {splits}")
+
+
+def test_lift_agrees_with_gather():
+    """Both tensor-core formulations of one M = 8 product (the MMAs over the
+    condensed K with gathered rows of B, and over the whole K with A
+    re-encoded) are within the fp32 bound of the oracle."""
+    R, K, N, V = 512, 2048, 264, 128
+    A, B, comp = _setup(R, K, N, V, 8, seed=65)
+    lifted, _ = run_spmm(A, B, torch.float32, plan=_lift_plan(A, B))
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    assert plan.lift == 0
+    gathered, _ = run_spmm(A, B, torch.float32, plan=plan)
+    for got, what in ((lifted, "lift"), (gathered, "gather")):
+        check_tight_f32(got, comp, R, K, V, 8, B, what=what)
+
+
+def test_lift_plan_checks():
+    R, K, N, V = 256, 1024, 64, 128
+    A, B, _ = _setup(R, K, N, V, 8, seed=66)
+    plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
+    assert plan.lift == 0 and plan.tile_m == 128
+    plan.lift = 2
+    with pytest.raises(vnm.VnmError) as e:
+        run_spmm(A, B, plan=plan)
+    assert e.value.code == vnm.VNM_ERR_INVALID_ARG
+    plan.lift = 1
+    plan.tile_m = 64
+    with pytest.raises(vnm.VnmError) as e:
+        run_spmm(A, B, plan=plan)
+    assert e.value.code == vnm.VNM_ERR_UNSUPPORTED
+    # K % 128 != 0 (but K/M % 32 == 0 is not met either): the CUDA-core path
+    A2, B2, comp2 = _setup(64, 1088, 40, 16, 8, seed=67)
+    plan2 = vnm.vnm_spmm_plan_query(A2, to_dev(B2))
+    assert plan2.path == vnm.VNM_PATH_SIMT and plan2.lift == 0
+    got, _ = run_spmm(A2, B2)
+    check_close(got, _ref(comp2, 64, 1088, 16, 8, B2), "K % 128 != 0")
 
 
 def test_reserved_plan_fields_rejected():
@@ -165,11 +295,16 @@ def test_unaligned_and_strided_operands():
 
 
 def test_unservable_plan_rejected():
-    R, K, N, V, M = 128, 512, 64, 64, 8
+    R, K, N, V, M = 128, 512, 64, 64, 16
     A, B, comp = _setup(R, K, N, V, M, seed=27)
     plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
-    assert plan.path == vnm.VNM_PATH_TC and plan.tile_m == 64
+    assert plan.path == vnm.VNM_PATH_TC and plan.tile_m == 64 and plan.lift == 0
     plan.tile_m = 128  # a 128-row tile would span two column-loc blocks
+    with pytest.raises(vnm.VnmError) as e:
+        run_spmm(A, B, plan=plan)
+    assert e.value.code == vnm.VNM_ERR_UNSUPPORTED
+    plan.tile_m = 64
+    plan.lift = 1  # M = 16 cannot be re-encoded as 2:4 over 8-column blocks
     with pytest.raises(vnm.VnmError) as e:
         run_spmm(A, B, plan=plan)
     assert e.value.code == vnm.VNM_ERR_UNSUPPORTED
@@ -316,7 +451,8 @@ def test_streaming_at_n8_by_plan():
     check_close(got, _ref(comp, R, K, V, M, B), "stream N=8")
 
 
-@pytest.mark.parametrize("R,K,N,V,M", [(1024, 4096, 512, 64, 8),   # tensor cores, gathered B
+@pytest.mark.parametrize("R,K,N,V,M", [(1024, 4096, 512, 32, 8),   # tensor cores, re-encoded A (lift)
+                                       (1024, 4096, 512, 64, 16),  # tensor cores, gathered B
                                        (256, 2560, 40, 128, 4),    # tensor cores, split K
                                        (512, 4096, 3, 64, 8)])     # streaming small N, split K
 def test_repeatable_bit_for_bit(R, K, N, V, M):
