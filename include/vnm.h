@@ -169,6 +169,28 @@ vnm_status vnm_compress(vnm_matrix A, const void* W, int64_t ld_w, vnm_stream_t 
 vnm_status vnm_decompress(vnm_matrix A, void* W_out, int64_t ld_w, vnm_stream_t stream);
 
 /*
+ * Fused dense GEMM + prune-and-encode: W = X . Y^T, then vnm_compress(W)
+ * into the handle's arrays, with W never written to global memory (DFSS,
+ * "Dynamic N:M fine-grained structured sparse attention", sections 4.2-4.3:
+ * the N:M selection and the encoding of values and metadata in the epilogue
+ * of the GEMM that produces the sparse operand, there Q K^T).
+ * X: fp16 R x D row-major (ld_x >= D); Y: fp16 K x D row-major (ld_y >= D),
+ * so W[r][k] = sum_d X[r][d] * Y[k][d], accumulated in fp32 and rounded once
+ * to fp16 (round to nearest even); R, K, V, M are the handle's. The result
+ * equals vnm_compress applied to that fp16 W (same selection rules, same
+ * arrays). W_out: if not NULL, W is also written there (fp16 R x K, leading
+ * dimension ld_w >= K, 2-byte aligned; for tests); else ignored.
+ * Shapes served: V divides 128, M in {4, 8, 16, 32, 64}; D >= 0 (D = 0 gives
+ * W = 0). X and Y 16-byte aligned with ld_x % 8 == 0 and ld_y % 8 == 0.
+ * Errors: VNM_ERR_INVALID_ARG (pointers, leading dimensions, D < 0),
+ * VNM_ERR_UNSUPPORTED (V or M outside the shapes served), VNM_ERR_CUDA;
+ * Inf/NaN in W (e.g. fp16 overflow) sets VNM_ERR_NONFINITE in the status
+ * word, a bounded wait that runs out VNM_ERR_TIMEOUT.
+ */
+vnm_status vnm_gemm_compress(vnm_matrix A, const void* X, int64_t ld_x, const void* Y, int64_t ld_y, int64_t D,
+                             void* W_out, int64_t ld_w, vnm_stream_t stream);
+
+/*
  * C = A . B (VENOM section 4, Figure 4: sparse A times dense B is dense C;
  * the column-loc of each block selects the 4 rows of B that its kept columns
  * meet, and the m-indices select 2 of those 4 per row).

@@ -9,7 +9,8 @@ The C source restates "VENOM: A Vectorized N:M Format for Unleashing the
 Power of Sparse Tensor Cores", section 3 (Figures 2 and 3) and section 4
 (Figure 4), with the 2:4 packing of the lecture notes "2:4 sparsity on sparse
 tensor cores" ("The compressed format", "Worked: compress a 2 x 8 matrix").
-Every function is pinned by tests/test_oracle.py.
+:func:`gemm_compress` composes numpy's fp64 matmul with the C compress
+(DFSS sections 4.2-4.3). Every function is pinned by tests/test_oracle.py.
 """
 from __future__ import annotations
 
@@ -115,6 +116,25 @@ def compress(W: np.ndarray, V: int, M: int, L: Optional[ctypes.CDLL] = None):
     if rc != OK:
         raise OracleError(rc, "compress")
     return values, meta, colidx
+
+
+def gemm_compress(X: np.ndarray, Y: np.ndarray, V: int, M: int, L: Optional[ctypes.CDLL] = None):
+    """The fused GEMM + prune-and-encode: W = X . Y^T, then ``compress(W)``.
+
+    Restates "Dynamic N:M fine-grained structured sparse attention" (DFSS),
+    sections 4.2-4.3: the dense product that yields the sparse operand (there
+    Q K^T) is pruned and encoded as it is produced; the pruning rule here is
+    that of :func:`compress` (VENOM section 3). X is fp16 R x D, Y fp16 K x D.
+    The product step is numpy's matmul in fp64 (every product of two fp16
+    values is exact in fp64); W is rounded once from fp64 to fp16, to nearest
+    even. Returns ``(W, (values, meta, colidx))`` with W fp16 R x K.
+    """
+    X = np.asarray(X, dtype=np.float16)
+    Y = np.asarray(Y, dtype=np.float16)
+    assert X.ndim == 2 and Y.ndim == 2 and X.shape[1] == Y.shape[1]
+    with np.errstate(over="ignore"):  # beyond the fp16 range: Inf, reported by compress()
+        W = (X.astype(np.float64) @ Y.astype(np.float64).T).astype(np.float16)
+    return W, compress(W, V, M, L)
 
 
 def decompress(values: np.ndarray, meta: np.ndarray, colidx: np.ndarray, R: int, K: int, V: int,

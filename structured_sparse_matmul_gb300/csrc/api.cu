@@ -342,6 +342,37 @@ vnm_status vnm_decompress(vnm_matrix A, void* W_out, int64_t ld_w, vnm_stream_t 
                : VNM_ERR_CUDA;
 }
 
+vnm_status vnm_gemm_compress(vnm_matrix A, const void* X, int64_t ld_x, const void* Y, int64_t ld_y, int64_t D,
+                             void* W_out, int64_t ld_w, vnm_stream_t stream) {
+    if (!valid_handle(A)) return VNM_ERR_INVALID_ARG;
+    if (D < 0 || D > (int64_t(1) << 31)) return VNM_ERR_INVALID_ARG;
+    if (ld_x < std::max<int64_t>(D, 1) || ld_y < std::max<int64_t>(D, 1)) return VNM_ERR_INVALID_ARG;
+    if (W_out != nullptr && (ld_w < std::max<int64_t>(A->K, 1) || !aligned(W_out, 2))) return VNM_ERR_INVALID_ARG;
+    if (!vnm::gemm_compress_shape_ok(A->V, A->M)) return VNM_ERR_UNSUPPORTED;
+    if (A->R == 0 || A->K == 0) return VNM_OK;
+    if (D > 0 && (X == nullptr || Y == nullptr || !aligned(X, 16) || !aligned(Y, 16) || ld_x % 8 != 0 ||
+                  ld_y % 8 != 0))
+        return VNM_ERR_INVALID_ARG;
+    vnm_status st = check_device(A);
+    if (st != VNM_OK) return st;
+    CUtensorMap tm_x, tm_y;
+    std::memset(&tm_x, 0, sizeof(tm_x));
+    std::memset(&tm_y, 0, sizeof(tm_y));
+    if (D > 0) {
+        // boxes of 64 D-columns (128 bytes) x 128 rows, 128B swizzle; rows and columns past
+        // the matrix read as zeros
+        const bool ok = encode_2d(&tm_x, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, D, A->R, ld_x * 2, 64, 128,
+                                  CU_TENSOR_MAP_SWIZZLE_128B) &&
+                        encode_2d(&tm_y, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, Y, D, A->K, ld_y * 2, 64, 128,
+                                  CU_TENSOR_MAP_SWIZZLE_128B);
+        if (!ok) return VNM_ERR_CUDA;
+    }
+    return vnm::launch_gemm_compress(*A, tm_x, tm_y, D, W_out, ld_w, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? VNM_OK
+               : VNM_ERR_CUDA;
+}
+
 vnm_status vnm_spmm_plan_query(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, vnm_dtype c_type,
                                size_t workspace_bytes, vnm_spmm_plan* plan) {
     if (!valid_handle(A) || plan == nullptr) return VNM_ERR_INVALID_ARG;

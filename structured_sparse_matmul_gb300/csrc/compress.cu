@@ -20,6 +20,7 @@
 
 #include "vnm_internal.h"
 #include "vnm_ptx.cuh"
+#include "vnm_select.cuh"
 
 namespace vnm {
 namespace {
@@ -27,64 +28,6 @@ namespace {
 constexpr int kCompressThreads = 256;
 constexpr int kTileElems = 16384;  // V x TK elements of W staged per CTA (32 KB)
 constexpr int kTileMaxCols = 4096; // TK cap (bounds the column-sum array)
-
-// |h| in units of 2^-24 (binary16: 5 exponent bits, bias 15, 10 fraction bits).
-__device__ __forceinline__ uint64_t mag_units(uint16_t h) {
-    const uint32_t e = (h >> 10) & 0x1Fu, f = h & 0x3FFu;
-    return e == 0 ? static_cast<uint64_t>(f) : static_cast<uint64_t>(1024u + f) << (e - 1u);
-}
-
-__device__ __forceinline__ bool half_nonfinite(uint16_t h) { return (h & 0x7C00u) == 0x7C00u; }
-
-// Top 4 of n scores: largest first, lower index first on ties; returned as
-// 4 ascending column indices packed in bytes 0..3 of a word.
-__device__ __forceinline__ uint32_t top4_ascending(const uint64_t* score, int n) {
-    uint64_t bv[4] = {0, 0, 0, 0};
-    int bi[4] = {-1, -1, -1, -1};
-    for (int c = 0; c < n; ++c) {
-        const uint64_t v = score[c];
-        // insert after every entry that is >= v (keeps equal scores in index order)
-        if (bi[3] >= 0 && v <= bv[3]) continue;
-        int p = 3;
-        while (p > 0 && (bi[p - 1] < 0 || v > bv[p - 1])) {
-            bv[p] = bv[p - 1];
-            bi[p] = bi[p - 1];
-            --p;
-        }
-        bv[p] = v;
-        bi[p] = c;
-    }
-    // sort the four indices ascending
-    for (int a = 1; a < 4; ++a)
-        for (int b = a; b > 0 && bi[b - 1] > bi[b]; --b) {
-            const int t = bi[b];
-            bi[b] = bi[b - 1];
-            bi[b - 1] = t;
-        }
-    return static_cast<uint32_t>(bi[0]) | (static_cast<uint32_t>(bi[1]) << 8) |
-           (static_cast<uint32_t>(bi[2]) << 16) | (static_cast<uint32_t>(bi[3]) << 24);
-}
-
-// 2 of the 4 values a[0..3] with the largest |a| (lower slot on ties), in
-// ascending slot order. Returns the 4-bit code s0 | s1 << 2 and the two
-// fp16 bit patterns. Branch-free: slot i is kept when fewer than two slots
-// beat it, slot j < i beating i when |a_j| >= |a_i| and slot j > i when
-// |a_j| > |a_i| (finite fp16 magnitudes order like their integer bits).
-__device__ __forceinline__ uint32_t keep2of4(const uint16_t a[4], uint16_t& v0, uint16_t& v1) {
-    const uint32_t m0 = a[0] & 0x7FFFu, m1 = a[1] & 0x7FFFu, m2 = a[2] & 0x7FFFu, m3 = a[3] & 0x7FFFu;
-    const uint32_t g01 = m0 >= m1, g02 = m0 >= m2, g03 = m0 >= m3;
-    const uint32_t g12 = m1 >= m2, g13 = m1 >= m3, g23 = m2 >= m3;
-    const uint32_t r0 = (1u - g01) + (1u - g02) + (1u - g03);
-    const uint32_t r1 = g01 + (1u - g12) + (1u - g13);
-    const uint32_t r2 = g02 + g12 + (1u - g23);
-    const uint32_t r3 = g03 + g13 + g23;
-    const uint32_t keep = (r0 < 2u) | ((r1 < 2u) << 1) | ((r2 < 2u) << 2) | ((r3 < 2u) << 3);
-    const uint32_t s0 = __ffs(keep) - 1u;  // exactly two bits are set
-    const uint32_t s1 = 31u - __clz(keep);
-    v0 = s0 == 0u ? a[0] : (s0 == 1u ? a[1] : a[2]);
-    v1 = s1 == 3u ? a[3] : (s1 == 2u ? a[2] : a[1]);
-    return s0 | (s1 << 2);
-}
 
 // Bytes of the staged W tile, rounded up so the column sums that follow
 // are 16-byte aligned.

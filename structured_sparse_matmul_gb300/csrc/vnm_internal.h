@@ -135,6 +135,14 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
 cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, void* C,
                                  int64_t ld_c, bool c_f32, cudaStream_t stream);
 
+// Fused dense GEMM + prune-and-encode (W = X . Y^T compressed into A in the
+// GEMM's epilogue): tm_x / tm_y are X (R x D) and Y (K x D) as 2-D fp16
+// maps with boxes of 64 D-columns x 128 rows, 128B swizzle. Shapes it
+// serves: V divides 128, M in {4, 8, 16, 32, 64}.
+bool gemm_compress_shape_ok(int V, int M);
+cudaError_t launch_gemm_compress(const vnm_matrix_s& A, const CUtensorMap& tm_x, const CUtensorMap& tm_y, int64_t D,
+                                 void* w_out, int64_t ld_w, cudaStream_t stream);
+
 // Pipeline stages the tensor-core kernel is built with for a tile (0: no such tile).
 int tc_default_stages(int tile_m, int tile_n, bool gather);
 

@@ -61,6 +61,7 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.vnm_matrix_destroy.argtypes = [p]
     L.vnm_compress.argtypes = [p, p, i64, p]
     L.vnm_decompress.argtypes = [p, p, i64, p]
+    L.vnm_gemm_compress.argtypes = [p, p, i64, p, i64, i64, p, i64, p]
     L.vnm_spmm.argtypes = [p, p, i64, i64, p, i64, ctypes.c_int, p, sz, p]
     L.vnm_spmm_workspace_size.argtypes = [p, i64, p]
     L.vnm_spmm_plan_query.argtypes = [p, p, i64, i64, ctypes.c_int, sz, ctypes.POINTER(vnm_spmm_plan)]
@@ -183,6 +184,26 @@ def vnm_decompress(A: VnmMatrix, W_out: torch.Tensor, stream=None) -> None:
         raise ValueError("W_out must be a CUDA fp16 tensor of shape (R, K)")
     _check(lib().vnm_decompress(A.handle, W_out.data_ptr() or None, _rowmajor(W_out, "W_out"), _stream_ptr(stream)),
            "vnm_decompress")
+
+
+def vnm_gemm_compress(A: VnmMatrix, X: torch.Tensor, Y: torch.Tensor, W_out: Optional[torch.Tensor] = None,
+                      stream=None) -> None:
+    """W = X . Y^T (X: R x D, Y: K x D, fp16), compressed into A in the GEMM's
+    epilogue; W_out (R x K fp16), if given, also receives W."""
+    if X.dtype != torch.float16 or not X.is_cuda or X.dim() != 2 or X.shape[0] != A.R:
+        raise ValueError("X must be a CUDA fp16 tensor of shape (R, D)")
+    if Y.dtype != torch.float16 or not Y.is_cuda or Y.dim() != 2 or Y.shape[0] != A.K or Y.shape[1] != X.shape[1]:
+        raise ValueError("Y must be a CUDA fp16 tensor of shape (K, D)")
+    D = int(X.shape[1])
+    w_ptr, ld_w = None, max(A.K, 1)
+    if W_out is not None:
+        if W_out.dtype != torch.float16 or not W_out.is_cuda or tuple(W_out.shape) != (A.R, A.K):
+            raise ValueError("W_out must be a CUDA fp16 tensor of shape (R, K)")
+        w_ptr, ld_w = W_out.data_ptr() or None, _rowmajor(W_out, "W_out")
+    ld_x = _rowmajor(X, "X") if D > 0 else 1
+    ld_y = _rowmajor(Y, "Y") if D > 0 else 1
+    _check(lib().vnm_gemm_compress(A.handle, X.data_ptr() or None, ld_x, Y.data_ptr() or None, ld_y, D, w_ptr, ld_w,
+                                   _stream_ptr(stream)), "vnm_gemm_compress")
 
 
 def _c_type(C: torch.Tensor) -> int:

@@ -297,10 +297,68 @@ def check_fig3_fixture(L):
     assert (np.diff(cl.astype(np.int64), axis=2) > 0).all()
 
 
+def check_gemm_compress_identity(L):
+    """X = I: the fused op's W is Y^T exactly (orientation W = X . Y^T), and
+    its arrays are compress(Y^T)."""
+    rng = np.random.default_rng(7)
+    R, K = 64, 96
+    Y = (rng.standard_normal((K, R)) * 0.5).astype(np.float16)
+    X = np.eye(R, dtype=np.float16)
+    for V, M in ((16, 8), (1, 4), (64, 32)):
+        W, got = oracle.gemm_compress(X, Y, V, M, L)
+        assert W.tobytes() == np.ascontiguousarray(Y.T).tobytes()
+        want = oracle.compress(np.ascontiguousarray(Y.T), V, M, L)
+        for a, b in zip(got, want):
+            assert np.array_equal(a, b)
+
+
+def check_gemm_compress_rank1(L):
+    """D = 1 with powers of two: W[r][k] = x[r] * y[k] exactly, a column's L1
+    over any rows is |y[k]| times a common factor, so every block keeps the 4
+    columns of largest |y| (lower column on ties), and every row the 2 of
+    those with the largest |y|: the expected arrays in closed form."""
+    rng = np.random.default_rng(8)
+    R, K, V, M = 32, 64, 8, 16
+    x = (2.0 ** rng.integers(-6, 4, R) * rng.choice([-1, 1], R)).astype(np.float16)
+    y = (2.0 ** rng.integers(-6, 4, K) * rng.choice([-1, 1], K)).astype(np.float16)
+    W, (values, meta, colidx) = oracle.gemm_compress(x[:, None], y[:, None], V, M, L)
+    assert np.array_equal(W.astype(np.float64), np.outer(x.astype(np.float64), y.astype(np.float64)))
+    for j in range(K // M):
+        mags = np.abs(y[j * M:(j + 1) * M].astype(np.float64))
+        order = sorted(range(M), key=lambda c: (-mags[c], c))
+        cols = sorted(order[:4])
+        keep = sorted(sorted(range(4), key=lambda s: (-mags[cols[s]], s))[:2])
+        for i in range(R // V):
+            assert colidx[i, j].tolist() == cols
+        for r in range(R):
+            want = [np.float16(x[r] * y[j * M + cols[s]]) for s in keep]
+            assert values[r, 2 * j:2 * j + 2].tobytes() == np.array(want, dtype=np.float16).tobytes()
+            assert _slots_of(meta[r], 2 * (K // M))[2 * j:2 * j + 2] == keep
+
+
+def check_gemm_compress_rounding(L):
+    """W is rounded once, to nearest even: exact sums halfway between two
+    fp16 values (1 + 2^-11, 1 + 3 * 2^-11, 1 - 2^-12, 2049) go to the even
+    neighbour (1, 1 + 2^-9, 1, 2048); an fp16 overflow is non-finite."""
+    X = np.array([[1, 2.0 ** -11], [1, 3 * 2.0 ** -11], [1, -(2.0 ** -12)], [2048, 1]], dtype=np.float16)
+    Y = np.zeros((4, 2), dtype=np.float16)
+    Y[0] = [1, 1]
+    W, (values, meta, colidx) = oracle.gemm_compress(X, Y, 1, 4, L)
+    want = np.array([1.0, 1 + 2.0 ** -9, 1.0, 2048.0], dtype=np.float16)
+    assert W[:, 0].tobytes() == want.tobytes()
+    assert not W[:, 1:].any()
+    # each row keeps column 0 and the lowest of the zero columns
+    assert values[:, 0].tobytes() == want.tobytes() and not values[:, 1].any()
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.gemm_compress(np.full((4, 1), 256, np.float16), np.full((4, 1), 256, np.float16), 1, 4, L)
+    assert e.value.code == oracle.NONFINITE
+
+
 PINS = [check_worked_example, check_worked_local_index, check_worked_product,
         check_storage_arithmetic, check_brute_force_ties, check_brute_force_subnormals,
         check_brute_force_normal, check_invariants_and_round_trip, check_spmm_against_numpy,
-        check_fig3_fixture]
+        check_fig3_fixture, check_gemm_compress_identity, check_gemm_compress_rank1,
+        check_gemm_compress_rounding]
 
 
 # ----------------------------------------------------------------------------
