@@ -55,6 +55,69 @@ constexpr int kGcPitchWords = kGcTile / 2 + 1;  // shared W tile: 65 words (130 
 constexpr uint32_t kSleepEpilogue = 256;
 constexpr int kMaxDevicesGc = 64;
 
+// |h| of an fp16 bit pattern, as fp32 (exact).
+__device__ __forceinline__ float abs_half_f32(uint16_t h) {
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h & 0x7FFFu)));
+}
+
+// Top 4 of n >= 5 fp32 column sums of V magnitudes each, when fp32 decides
+// it: `word` gets the 4 columns ascending and the result is true if the
+// 4th largest sum exceeds the 5th by more than both sums' rounding error
+// (at most V * 2^-24 of the larger, for V - 1 additions of non-negative
+// exact terms), so that the exact sums select the same 4 columns. Equal
+// or nearly equal sums return false (the caller sums exactly).
+__device__ __forceinline__ bool top4_f32_sure(const float* s, int n, int V, uint32_t& word) {
+    float k0 = -1.f, k1 = -1.f, k2 = -1.f, k3 = -1.f, k4 = -1.f;  // the 5 best, k0 largest
+    uint32_t i0 = 0, i1 = 0, i2 = 0, i3 = 0;
+    for (int c = 0; c < n; ++c) {
+        const float k = s[c];
+        if (k <= k4) continue;
+        if (k <= k3) {
+            k4 = k;
+            continue;
+        }
+        k4 = k3;
+        if (k > k2) {
+            k3 = k2;
+            i3 = i2;
+            if (k > k1) {
+                k2 = k1;
+                i2 = i1;
+                if (k > k0) {
+                    k1 = k0;
+                    i1 = i0;
+                    k0 = k;
+                    i0 = static_cast<uint32_t>(c);
+                } else {
+                    k1 = k;
+                    i1 = static_cast<uint32_t>(c);
+                }
+            } else {
+                k2 = k;
+                i2 = static_cast<uint32_t>(c);
+            }
+        } else {
+            k3 = k;
+            i3 = static_cast<uint32_t>(c);
+        }
+    }
+    // each sum is within V * 2^-24 * (its value) of the exact one: a gap above twice
+    // that of the larger keeps the order (2^-23 per term, with margin)
+    if (!(k3 - k4 > static_cast<float>(V) * 0x1p-22f * k3)) return false;
+    auto cx = [](uint32_t& a, uint32_t& b) {
+        const uint32_t lo = min(a, b), hi = max(a, b);
+        a = lo;
+        b = hi;
+    };
+    cx(i0, i1);
+    cx(i2, i3);
+    cx(i0, i2);
+    cx(i1, i3);
+    cx(i1, i2);
+    word = i0 | (i1 << 8) | (i2 << 16) | (i3 << 24);
+    return true;
+}
+
 struct GcArgs {
     int64_t R, K;
     int V, M;
@@ -72,8 +135,8 @@ struct GcArgs {
 // Shared-memory layout of the epilogue (inside the stage ring).
 constexpr int kGcTileBytes = kGcTile * kGcPitchWords * 4;         // 33280
 constexpr int kGcGroupBlocks = 16;                                 // V-row blocks summed per pass
-constexpr int kGcScoreOff = (kGcTileBytes + 15) & ~15;             // uint64 column sums of a group
-constexpr int kGcColwOff = kGcScoreOff + kGcGroupBlocks * kGcTile * 8;  // column-loc words of the tile
+constexpr int kGcScoreOff = (kGcTileBytes + 15) & ~15;             // fp32 column sums of a group
+constexpr int kGcColwOff = kGcScoreOff + kGcGroupBlocks * kGcTile * 4;  // column-loc words of the tile
 constexpr int kGcColwMax = kGcTile * (kGcTile / 8);                // (128 / V) x (128 / M) words, M > 4
 static_assert(kGcColwOff + kGcColwMax * 4 <= kGcStages * kGcStageBytes, "epilogue fits the stage ring");
 
@@ -207,10 +270,13 @@ __global__ void __launch_bounds__(kGcThreads, 3)
                     tile[trow * kGcPitchWords + c / 2 + u] = h[u];
                 }
                 if (row < p.R) {
+                    if (n0 + c + 16 <= p.K) {
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        const uint16_t x = static_cast<uint16_t>(h[u / 2] >> (16 * (u & 1)));
-                        if (n0 + c + u < p.K) bad |= half_nonfinite(x);
+                        for (int u = 0; u < 8; ++u)
+                            bad |= ((h[u] & 0x7C00u) == 0x7C00u) | ((h[u] & 0x7C000000u) == 0x7C000000u);
+                    } else {
+                        for (int u = 0; u < 16; ++u)
+                            if (n0 + c + u < p.K) bad |= half_nonfinite(static_cast<uint16_t>(h[u / 2] >> (16 * (u & 1))));
                     }
                     if (p.w_out != nullptr) {
                         uint16_t* dst = p.w_out + row * p.ld_w + n0 + c;
@@ -226,7 +292,7 @@ __global__ void __launch_bounds__(kGcThreads, 3)
 
             const int nb_tile = kGcTile / p.M;  // blocks per tile row
             uint32_t* colw = reinterpret_cast<uint32_t*>(smem_gen + kGcColwOff);
-            uint64_t* score = reinterpret_cast<uint64_t*>(smem_gen + kGcScoreOff);
+            float* fscore = reinterpret_cast<float*>(smem_gen + kGcScoreOff);
             // 2. column-loc of every V-row block of the tile (rows past R: none), in
             //    groups of up to kGcGroupBlocks row blocks: thread t sums column t % 128
             //    over every other row block of the group, then the (row block, block)
@@ -239,20 +305,31 @@ __global__ void __launch_bounds__(kGcThreads, 3)
                     const int g1 = min(rblocks, g0 + kGcGroupBlocks);
                     for (int rb = g0 + part; rb < g1; rb += 2) {
                         const uint16_t* col = tile_h + rb * p.V * (2 * kGcPitchWords) + c;
-                        uint64_t s0 = 0, s1 = 0;
+                        float s0 = 0.f, s1 = 0.f;
                         int r = 0;
                         for (; r + 2 <= p.V; r += 2) {
-                            s0 += mag_units(col[r * (2 * kGcPitchWords)]);
-                            s1 += mag_units(col[(r + 1) * (2 * kGcPitchWords)]);
+                            s0 += abs_half_f32(col[r * (2 * kGcPitchWords)]);
+                            s1 += abs_half_f32(col[(r + 1) * (2 * kGcPitchWords)]);
                         }
-                        if (r < p.V) s0 += mag_units(col[r * (2 * kGcPitchWords)]);
-                        score[(rb - g0) * kGcTile + c] = s0 + s1;
+                        if (r < p.V) s0 += abs_half_f32(col[r * (2 * kGcPitchWords)]);
+                        fscore[(rb - g0) * kGcTile + c] = s0 + s1;
                     }
                     named_barrier(1, kGcEpiThreads);
                     for (int pi = t; pi < (g1 - g0) * nb_tile; pi += kGcEpiThreads) {
                         const int rbl = pi / nb_tile, j = pi - rbl * nb_tile;
                         if (n0 + static_cast<int64_t>(j) * p.M >= p.K) continue;
-                        const uint32_t w = top4_ascending(score + rbl * kGcTile + j * p.M, p.M);
+                        uint32_t w;
+                        if (!top4_f32_sure(fscore + rbl * kGcTile + j * p.M, p.M, p.V, w)) {
+                            // too close to call in fp32: exact integer sums of the block's columns
+                            Top4 best;
+                            for (int cc = 0; cc < p.M; ++cc) {
+                                const uint16_t* col = tile_h + (g0 + rbl) * p.V * (2 * kGcPitchWords) + j * p.M + cc;
+                                uint64_t e = 0;
+                                for (int r = 0; r < p.V; ++r) e += mag_units(col[r * (2 * kGcPitchWords)]);
+                                best.offer(e, static_cast<uint32_t>(cc));
+                            }
+                            w = best.word();
+                        }
                         colw[(g0 + rbl) * nb_tile + j] = w;
                         p.colidx[(m0 / p.V + g0 + rbl) * p.nblk + n0 / p.M + j] = w;
                     }

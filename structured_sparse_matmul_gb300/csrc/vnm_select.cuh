@@ -19,16 +19,17 @@ __device__ __forceinline__ uint64_t mag_units(uint16_t h) {
 
 __device__ __forceinline__ bool half_nonfinite(uint16_t h) { return (h & 0x7C00u) == 0x7C00u; }
 
-// Top 4 of n >= 4 scores: largest first, lower index first on ties;
-// returned as 4 ascending column indices packed in bytes 0..3 of a word.
-// Registers only: the four best keys (score + 1; 0 = empty) shift down as a
-// larger key arrives, and an equal key never displaces an earlier index.
-__device__ __forceinline__ uint32_t top4_ascending(const uint64_t* score, int n) {
+// The 4 largest of a stream of (score, index) pairs offered in increasing
+// index order: largest first, the lower index first on ties (a later equal
+// score never displaces an earlier one). Registers only: the four best keys
+// (score + 1; 0 = empty) shift down as a larger key arrives.
+struct Top4 {
     uint64_t k0 = 0, k1 = 0, k2 = 0, k3 = 0;
     uint32_t i0 = 0, i1 = 0, i2 = 0, i3 = 0;
-    for (int c = 0; c < n; ++c) {
-        const uint64_t k = score[c] + 1;
-        if (k <= k3) continue;
+
+    __device__ __forceinline__ void offer(uint64_t score, uint32_t c) {
+        const uint64_t k = score + 1;
+        if (k <= k3) return;
         if (k > k2) {
             k3 = k2;
             i3 = i2;
@@ -39,32 +40,44 @@ __device__ __forceinline__ uint32_t top4_ascending(const uint64_t* score, int n)
                     k1 = k0;
                     i1 = i0;
                     k0 = k;
-                    i0 = static_cast<uint32_t>(c);
+                    i0 = c;
                 } else {
                     k1 = k;
-                    i1 = static_cast<uint32_t>(c);
+                    i1 = c;
                 }
             } else {
                 k2 = k;
-                i2 = static_cast<uint32_t>(c);
+                i2 = c;
             }
         } else {
             k3 = k;
-            i3 = static_cast<uint32_t>(c);
+            i3 = c;
         }
     }
-    // the four indices ascending (a sorting network of 5 compare-exchanges)
-    auto cx = [](uint32_t& a, uint32_t& b) {
-        const uint32_t lo = min(a, b), hi = max(a, b);
-        a = lo;
-        b = hi;
-    };
-    cx(i0, i1);
-    cx(i2, i3);
-    cx(i0, i2);
-    cx(i1, i3);
-    cx(i1, i2);
-    return i0 | (i1 << 8) | (i2 << 16) | (i3 << 24);
+
+    // the four indices ascending (a sorting network of 5 compare-exchanges),
+    // packed in bytes 0..3
+    __device__ __forceinline__ uint32_t word() const {
+        uint32_t a = i0, b = i1, c = i2, d = i3;
+        auto cx = [](uint32_t& x, uint32_t& y) {
+            const uint32_t lo = min(x, y), hi = max(x, y);
+            x = lo;
+            y = hi;
+        };
+        cx(a, b);
+        cx(c, d);
+        cx(a, c);
+        cx(b, d);
+        cx(b, c);
+        return a | (b << 8) | (c << 16) | (d << 24);
+    }
+};
+
+// Top 4 of n >= 4 scores as 4 ascending column indices packed in bytes 0..3.
+__device__ __forceinline__ uint32_t top4_ascending(const uint64_t* score, int n) {
+    Top4 t;
+    for (int c = 0; c < n; ++c) t.offer(score[c], static_cast<uint32_t>(c));
+    return t.word();
 }
 
 // 2 of the 4 values a[0..3] with the largest |a| (lower slot on ties), in
