@@ -376,6 +376,100 @@ def roofline_of(case, peaks, spmm_us, a_bytes):
             "frac": t_roof / (spmm_us * 1e-6), "bytes": byts, "effective_flops": case.effective_flops()}
 
 
+def _time_graph(dev, fn, launches: int) -> float:
+    """Median of 7 replays of a CUDA graph of `launches` calls fn(i, stream),
+    in microseconds per call (events on the replaying stream)."""
+    import torch
+    cur = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(cur)
+    with torch.cuda.stream(side):
+        fn(0, side)  # warm (and the kernels' one-time set-up) outside the capture
+        side.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=side):
+            for i in range(launches):
+                fn(i, side)
+    torch.cuda.synchronize(dev)
+    g.replay()
+    torch.cuda.synchronize(dev)
+    ts = []
+    for _ in range(7):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(cur)
+        g.replay()
+        e1.record(cur)
+        torch.cuda.synchronize(dev)
+        ts.append(e0.elapsed_time(e1) * 1e3 / launches)
+    return statistics.median(ts)
+
+
+# The fused dense GEMM + prune-and-encode (vnm_gemm_compress) on attention-
+# score-like products X . Y^T (X, Y: L tokens x head dimension D), the
+# operand DFSS prunes on the fly, and one weight-like product with a long D.
+GEMM_COMPRESS_CASES = [
+    # R, K, D, V, M
+    (4096, 4096, 64, 1, 4),
+    (4096, 4096, 128, 16, 8),
+    (8192, 8192, 128, 64, 8),
+    (4096, 4096, 4096, 64, 8),
+]
+
+
+def measure_gemm_compress(dev, peaks, launches: int):
+    """vnm_gemm_compress against the same result in two launches (dense
+    torch.matmul writing W, then vnm_compress reading it), both timed like
+    the per-workload table, with the fused kernel's roofline: dense flops
+    2*R*K*D against the measured tensor peak, bytes X + Y + the compressed
+    arrays against HBM."""
+    import torch
+
+    from structured_sparse_matmul_gb300 import vnm
+
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4242)
+    out = {}
+    for (R, K, D, V, M) in GEMM_COMPRESS_CASES:
+        vb, mb, cb = vnm.vnm_sizes(R, K, V, M)
+        set_bytes = 2 * (R + K) * D + vb + mb + cb
+        n_sets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+        sets = [{"X": torch.randn(R, D, device=dev, generator=gen).half(),
+                 "Y": torch.randn(K, D, device=dev, generator=gen).half(),
+                 "A": vnm.vnm_matrix_alloc(R, K, V, M, dev)} for _ in range(n_sets)]
+        W = torch.empty(R, K, dtype=torch.float16, device=dev)
+
+        def fused(i, st):
+            x = sets[i % n_sets]
+            vnm.vnm_gemm_compress(x["A"], x["X"], x["Y"], stream=st)
+
+        def unfused(i, st):
+            x = sets[i % n_sets]
+            torch.matmul(x["X"], x["Y"].t(), out=W)
+            vnm.vnm_compress(x["A"], W, stream=st)
+
+        t_f = _time_graph(dev, fused, launches)
+        t_u = _time_graph(dev, unfused, launches)
+        for x in sets:
+            st_ = vnm.vnm_get_status(x["A"])
+            if st_ != vnm.VNM_OK:
+                raise RuntimeError(f"kernel status {vnm.status_string(st_)} in gemm_compress {R}x{K}x{D}")
+        flops = 2.0 * R * K * D
+        byts = 2 * (R + K) * D + vb + mb + cb
+        t_roof = max(flops / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9)) * 1e6
+        out[f"{R}x{K}x{D}-{V}:2:{M}"] = {
+            "fused_us": t_f, "matmul_then_compress_us": t_u,
+            "roofline": {"bound": "tensor" if flops / peaks["bf16_tflops"] / 1e12 > byts / peaks["hbm_gbs"] / 1e9
+                         else "hbm", "t_roof_us": t_roof, "frac": t_roof / t_f},
+            "sets": n_sets}
+        del sets, W
+        torch.cuda.empty_cache()
+    return {"launches_per_graph": launches, "replays": 7, "statistic": "median",
+            "inputs": "torch seeded device generator, X, Y ~ N(0, 1)",
+            "l2_eviction": "rotating input sets of more than twice the L2 in each graph", "cases": out}
+
+
 def measure_per_config(dev, peaks, launches: int):
     """Every case of workloads 1-5: SpMM and compress launch times (median of
     7 replays of a graph of `launches` launches over rotating input sets that
@@ -797,6 +891,7 @@ def main():
     per_config = None
     if not args.no_per_config:
         per_config = measure_per_config(dev, peaks, max(2, args.per_config_launches))
+        per_config["gemm_compress"] = measure_gemm_compress(dev, peaks, max(2, args.per_config_launches))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

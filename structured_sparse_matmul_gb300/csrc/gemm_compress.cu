@@ -25,8 +25,9 @@
 //                V-row block (integers in units of 2^-24); the (row block,
 //                block) pairs are spread over the threads, each picking its
 //                block's 4 columns;
-//             3. each thread encodes its row: per block the 2 largest of the
-//                4 selected values, and their slots.
+//             3. the (row, block) items, numbered row-major over the
+//                threads so that a warp's stores are coalesced: per block the
+//                2 largest of the 4 selected values, and their slots.
 // The epilogue's shared memory is the stage ring's: the MMAs are done with
 // it once the accumulator is complete. Every mbarrier wait is bounded.
 #include <cuda_fp16.h>
@@ -290,7 +291,8 @@ __global__ void __launch_bounds__(kGcThreads, 3)
             tc_fence_before_sync();
             named_barrier(1, kGcEpiThreads);
 
-            const int nb_tile = kGcTile / p.M;  // blocks per tile row
+            const int nb_tile = kGcTile / p.M;  // blocks per tile row (a power of 2, as is V)
+            const int lg_nb = __ffs(nb_tile) - 1, lg_v = __ffs(p.V) - 1;
             uint32_t* colw = reinterpret_cast<uint32_t*>(smem_gen + kGcColwOff);
             float* fscore = reinterpret_cast<float*>(smem_gen + kGcScoreOff);
             // 2. column-loc of every V-row block of the tile (rows past R: none), in
@@ -316,7 +318,7 @@ __global__ void __launch_bounds__(kGcThreads, 3)
                     }
                     named_barrier(1, kGcEpiThreads);
                     for (int pi = t; pi < (g1 - g0) * nb_tile; pi += kGcEpiThreads) {
-                        const int rbl = pi / nb_tile, j = pi - rbl * nb_tile;
+                        const int rbl = pi >> lg_nb, j = pi & (nb_tile - 1);
                         if (n0 + static_cast<int64_t>(j) * p.M >= p.K) continue;
                         uint32_t w;
                         if (!top4_f32_sure(fscore + rbl * kGcTile + j * p.M, p.M, p.V, w)) {
@@ -338,41 +340,42 @@ __global__ void __launch_bounds__(kGcThreads, 3)
             } else {
                 // M = 4: every block keeps its 4 columns
                 for (int pi = t; pi < rblocks * nb_tile; pi += kGcEpiThreads) {
-                    const int rb = pi / nb_tile, j = pi - rb * nb_tile;
+                    const int rb = pi >> lg_nb, j = pi & (nb_tile - 1);
                     if (n0 + static_cast<int64_t>(j) * p.M < p.K)
                         p.colidx[(m0 / p.V + rb) * p.nblk + n0 / p.M + j] = 0x03020100u;
                 }
             }
-            // 3. one row, half of its blocks (all of both when the tile holds 2): per
-            //    block 2 of the 4 selected values, and their slots
-            const int er = t & (kGcTile - 1), ehalf = t >> 7;
-            const int64_t erow = m0 + er;
+            // 3. per (row, block) item, 2 of the block's 4 selected values and their
+            //    slots. Items are numbered row-major, so the lanes of a warp hold
+            //    consecutive blocks of a row and its stores are coalesced: values
+            //    as 4-byte words, the slots of two neighbouring blocks as one byte
+            //    (the even lane of the pair writes it)
             const int64_t left = (p.K - n0) / p.M;  // blocks of the tile inside K
             const int nvalid = static_cast<int>(left < nb_tile ? left : nb_tile);
-            const int jb = nb_tile >= 4 ? ehalf * (nb_tile / 2) : 0;
-            const int je = min(nvalid, nb_tile >= 4 ? jb + nb_tile / 2 : (ehalf == 0 ? nb_tile : 0));
-            if (erow < p.R && jb < je) {
-                const int rb = er / p.V;
-                uint16_t* vrow = p.values + erow * p.vpr + (n0 / p.M) * 2;
-                uint8_t* mrow = p.meta + erow * p.mpitch + n0 / (2 * p.M);
-                uint32_t codes = 0;  // two blocks' 4-bit codes per byte
-                int j = jb;
-                for (; j < je; ++j) {
-                    const uint32_t w = p.M > 4 ? colw[rb * nb_tile + j] : 0x03020100u;
+            const int items = static_cast<int>(rows_here) * nb_tile;  // nb_tile is a power of 2, >= 2
+            const int lane_e = t & 31;
+            uint16_t* const vtile = p.values + m0 * p.vpr + (n0 / p.M) * 2;   // the tile's first value
+            uint8_t* const mtile = p.meta + m0 * p.mpitch + n0 / (2 * p.M);  // and m-index byte
+            for (int i0 = t - lane_e; i0 < items; i0 += kGcEpiThreads) {
+                const int i = i0 + lane_e;
+                const int er = i >> lg_nb, j = i & (nb_tile - 1);
+                const bool live = i < items && j < nvalid;
+                uint32_t code = 0;
+                if (live) {
+                    const uint32_t w = p.M > 4 ? colw[((er >> lg_v) << lg_nb) + j] : 0x03020100u;
+                    const uint16_t* trow_h = tile_h + er * (2 * kGcPitchWords) + j * p.M;
                     uint16_t a[4];
 #pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        a[s] = tile_h[er * (2 * kGcPitchWords) + j * p.M + ((w >> (8 * s)) & 0xFFu)];
+                    for (int s = 0; s < 4; ++s) a[s] = trow_h[(w >> (8 * s)) & 0xFFu];
                     uint16_t v0, v1;
-                    const uint32_t code = keep2of4(a, v0, v1);
-                    *reinterpret_cast<uint32_t*>(vrow + 2 * j) = static_cast<uint32_t>(v0) | (static_cast<uint32_t>(v1) << 16);
-                    codes |= code << (4 * (j & 1));
-                    if (j & 1) {
-                        mrow[j / 2] = static_cast<uint8_t>(codes);
-                        codes = 0;
-                    }
+                    code = keep2of4(a, v0, v1);
+                    *reinterpret_cast<uint32_t*>(vtile + er * p.vpr + 2 * j) =
+                        static_cast<uint32_t>(v0) | (static_cast<uint32_t>(v1) << 16);
                 }
-                if (j & 1) mrow[j / 2] = static_cast<uint8_t>(codes);  // an odd last block: upper nibble 0
+                // the odd neighbour's code (0 when it lies past K: upper nibble 0)
+                const uint32_t hi = __shfl_down_sync(0xFFFFFFFFu, code, 1);
+                if (live && (j & 1) == 0)
+                    mtile[er * p.mpitch + j / 2] = static_cast<uint8_t>(code | (hi << 4));
             }
         }
     }
