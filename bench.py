@@ -470,6 +470,49 @@ def measure_gemm_compress(dev, peaks, launches: int):
             "l2_eviction": "rotating input sets of more than twice the L2 in each graph", "cases": out}
 
 
+def measure_energy(dev):
+    """Energy (magnitude preservation) of the three selection policies at the
+    V:N:M densities 2/M on a synthetic N(0, 0.02) weight of the 768 x 768
+    shape of the pages' Figure 11 study (VENOM section 5), and the time of one
+    vnm_energy call (its host read-back included) on a 4096 x 4096 weight."""
+    import torch
+
+    from structured_sparse_matmul_gb300 import inputs, vnm
+
+    W_h = inputs.normal_f16((768, 768), 1011, 0, 0.02)
+    W = torch.from_numpy(W_h).to(dev)
+    table = {}
+    for M in (4, 8, 16, 32):
+        row = {}
+        A1 = vnm.vnm_matrix_alloc(768, 768, 16, M, dev)
+        row["unstructured"] = vnm.vnm_energy(A1, W, vnm.VNM_PATTERN_UNSTRUCTURED)[0]
+        for V in (1, 16, 32, 64, 128):
+            A = vnm.vnm_matrix_alloc(768, 768, V, M, dev)
+            vnm.vnm_compress(A, W)
+            row[f"{V}:2:{M}"] = vnm.vnm_energy(A, W, vnm.VNM_PATTERN_VNM)[0]
+        for l in (4, 8, 16, 32):
+            A = vnm.vnm_matrix_alloc(768, 768, l, M, dev)
+            row[f"vw_{l}"] = vnm.vnm_energy(A, W, vnm.VNM_PATTERN_VECTORWISE)[0]
+        table[f"density 2/{M}"] = row
+    big = torch.from_numpy(inputs.normal_f16((4096, 4096), 1012, 0, 0.02)).to(dev)
+    A = vnm.vnm_matrix_alloc(4096, 4096, 64, 8, dev)
+    vnm.vnm_compress(A, big)
+    ws = torch.empty(vnm.vnm_energy_workspace_size(A), dtype=torch.uint8, device=dev)
+    times = {}
+    for name, pat in (("vnm", vnm.VNM_PATTERN_VNM), ("unstructured", vnm.VNM_PATTERN_UNSTRUCTURED),
+                      ("vectorwise", vnm.VNM_PATTERN_VECTORWISE)):
+        ts = []
+        for _ in range(7):
+            torch.cuda.synchronize(dev)
+            t0 = time.perf_counter()
+            vnm.vnm_energy(A, big, pat, workspace=ws)
+            ts.append((time.perf_counter() - t0) * 1e6)
+        times[name] = statistics.median(ts)
+    return {"weight": "768x768 N(0, 0.02), synthetic (the shape of the pages' Figure 11 study)",
+            "energy": table,
+            "call_us_4096x4096_v64m8": times}
+
+
 def measure_per_config(dev, peaks, launches: int):
     """Every case of workloads 1-5: SpMM and compress launch times (median of
     7 replays of a graph of `launches` launches over rotating input sets that
@@ -892,6 +935,7 @@ def main():
     if not args.no_per_config:
         per_config = measure_per_config(dev, peaks, max(2, args.per_config_launches))
         per_config["gemm_compress"] = measure_gemm_compress(dev, peaks, max(2, args.per_config_launches))
+        per_config["energy"] = measure_energy(dev)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -77,6 +77,13 @@ typedef enum vnm_path {
                           distributed shared memory); larger N, one warp per row */
 } vnm_path;
 
+/* Selection policies of vnm_energy (all at the V:N:M density 2/M). */
+typedef enum vnm_pattern {
+    VNM_PATTERN_VNM = 0,          /* the kept values of the compressed matrix */
+    VNM_PATTERN_UNSTRUCTURED = 1, /* the 2RK/M largest |w| of the whole matrix */
+    VNM_PATTERN_VECTORWISE = 2    /* per panel of V rows, the 2K/M columns of largest L1 norm */
+} vnm_pattern;
+
 /* A launch plan for vnm_spmm. vnm_spmm_plan_query fills one; a caller may
  * edit it and pass it to vnm_spmm_with_plan (tests and tuning sweeps do). */
 typedef struct vnm_spmm_plan {
@@ -167,6 +174,34 @@ vnm_status vnm_compress(vnm_matrix A, const void* W, int64_t ld_w, vnm_stream_t 
  * Errors: VNM_ERR_INVALID_ARG.
  */
 vnm_status vnm_decompress(vnm_matrix A, void* W_out, int64_t ld_w, vnm_stream_t stream);
+
+/*
+ * Energy (magnitude preservation) of pruning the dense fp16 matrix W (R x K,
+ * leading dimension ld_w >= K; R, K, V, M are the handle's) with a selection
+ * policy (VENOM section 5, Figure 11): sum of the kept |w| over the sum of
+ * all |w|, at the V:N:M density 2/M for every policy:
+ *   VNM_PATTERN_VNM           the kept values of A: A must hold the
+ *                             compression of W (vnm_compress(A, W) first);
+ *   VNM_PATTERN_UNSTRUCTURED  the R*2K/M largest |w| of W (the ideal);
+ *   VNM_PATTERN_VECTORWISE    vectors of V x 1: per panel of V consecutive
+ *                             rows, the 2K/M columns of largest L1 norm over
+ *                             the panel.
+ * The sums are exact: kept_units and total_units (each {low 64 bits, high 64
+ * bits}, either may be NULL) count units of 2^-24; *energy (may be NULL) is
+ * their ratio as a double, 1.0 when W is all zeros. Ties cannot change a
+ * kept sum, so each value is unique.
+ * workspace: device memory of at least vnm_energy_workspace_size bytes,
+ * 16-byte aligned. W: 2-byte aligned. The call synchronizes `stream` (it
+ * returns the result on the host).
+ * Errors: VNM_ERR_INVALID_ARG (pointers, ld_w, pattern, workspace size),
+ * VNM_ERR_NONFINITE (W holds Inf or NaN), VNM_ERR_CUDA.
+ */
+vnm_status vnm_energy(vnm_matrix A, const void* W, int64_t ld_w, vnm_pattern pattern, void* workspace,
+                      size_t workspace_bytes, uint64_t kept_units[2], uint64_t total_units[2], double* energy,
+                      vnm_stream_t stream);
+
+/* Bytes of device workspace vnm_energy needs for the handle's shape (host only). */
+vnm_status vnm_energy_workspace_size(vnm_matrix A, size_t* bytes);
 
 /*
  * Fused dense GEMM + prune-and-encode: W = X . Y^T, then vnm_compress(W)

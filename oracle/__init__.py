@@ -137,6 +137,48 @@ def gemm_compress(X: np.ndarray, Y: np.ndarray, V: int, M: int, L: Optional[ctyp
     return W, compress(W, V, M, L)
 
 
+PATTERN_VNM, PATTERN_UNSTRUCTURED, PATTERN_VECTORWISE = 0, 1, 2
+
+
+def _units(h16: np.ndarray) -> np.ndarray:
+    """|w| of fp16 values in units of 2^-24, as exact integers (uint64): the
+    fp16 -> fp64 conversion is exact and every |fp16| is a multiple of 2^-24
+    below 2^41."""
+    return (np.abs(np.asarray(h16, dtype=np.float16).astype(np.float64)) * 2.0 ** 24).astype(np.uint64)
+
+
+def energy(W: np.ndarray, V: int, M: int, pattern: int, L: Optional[ctypes.CDLL] = None):
+    """Energy (magnitude preservation) of pruning fp16 W at density 2/M.
+
+    Restates "VENOM", section 5 (Figure 11): the sum of the kept |w| over the
+    sum of all |w|. ``pattern``: PATTERN_VNM keeps the values of
+    :func:`compress` (V:N:M); PATTERN_UNSTRUCTURED the R*2K/M largest |w|;
+    PATTERN_VECTORWISE, per panel of V rows, the 2K/M columns of largest L1
+    norm over the panel (vectors of V x 1). Returns ``(energy, kept, total)``
+    with kept and total exact Python integers in units of 2^-24 (energy 1.0
+    for an all-zero W).
+    """
+    W = np.ascontiguousarray(W, dtype=np.float16)
+    R, K = W.shape
+    u = _units(W)
+    total = int(u.sum(dtype=np.uint64)) if u.size else 0
+    k = 2 * (K // M)
+    if pattern == PATTERN_VNM:
+        values = compress(W, V, M, L)[0]
+        kept = int(_units(values.view(np.float16)).sum(dtype=np.uint64)) if values.size else 0
+    elif pattern == PATTERN_UNSTRUCTURED:
+        flat = np.sort(u.ravel())[::-1]
+        kept = sum(int(x) for x in flat[:R * k])
+    elif pattern == PATTERN_VECTORWISE:
+        kept = 0
+        for i in range(R // V):
+            col = u[i * V:(i + 1) * V].sum(axis=0, dtype=np.uint64)  # exact: below 2^53
+            kept += sum(int(x) for x in np.sort(col)[::-1][:k])
+    else:
+        raise ValueError(f"no pattern {pattern}")
+    return (1.0 if total == 0 else kept / total), kept, total
+
+
 def decompress(values: np.ndarray, meta: np.ndarray, colidx: np.ndarray, R: int, K: int, V: int,
                M: int, L: Optional[ctypes.CDLL] = None) -> np.ndarray:
     """Dense fp16 R x K from the compressed arrays (pruned positions +0.0)."""

@@ -9,6 +9,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "vnm_internal.h"
 #include "vnm_testing.h"
@@ -340,6 +341,68 @@ vnm_status vnm_decompress(vnm_matrix A, void* W_out, int64_t ld_w, vnm_stream_t 
     return vnm::launch_decompress(*A, W_out, ld_w, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? VNM_OK
                : VNM_ERR_CUDA;
+}
+
+vnm_status vnm_energy_workspace_size(vnm_matrix A, size_t* bytes) {
+    if (!valid_handle(A) || bytes == nullptr) return VNM_ERR_INVALID_ARG;
+    *bytes = vnm::energy_workspace_bytes(A->R, A->K, A->V);
+    return VNM_OK;
+}
+
+vnm_status vnm_energy(vnm_matrix A, const void* W, int64_t ld_w, vnm_pattern pattern, void* workspace,
+                      size_t workspace_bytes, uint64_t kept_units[2], uint64_t total_units[2], double* energy,
+                      vnm_stream_t stream) {
+    if (!valid_handle(A)) return VNM_ERR_INVALID_ARG;
+    if (pattern != VNM_PATTERN_VNM && pattern != VNM_PATTERN_UNSTRUCTURED && pattern != VNM_PATTERN_VECTORWISE)
+        return VNM_ERR_INVALID_ARG;
+    if (ld_w < std::max<int64_t>(A->K, 1)) return VNM_ERR_INVALID_ARG;
+    auto put = [&](unsigned __int128 kept, unsigned __int128 total) {
+        if (kept_units) {
+            kept_units[0] = static_cast<uint64_t>(kept);
+            kept_units[1] = static_cast<uint64_t>(kept >> 64);
+        }
+        if (total_units) {
+            total_units[0] = static_cast<uint64_t>(total);
+            total_units[1] = static_cast<uint64_t>(total >> 64);
+        }
+        if (energy) *energy = total == 0 ? 1.0 : static_cast<double>(static_cast<long double>(kept) /
+                                                                     static_cast<long double>(total));
+    };
+    if (A->R == 0 || A->K == 0) {
+        put(0, 0);
+        return VNM_OK;
+    }
+    if (W == nullptr || !aligned(W, 2)) return VNM_ERR_INVALID_ARG;
+    if (workspace == nullptr || !aligned(workspace, 16) ||
+        workspace_bytes < vnm::energy_workspace_bytes(A->R, A->K, A->V))
+        return VNM_ERR_INVALID_ARG;
+    vnm_status st = check_device(A);
+    if (st != VNM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    int n_total = 0, n_kept = 0;
+    if (vnm::launch_energy(*A, W, ld_w, static_cast<int>(pattern), workspace, A->sm_count, &n_total, &n_kept, s) !=
+        cudaSuccess)
+        return VNM_ERR_CUDA;
+    std::vector<uint64_t> host(2 * (vnm::kEnergyKeptPair + std::max(n_kept, 1)));
+    int flags = 0;
+    const uint8_t* ws = static_cast<const uint8_t*>(workspace);
+    if (cudaMemcpyAsync(&flags, ws, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemcpyAsync(host.data(), ws + 256, sizeof(uint64_t) * 2 * n_total, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(host.data() + 2 * vnm::kEnergyKeptPair, ws + 256 + 16 * vnm::kEnergyKeptPair,
+                        sizeof(uint64_t) * 2 * n_kept, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return VNM_ERR_CUDA;
+    if (flags) return VNM_ERR_NONFINITE;
+    unsigned __int128 total = 0, kept = 0;
+    for (int i = 0; i < n_total; ++i)
+        total += (static_cast<unsigned __int128>(host[2 * i + 1]) << 64) | host[2 * i];
+    for (int i = 0; i < n_kept; ++i) {
+        const size_t j = 2 * (vnm::kEnergyKeptPair + i);
+        kept += (static_cast<unsigned __int128>(host[j + 1]) << 64) | host[j];
+    }
+    put(kept, total);
+    return VNM_OK;
 }
 
 vnm_status vnm_gemm_compress(vnm_matrix A, const void* X, int64_t ld_x, const void* Y, int64_t ld_y, int64_t D,

@@ -143,6 +143,15 @@ bool gemm_compress_shape_ok(int V, int M);
 cudaError_t launch_gemm_compress(const vnm_matrix_s& A, const CUtensorMap& tm_x, const CUtensorMap& tm_y, int64_t D,
                                  void* w_out, int64_t ld_w, cudaStream_t stream);
 
+// Energy of a pruning pattern (a vnm_pattern): partial sums in units of
+// 2^-24 as pairs of uint64 (low, high) in the workspace, from byte 256 on:
+// n_total pairs of sum |W|, then (from pair kEnergyKeptPair) n_kept pairs of
+// the kept |w|; word 0 of the workspace is set when W holds Inf or NaN.
+constexpr int kEnergyKeptPair = 1024;
+size_t energy_workspace_bytes(int64_t R, int64_t K, int V);
+cudaError_t launch_energy(const vnm_matrix_s& A, const void* W, int64_t ld_w, int pattern, void* workspace,
+                          int sm_count, int* n_total_partials, int* n_kept_partials, cudaStream_t stream);
+
 // Pipeline stages the tensor-core kernel is built with for a tile (0: no such tile).
 int tc_default_stages(int tile_m, int tile_n, bool gather);
 

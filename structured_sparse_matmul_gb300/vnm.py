@@ -62,6 +62,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.vnm_compress.argtypes = [p, p, i64, p]
     L.vnm_decompress.argtypes = [p, p, i64, p]
     L.vnm_gemm_compress.argtypes = [p, p, i64, p, i64, i64, p, i64, p]
+    L.vnm_energy.argtypes = [p, p, i64, ctypes.c_int, p, sz, p, p, p, p]
+    L.vnm_energy_workspace_size.argtypes = [p, p]
     L.vnm_spmm.argtypes = [p, p, i64, i64, p, i64, ctypes.c_int, p, sz, p]
     L.vnm_spmm_workspace_size.argtypes = [p, i64, p]
     L.vnm_spmm_plan_query.argtypes = [p, p, i64, i64, ctypes.c_int, sz, ctypes.POINTER(vnm_spmm_plan)]
@@ -204,6 +206,33 @@ def vnm_gemm_compress(A: VnmMatrix, X: torch.Tensor, Y: torch.Tensor, W_out: Opt
     ld_y = _rowmajor(Y, "Y") if D > 0 else 1
     _check(lib().vnm_gemm_compress(A.handle, X.data_ptr() or None, ld_x, Y.data_ptr() or None, ld_y, D, w_ptr, ld_w,
                                    _stream_ptr(stream)), "vnm_gemm_compress")
+
+
+VNM_PATTERN_VNM, VNM_PATTERN_UNSTRUCTURED, VNM_PATTERN_VECTORWISE = 0, 1, 2
+
+
+def vnm_energy_workspace_size(A: VnmMatrix) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().vnm_energy_workspace_size(A.handle, ctypes.byref(n)), "vnm_energy_workspace_size")
+    return int(n.value)
+
+
+def vnm_energy(A: VnmMatrix, W: torch.Tensor, pattern: int, workspace: Optional[torch.Tensor] = None,
+               stream=None) -> Tuple[float, int, int]:
+    """Energy of pruning W (R x K fp16) with `pattern` at density 2/M:
+    (energy, kept units, total units), the sums exact in units of 2^-24.
+    VNM_PATTERN_VNM reads A, which must hold vnm_compress(A, W)."""
+    if W.dtype != torch.float16 or not W.is_cuda or tuple(W.shape) != (A.R, A.K):
+        raise ValueError("W must be a CUDA fp16 tensor of shape (R, K)")
+    if workspace is None:
+        workspace = torch.empty(vnm_energy_workspace_size(A), dtype=torch.uint8, device=W.device)
+    kept = (ctypes.c_uint64 * 2)()
+    total = (ctypes.c_uint64 * 2)()
+    e = ctypes.c_double(0.0)
+    _check(lib().vnm_energy(A.handle, W.data_ptr() or None, _rowmajor(W, "W"), int(pattern), workspace.data_ptr(),
+                            workspace.numel() * workspace.element_size(), kept, total, ctypes.byref(e),
+                            _stream_ptr(stream)), "vnm_energy")
+    return float(e.value), int(kept[0]) | (int(kept[1]) << 64), int(total[0]) | (int(total[1]) << 64)
 
 
 def _c_type(C: torch.Tensor) -> int:

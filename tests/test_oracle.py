@@ -354,11 +354,52 @@ def check_gemm_compress_rounding(L):
     assert e.value.code == oracle.NONFINITE
 
 
+def check_energy_worked_example(L):
+    """The 2 x 8 matrix of the 2:4 notes' worked example at density 1/2: V:N:M
+    (V = 2, 2:4) keeps the printed values 0.9 -0.4 0.7 -1.2 / 0.3 0.5 -0.8 0.6;
+    unstructured keeps the 8 largest magnitudes 1.2 0.9 0.8 0.7 0.6 0.5 0.4 0.4;
+    vector-wise (one panel of both rows) keeps the 4 columns of largest L1
+    norm, columns 7, 0, 5, 2 (norms 1.8, 1.1, 1.1, 0.9)."""
+    fx = read_fixture(os.path.join(GOLDEN, "worked_2x8.txt"))
+    W = np.array([_floats(fx["dense_row0"]), _floats(fx["dense_row1"])], dtype=np.float16)
+    h = lambda xs: sum(abs(float(np.float16(x))) for x in xs)  # noqa: E731
+    total = h(_floats(fx["dense_row0"]) + _floats(fx["dense_row1"]))
+    want = {oracle.PATTERN_VNM: h([0.9, -0.4, 0.7, -1.2, 0.3, 0.5, -0.8, 0.6]),
+            oracle.PATTERN_UNSTRUCTURED: h([1.2, 0.9, 0.8, 0.7, 0.6, 0.5, 0.4, 0.4]),
+            oracle.PATTERN_VECTORWISE: h([1.2, 0.6, 0.9, 0.2, 0.7, 0.4, -0.4, 0.5])}
+    for pattern, kept in want.items():
+        e, k_units, t_units = oracle.energy(W, 2, 4, pattern, L)
+        assert k_units == round(kept * 2 ** 24) and t_units == round(total * 2 ** 24), (pattern, k_units, t_units)
+        assert abs(e - kept / total) < 1e-15
+
+
+def check_energy_invariants(L):
+    """Equal magnitudes keep exactly the density 2/M; on any matrix the
+    unstructured selection (the ideal) keeps at least as much as V:N:M and
+    vector-wise; V:N:M with V = 1 and M = 4 equals the sum of the two largest
+    |w| of every group of 4 (brute force)."""
+    rng = np.random.default_rng(11)
+    R, K = 64, 128
+    ones = (rng.choice([-1.0, 1.0], (R, K))).astype(np.float16)
+    for M in (4, 8, 16):
+        for pattern in (oracle.PATTERN_VNM, oracle.PATTERN_UNSTRUCTURED, oracle.PATTERN_VECTORWISE):
+            e, kept, total = oracle.energy(ones, 16, M, pattern, L)
+            assert kept * M == total * 2, (M, pattern)
+    W = (rng.standard_normal((R, K)) * 0.02).astype(np.float16)
+    for V, M in ((16, 8), (64, 16), (1, 4)):
+        ideal = oracle.energy(W, V, M, oracle.PATTERN_UNSTRUCTURED, L)[1]
+        assert ideal >= oracle.energy(W, V, M, oracle.PATTERN_VNM, L)[1]
+        assert ideal >= oracle.energy(W, V, M, oracle.PATTERN_VECTORWISE, L)[1]
+    groups = np.abs(W.astype(np.float64)).reshape(R, K // 4, 4)
+    brute = np.sort(groups, axis=2)[:, :, 2:].sum()
+    assert oracle.energy(W, 1, 4, oracle.PATTERN_VNM, L)[1] == round(brute * 2 ** 24)
+
+
 PINS = [check_worked_example, check_worked_local_index, check_worked_product,
         check_storage_arithmetic, check_brute_force_ties, check_brute_force_subnormals,
         check_brute_force_normal, check_invariants_and_round_trip, check_spmm_against_numpy,
         check_fig3_fixture, check_gemm_compress_identity, check_gemm_compress_rank1,
-        check_gemm_compress_rounding]
+        check_gemm_compress_rounding, check_energy_worked_example, check_energy_invariants]
 
 
 # ----------------------------------------------------------------------------
