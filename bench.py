@@ -470,6 +470,87 @@ def measure_gemm_compress(dev, peaks, launches: int):
             "l2_eviction": "rotating input sets of more than twice the L2 in each graph", "cases": out}
 
 
+# The Linear-layer form Y = act(X . A^T + bias) on the transformer-encoder
+# linear shapes of workload 3 (8192 tokens), V = 128.
+LINEAR_CASES = [
+    # R (out features), K (in features), T (tokens), V, M
+    (4096, 1024, 8192, 128, 4),
+    (4096, 1024, 8192, 128, 8),
+    (1024, 4096, 8192, 128, 4),
+    (1024, 4096, 8192, 128, 16),
+]
+
+
+def measure_linear(dev, peaks, launches: int):
+    """vnm_linear with and without a bias + GELU epilogue, against what the
+    SpMM alone needs for the same layer (X transposed, vnm_spmm, C transposed
+    back) and dense torch.nn.functional.linear + GELU (context). Timed like
+    the per-workload table; the roofline of the plain vnm_linear launch is the
+    SpMM's (effective flops, bytes A + X + Y)."""
+    import torch
+    import torch.nn.functional as F
+
+    from structured_sparse_matmul_gb300 import vnm
+
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20))
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5151)
+    out = {}
+    for (R, K, T, V, M) in LINEAR_CASES:
+        vb, mb, cb = vnm.vnm_sizes(R, K, V, M)
+        set_bytes = vb + mb + cb + 2 * T * K + 2 * T * R
+        n_sets = max(2, math.ceil(2 * l2 / set_bytes) + 1)
+        Wd = (torch.randn(R, K, device=dev, generator=gen) * 0.02).half()
+        bias = (torch.randn(R, device=dev, generator=gen) * 0.5).half()
+        A = vnm.vnm_matrix_alloc(R, K, V, M, dev)
+        vnm.vnm_compress(A, Wd)
+        Wp = torch.empty_like(Wd)
+        vnm.vnm_decompress(A, Wp)  # the pruned weight, dense (for the dense context line)
+        sets = [{"X": torch.randn(T, K, device=dev, generator=gen).half(),
+                 "Y": torch.empty(T, R, dtype=torch.float16, device=dev)} for _ in range(n_sets)]
+        ws = torch.empty(max(1, vnm.vnm_linear_workspace_size(A, T)), dtype=torch.uint8, device=dev)
+        Xt = torch.empty(K, T, dtype=torch.float16, device=dev)
+        Ct = torch.empty(R, T, dtype=torch.float16, device=dev)
+        sws = vnm.workspace_for(A, T, dev)
+
+        def lin(i, st, b=None, act=vnm.VNM_ACT_NONE):
+            x = sets[i % n_sets]
+            vnm.vnm_linear(A, x["X"], x["Y"], b, act, workspace=ws, stream=st)
+
+        def via_spmm(i, st):
+            x = sets[i % n_sets]
+            Xt.copy_(x["X"].t())
+            vnm.vnm_spmm(A, Xt, Ct, workspace=sws, stream=st)
+            x["Y"].copy_(Ct.t())
+
+        def dense(i, st):
+            x = sets[i % n_sets]
+            F.gelu(F.linear(x["X"], Wp, bias))
+
+        t_plain = _time_graph(dev, lin, launches)
+        t_epi = _time_graph(dev, lambda i, st: lin(i, st, bias, vnm.VNM_ACT_GELU), launches)
+        t_via = _time_graph(dev, via_spmm, launches)
+        try:
+            t_dense = _time_graph(dev, dense, launches)
+        except Exception as exc:  # context only
+            t_dense = f"unavailable: {exc}"
+        st_ = vnm.vnm_get_status(A)
+        if st_ != vnm.VNM_OK:
+            raise RuntimeError(f"kernel status {vnm.status_string(st_)} in vnm_linear {R}x{K}x{T}")
+        eff = 2.0 * R * T * K * 2 / M
+        byts = vb + mb + cb + 2 * T * K + 2 * T * R
+        t_roof = max(eff / (peaks["bf16_tflops"] * 1e12), byts / (peaks["hbm_gbs"] * 1e9)) * 1e6
+        out[f"Y[{T}x{R}] = X[{T}x{K}] . A^T, {V}:2:{M}"] = {
+            "vnm_linear_us": t_plain, "vnm_linear_bias_gelu_us": t_epi,
+            "transpose_spmm_transpose_us": t_via, "dense_linear_gelu_us": t_dense,
+            "roofline": {"t_roof_us": t_roof, "frac": t_roof / t_plain}, "sets": n_sets}
+        del sets, Wd, Wp, Xt, Ct, ws
+        torch.cuda.empty_cache()
+    return {"launches_per_graph": launches, "replays": 7, "statistic": "median",
+            "inputs": "torch seeded device generator, W ~ N(0, 0.02), X ~ N(0, 1), bias ~ N(0, 0.25)",
+            "l2_eviction": "rotating X / Y sets of more than twice the L2 in each graph", "cases": out}
+
+
 def measure_energy(dev):
     """Energy (magnitude preservation) of the three selection policies at the
     V:N:M densities 2/M on a synthetic N(0, 0.02) weight of the 768 x 768
@@ -936,6 +1017,7 @@ def main():
         per_config = measure_per_config(dev, peaks, max(2, args.per_config_launches))
         per_config["gemm_compress"] = measure_gemm_compress(dev, peaks, max(2, args.per_config_launches))
         per_config["energy"] = measure_energy(dev)
+        per_config["linear"] = measure_linear(dev, peaks, max(2, args.per_config_launches))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -77,6 +77,13 @@ typedef enum vnm_path {
                           distributed shared memory); larger N, one warp per row */
 } vnm_path;
 
+/* Activations of the Linear-layer form (vnm_linear). */
+typedef enum vnm_activation {
+    VNM_ACT_NONE = 0,
+    VNM_ACT_RELU = 1, /* max(x, 0) */
+    VNM_ACT_GELU = 2  /* x * (1 + erf(x / sqrt 2)) / 2 */
+} vnm_activation;
+
 /* Selection policies of vnm_energy (all at the V:N:M density 2/M). */
 typedef enum vnm_pattern {
     VNM_PATTERN_VNM = 0,          /* the kept values of the compressed matrix */
@@ -174,6 +181,31 @@ vnm_status vnm_compress(vnm_matrix A, const void* W, int64_t ld_w, vnm_stream_t 
  * Errors: VNM_ERR_INVALID_ARG.
  */
 vnm_status vnm_decompress(vnm_matrix A, void* W_out, int64_t ld_w, vnm_stream_t stream);
+
+/*
+ * The Linear-layer form of the product: Y = act(X . A^T + bias), as the
+ * transformer layers of VENOM section 7 apply a pruned weight A (R x K,
+ * output features x input features) to activations X (T tokens x K).
+ * X: fp16 T x K row-major (ld_x >= K); Y: T x R row-major (ld_y >= R), fp16
+ * (one rounding, RNE) or fp32; bias: fp16 [R] or NULL; act: a
+ * vnm_activation, applied in fp32 after the bias. fp32 accumulation.
+ * It is the SpMM C = A . X^T with C written transposed into Y and the bias
+ * and activation applied as C is written (one kernel where the tensor cores
+ * read X in place: M == 4, and M == 8 re-encoded as 2:4; a split K adds the
+ * reduction kernel; the gather of M > 8, or an X whose rows are not 16-byte
+ * aligned, first transposes X into the workspace).
+ * workspace: device memory, 256-byte aligned, of at least
+ * vnm_linear_workspace_size bytes for the largest split (a smaller one
+ * lowers the split; it must still hold X^T when the path needs it).
+ * Errors: VNM_ERR_INVALID_ARG (pointers, leading dimensions, act, y_type,
+ * workspace too small), VNM_ERR_CUDA.
+ */
+vnm_status vnm_linear(vnm_matrix A, const void* X, int64_t ld_x, int64_t T, const void* bias, vnm_activation act,
+                      void* Y, int64_t ld_y, vnm_dtype y_type, void* workspace, size_t workspace_bytes,
+                      vnm_stream_t stream);
+
+/* Bytes of workspace vnm_linear may need for T tokens (host only). */
+vnm_status vnm_linear_workspace_size(vnm_matrix A, int64_t T, size_t* bytes);
 
 /*
  * Energy (magnitude preservation) of pruning the dense fp16 matrix W (R x K,

@@ -137,6 +137,28 @@ def gemm_compress(X: np.ndarray, Y: np.ndarray, V: int, M: int, L: Optional[ctyp
     return W, compress(W, V, M, L)
 
 
+ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
+
+
+def linear(values: np.ndarray, meta: np.ndarray, colidx: np.ndarray, R: int, K: int, V: int, M: int,
+           X: np.ndarray, bias: Optional[np.ndarray] = None, act: int = ACT_NONE) -> np.ndarray:
+    """Y = act(X . A^T + bias) in fp64 (the Linear-layer form of the SpMM, as
+    "VENOM" section 7's transformer layers apply a pruned weight): the fp64
+    :func:`spmm` of A by X^T, transposed, plus the fp16 bias, then ReLU
+    max(y, 0) or GELU y * (1 + erf(y / sqrt 2)) / 2. X is fp16 T x K."""
+    import math
+    X = np.asarray(X, dtype=np.float16)
+    C = spmm(values, meta, colidx, R, K, V, M, np.ascontiguousarray(X.T), acc="f64")  # R x T
+    Y = C.T.copy()
+    if bias is not None:
+        Y += np.asarray(bias, dtype=np.float16).astype(np.float64)[None, :]
+    if act == ACT_RELU:
+        Y = np.maximum(Y, 0.0)
+    elif act == ACT_GELU:
+        Y = Y * (1.0 + np.vectorize(math.erf)(Y / math.sqrt(2.0))) / 2.0
+    return Y
+
+
 PATTERN_VNM, PATTERN_UNSTRUCTURED, PATTERN_VECTORWISE = 0, 1, 2
 
 

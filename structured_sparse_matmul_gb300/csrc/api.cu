@@ -193,16 +193,23 @@ vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void
     return VNM_OK;
 }
 
-vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_t ld_b, int64_t N, void* C,
-                    int64_t ld_c, vnm_dtype c_type, void* workspace, cudaStream_t stream, int skip_stage = -1) {
-    const bool c_f32 = c_type == VNM_F32;
+// The B operand of a product: element (k, n) at ptr + k * bk + n * bn.
+// Row-major B (vnm_spmm): bk = ld_b, bn = 1. The Linear-layer form reads X
+// (N x K, row-major) as a K-major B: bk = 1, bn = ld_x.
+struct BOperand {
+    const void* ptr;
+    int64_t bk, bn;
+    bool kmajor() const { return bk == 1 && bn != 1; }
+};
+
+vnm_status run_product(vnm_matrix A, const vnm_spmm_plan& pl, const BOperand& B, int64_t N, const vnm::OutSpec& out,
+                       void* workspace, cudaStream_t stream, int skip_stage = -1) {
     cudaError_t e = cudaSuccess;
     if (pl.path == VNM_PATH_SIMT) {
         if (N <= 8)
-            e = vnm::launch_spmm_stream(*A, B, ld_b, N, C, ld_c, c_f32, effective_stream_splits(*A, pl.splits),
-                                        stream);
+            e = vnm::launch_spmm_stream(*A, B.ptr, B.bk, B.bn, N, out, effective_stream_splits(*A, pl.splits), stream);
         else
-            e = vnm::launch_spmm_simt(*A, B, ld_b, N, C, ld_c, c_f32, stream);
+            e = vnm::launch_spmm_simt(*A, B.ptr, B.bk, B.bn, N, out, stream);
     } else if (pl.path == VNM_PATH_TC) {
         vnm::TcLaunch L;
         std::memset(&L, 0, sizeof(L));
@@ -210,6 +217,8 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         L.tile_n = pl.tile_n;
         L.mode = A->M == 4 ? vnm::kTcTiled : pl.lift ? vnm::kTcLift : vnm::kTcGather;
         const bool gather = L.mode == vnm::kTcGather;
+        L.b_kmajor = B.kmajor();
+        if (L.b_kmajor && gather) return VNM_ERR_INTERNAL;
         L.stages = vnm::tc_default_stages(pl.tile_m, pl.tile_n, gather);
         L.splits = effective_splits(*A, pl.splits, pl.lift != 0);
         L.sm_count = A->sm_count;
@@ -218,18 +227,30 @@ vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_
         // A values: one stage (64 values per row, 4 MMA k-steps) per box, 128B swizzle
         bool ok = encode_2d(&L.tm_a, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, A->values, vpr, A->R, vpr * 2, 64,
                             static_cast<uint32_t>(pl.tile_m), CU_TENSOR_MAP_SWIZZLE_128B);
-        // B tiles by TMA (M == 4): 64-column atoms, or exactly tile_n columns with the
-        // matching swizzle for 16- and 32-column tiles
-        const bool narrow = vnm::tc_narrow_b(pl.tile_n, gather);
-        ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B, N, A->K, ld_b * 2,
-                             narrow ? static_cast<uint32_t>(pl.tile_n) : 64,
-                             gather ? 1 : static_cast<uint32_t>(vnm::kTcStageK),
-                             !narrow ? CU_TENSOR_MAP_SWIZZLE_128B
-                                     : pl.tile_n == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
+        if (L.b_kmajor) {
+            // K-major B: boxes of 64 K (128 bytes) x tile_n rows, 128B swizzle
+            ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B.ptr, A->K, N, B.bn * 2, 64,
+                                 static_cast<uint32_t>(pl.tile_n), CU_TENSOR_MAP_SWIZZLE_128B);
+        } else {
+            // B tiles by TMA (M == 4, lift): 64-column atoms, or exactly tile_n columns with the
+            // matching swizzle for 16- and 32-column tiles; the gather reads B itself
+            const bool narrow = vnm::tc_narrow_b(pl.tile_n, gather);
+            ok = ok && encode_2d(&L.tm_b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, B.ptr, N, A->K, B.bk * 2,
+                                 narrow ? static_cast<uint32_t>(pl.tile_n) : 64,
+                                 gather ? 1 : static_cast<uint32_t>(vnm::kTcStageK),
+                                 !narrow ? CU_TENSOR_MAP_SWIZZLE_128B
+                                         : pl.tile_n == 16 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B);
+        }
         if (!ok) return VNM_ERR_CUDA;
-        e = vnm::launch_spmm_tc(*A, L, B, ld_b, N, C, ld_c, c_f32, static_cast<float*>(workspace), stream);
+        e = vnm::launch_spmm_tc(*A, L, B.ptr, B.bk, N, out, static_cast<float*>(workspace), stream);
     }
     return e == cudaSuccess ? VNM_OK : VNM_ERR_CUDA;
+}
+
+vnm_status run_spmm(vnm_matrix A, const vnm_spmm_plan& pl, const void* B, int64_t ld_b, int64_t N, void* C,
+                    int64_t ld_c, vnm_dtype c_type, void* workspace, cudaStream_t stream, int skip_stage = -1) {
+    return run_product(A, pl, BOperand{B, ld_b, 1}, N, vnm::out_rowmajor(C, ld_c, c_type == VNM_F32), workspace,
+                       stream, skip_stage);
 }
 
 vnm_status check_spmm_args(vnm_matrix A, const void* B, int64_t ld_b, int64_t N, const void* C, int64_t ld_c,
@@ -341,6 +362,96 @@ vnm_status vnm_decompress(vnm_matrix A, void* W_out, int64_t ld_w, vnm_stream_t 
     return vnm::launch_decompress(*A, W_out, ld_w, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? VNM_OK
                : VNM_ERR_CUDA;
+}
+
+// ---- the Linear-layer form Y = act(X . A^T + bias) ----
+
+// How vnm_linear runs a product: the plan, whether X is first transposed into
+// the workspace (the gather needs a row-major B), and the workspace layout.
+struct LinearPlan {
+    vnm_spmm_plan pl;
+    bool transpose;       // X^T (K x T, leading dimension ldt) at the workspace start
+    int64_t ldt;
+    size_t t_bytes;       // bytes of X^T, 256-byte aligned
+    size_t bytes;         // total workspace: X^T, then the split-K partials
+};
+
+LinearPlan make_linear_plan(const vnm_matrix_s& A, bool x_aligned, int64_t T, size_t workspace_bytes) {
+    LinearPlan lp;
+    std::memset(&lp, 0, sizeof(lp));
+    lp.ldt = ((std::max<int64_t>(T, 1) + 7) / 8) * 8;
+    // the plan vnm_spmm makes for a row-major B of T columns (alignment assumed)
+    const void* aligned_b = reinterpret_cast<const void*>(uintptr_t(256));
+    lp.pl = make_plan(A, aligned_b, lp.ldt, T, SIZE_MAX / 2);
+    if (lp.pl.path == VNM_PATH_TC) {
+        // K-major B is read in place by TMA where the B tiles are not gathered: M == 4, or
+        // M == 8 re-encoded (lift); the gather needs X^T in the workspace, as does an X that
+        // TMA cannot read (not 16-byte aligned rows)
+        if (A.M == 8 && lift_ok(A) && !lp.pl.lift) {
+            lp.pl.lift = 1;
+            lp.pl.tile_m = 128;
+            lp.pl.stages = vnm::tc_default_stages(128, lp.pl.tile_n, false);
+            const int64_t tiles = ceil_div(A.R, 128) * ceil_div(T, lp.pl.tile_n);
+            const int64_t num_kt = vnm::tc_k_units(A.K, A.M, true);
+            lp.pl.splits = tiles < A.sm_count
+                               ? static_cast<int32_t>(std::min<int64_t>(num_kt, std::max<int64_t>(1, A.sm_count / tiles)))
+                               : 1;
+        }
+        const bool gather = A.M > 4 && !lp.pl.lift;
+        lp.transpose = gather || !x_aligned;
+    }
+    if (lp.transpose) lp.t_bytes = (static_cast<size_t>(A.K) * lp.ldt * 2 + 255) & ~static_cast<size_t>(255);
+    // split K only within the workspace given
+    if (lp.pl.path == VNM_PATH_TC && lp.pl.splits > 1) {
+        const size_t per_split = static_cast<size_t>(A.R) * T * sizeof(float);
+        const size_t room = workspace_bytes > lp.t_bytes ? workspace_bytes - lp.t_bytes : 0;
+        lp.pl.splits = static_cast<int32_t>(std::max<int64_t>(
+            1, std::min<int64_t>(lp.pl.splits, static_cast<int64_t>(room / std::max<size_t>(per_split, 1)))));
+    }
+    const int s = lp.pl.path == VNM_PATH_TC ? effective_splits(A, lp.pl.splits, lp.pl.lift != 0) : 1;
+    lp.bytes = lp.t_bytes + (s > 1 ? static_cast<size_t>(s) * A.R * T * sizeof(float) : 0);
+    return lp;
+}
+
+vnm_status vnm_linear_workspace_size(vnm_matrix A, int64_t T, size_t* bytes) {
+    if (!valid_handle(A) || bytes == nullptr || T < 0) return VNM_ERR_INVALID_ARG;
+    // the largest need: an unaligned X (transposed) and an unlimited split
+    *bytes = make_linear_plan(*A, false, T, SIZE_MAX / 2).bytes;
+    return VNM_OK;
+}
+
+vnm_status vnm_linear(vnm_matrix A, const void* X, int64_t ld_x, int64_t T, const void* bias, vnm_activation act,
+                      void* Y, int64_t ld_y, vnm_dtype y_type, void* workspace, size_t workspace_bytes,
+                      vnm_stream_t stream) {
+    if (!valid_handle(A)) return VNM_ERR_INVALID_ARG;
+    if (y_type != VNM_F16 && y_type != VNM_F32) return VNM_ERR_INVALID_ARG;
+    if (act != VNM_ACT_NONE && act != VNM_ACT_RELU && act != VNM_ACT_GELU) return VNM_ERR_INVALID_ARG;
+    if (T < 0 || T > (int64_t(1) << 31) || ld_x < std::max<int64_t>(A->K, 1) || ld_y < std::max<int64_t>(A->R, 1))
+        return VNM_ERR_INVALID_ARG;
+    if (A->R == 0 || T == 0) return VNM_OK;
+    if (Y == nullptr || !aligned(Y, y_type == VNM_F32 ? 4 : 2)) return VNM_ERR_INVALID_ARG;
+    if (bias != nullptr && !aligned(bias, 2)) return VNM_ERR_INVALID_ARG;
+    if (A->K > 0 && (X == nullptr || !aligned(X, 2))) return VNM_ERR_INVALID_ARG;
+    if (workspace == nullptr) workspace_bytes = 0;
+    vnm_status st = check_device(A);
+    if (st != VNM_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    // C = A . X^T is R x T; it is Y^T: element (r, t) at Y + t * ld_y + r
+    vnm::OutSpec out{Y, 1, ld_y, y_type == VNM_F32, static_cast<const __half*>(bias), static_cast<int>(act)};
+    if (A->K == 0) {
+        // Y = act(bias): the split-K reduction over no partial sums
+        return vnm::launch_splitk_reduce(nullptr, 0, A->R, T, out, s) == cudaSuccess ? VNM_OK : VNM_ERR_CUDA;
+    }
+    const bool x_aligned = aligned(X, 16) && ld_x % 8 == 0;
+    const LinearPlan lp = make_linear_plan(*A, x_aligned, T, workspace_bytes);
+    if (workspace_bytes < lp.bytes || (lp.bytes > 0 && !aligned(workspace, 256))) return VNM_ERR_INVALID_ARG;
+    BOperand B{X, 1, ld_x};
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    if (lp.transpose) {
+        if (vnm::launch_transpose_f16(X, ld_x, T, A->K, ws, lp.ldt, s) != cudaSuccess) return VNM_ERR_CUDA;
+        B = BOperand{ws, lp.ldt, 1};
+    }
+    return run_product(A, lp.pl, B, T, out, ws + lp.t_bytes, s);
 }
 
 vnm_status vnm_energy_workspace_size(vnm_matrix A, size_t* bytes) {

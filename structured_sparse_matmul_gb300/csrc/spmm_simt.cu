@@ -25,13 +25,11 @@ struct SimtArgs {
     const uint8_t* meta;     // [R][mpitch]
     const uint32_t* colidx;  // [R/V][nblk] words: 4 column bytes
     const __half* B;
-    int64_t ld_b;
-    void* C;
-    int64_t ld_c;
+    int64_t bk, bn;          // B element (k, n) at B + k * bk + n * bn
+    OutSpec out;
     int64_t R, N;
     int V, M;
     int64_t nblk, mpitch;
-    bool c_f32;
 };
 
 template <int NB>
@@ -41,13 +39,13 @@ __device__ __forceinline__ void accumulate_block(const SimtArgs& p, int64_t row,
     const int64_t k1 = j * p.M + ((sel >> (8u * (code >> 2))) & 0xFFu);
     const float a0 = __half2float(__ushort_as_half(static_cast<unsigned short>(vv & 0xFFFFu)));
     const float a1 = __half2float(__ushort_as_half(static_cast<unsigned short>(vv >> 16)));
-    const __half* b0 = p.B + k0 * p.ld_b + n0;
-    const __half* b1 = p.B + k1 * p.ld_b + n0;
+    const __half* b0 = p.B + k0 * p.bk + n0 * p.bn;
+    const __half* b1 = p.B + k1 * p.bk + n0 * p.bn;
 #pragma unroll
     for (int q = 0; q < NB; ++q) {
         if (n0 + q < p.N) {
-            acc[q] = fmaf(a0, __half2float(b0[q]), acc[q]);
-            acc[q] = fmaf(a1, __half2float(b1[q]), acc[q]);
+            acc[q] = fmaf(a0, __half2float(b0[q * p.bn]), acc[q]);
+            acc[q] = fmaf(a1, __half2float(b1[q * p.bn]), acc[q]);
         }
     }
 }
@@ -96,27 +94,23 @@ __global__ void __launch_bounds__(32 * kSimtWarps) spmm_simt_kernel(const SimtAr
 #pragma unroll
             for (int q = 1; q < NB; ++q)
                 if (lane == q) v = acc[q];
-            if (p.c_f32)
-                static_cast<float*>(p.C)[row * p.ld_c + n0 + lane] = v;
-            else
-                static_cast<__half*>(p.C)[row * p.ld_c + n0 + lane] = __float2half_rn(v);
+            out_store(p.out, row, n0 + lane, v);
         }
     }
 }
 
 // C[r][n] = sum over s = 0 .. splits-1 (in order) of partial[s][r][n].
-__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, int64_t R, int64_t N, void* C,
-                                     int64_t ld_c, bool c_f32) {
+__global__ void splitk_reduce_kernel(const float* __restrict__ partial, int splits, int64_t R, int64_t N,
+                                     const OutSpec out) {
     const int64_t total = R * N;
     for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < total;
          q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = q / N, n = q % N;
+        // a transposed C: consecutive threads take consecutive rows of one column
+        const int64_t r = out.ns == 1 ? q / N : q % R, n = out.ns == 1 ? q % N : q / R;
+        const int64_t e = r * N + n;
         float s = 0.f;
-        for (int z = 0; z < splits; ++z) s += __ldg(partial + z * total + q);
-        if (c_f32)
-            static_cast<float*>(C)[r * ld_c + n] = s;
-        else
-            static_cast<__half*>(C)[r * ld_c + n] = __float2half_rn(s);
+        for (int z = 0; z < splits; ++z) s += __ldg(partial + z * total + e);
+        out_store(out, r, n, s);
     }
 }
 
@@ -139,15 +133,13 @@ struct StreamArgs {
     const uint8_t* meta;     // [R][mpitch]
     const uint32_t* colidx;  // [R/V][nblk] words: 4 column bytes
     const __half* B;
-    int64_t ld_b;
-    void* C;
-    int64_t ld_c;
+    int64_t bk, bn;          // B element (k, n) at B + k * bk + n * bn
+    OutSpec out;
     int64_t R, N;
     int V, M;
     int64_t nblk, mpitch;
     int splits;
     int64_t bps;             // blocks per split
-    bool c_f32;
 };
 
 // acc + (float)a * (float)b for the fp16 a, b in the low 16 bits (exact
@@ -208,10 +200,10 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
                 const uint32_t w = __ldg(crow + j0 + jl);
                 // column-loc byte, clamped so that a corrupt array cannot address past K
                 const uint32_t cb = min((w >> (8 * slot)) & 0xFFu, static_cast<uint32_t>(p.M - 1));
-                const __half* src = p.B + ((j0 + jl) * p.M + cb) * p.ld_b;
+                const __half* src = p.B + ((j0 + jl) * p.M + cb) * p.bk;
                 __half* dst = Bc + jl * kStride + slot;
 #pragma unroll
-                for (int n = 0; n < NB; ++n) dst[4 * n] = n < p.N ? src[n] : __float2half_rn(0.f);
+                for (int n = 0; n < NB; ++n) dst[4 * n] = n < p.N ? src[n * p.bn] : __float2half_rn(0.f);
             }
             __syncthreads();
 #pragma unroll
@@ -235,13 +227,7 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
                 }
             }
         }
-        auto store = [&](int r, int n, float v) {
-            const int64_t row = i * p.V + r;
-            if (p.c_f32)
-                static_cast<float*>(p.C)[row * p.ld_c + n] = v;
-            else
-                static_cast<__half*>(p.C)[row * p.ld_c + n] = __float2half_rn(v);
-        };
+        auto store = [&](int r, int n, float v) { out_store(p.out, i * p.V + r, n, v); };
 #pragma unroll
         for (int t = 0; t < RW; ++t) {
             const int r = r0 + kStreamWarps * t;
@@ -319,23 +305,22 @@ cudaError_t launch_nb(const SimtArgs& p, cudaStream_t stream) {
 
 }  // namespace
 
-cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
-                             int64_t ld_c, bool c_f32, cudaStream_t stream) {
+cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t bk, int64_t bn, int64_t N,
+                             const OutSpec& out, cudaStream_t stream) {
     SimtArgs p;
     p.values = static_cast<const uint32_t*>(A.values);
     p.meta = static_cast<const uint8_t*>(A.meta);
     p.colidx = static_cast<const uint32_t*>(A.colidx);
     p.B = static_cast<const __half*>(B);
-    p.ld_b = ld_b;
-    p.C = C;
-    p.ld_c = ld_c;
+    p.bk = bk;
+    p.bn = bn;
+    p.out = out;
     p.R = A.R;
     p.N = N;
     p.V = A.V;
     p.M = A.M;
     p.nblk = A.K / A.M;
     p.mpitch = meta_pitch(A.K, A.M);
-    p.c_f32 = c_f32;
     if (A.R == 0 || N == 0) return cudaSuccess;
     if (N <= 1) return launch_nb<1>(p, stream);
     if (N <= 2) return launch_nb<2>(p, stream);
@@ -346,23 +331,22 @@ cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b,
 
 int stream_chunk_blocks(int V) { return V <= 32 ? 256 : V <= 64 ? 128 : 64; }
 
-cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
-                               int64_t ld_c, bool c_f32, int splits, cudaStream_t stream) {
+cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t bk, int64_t bn, int64_t N,
+                               const OutSpec& out, int splits, cudaStream_t stream) {
     StreamArgs p;
     p.values = static_cast<const uint32_t*>(A.values);
     p.meta = static_cast<const uint8_t*>(A.meta);
     p.colidx = static_cast<const uint32_t*>(A.colidx);
     p.B = static_cast<const __half*>(B);
-    p.ld_b = ld_b;
-    p.C = C;
-    p.ld_c = ld_c;
+    p.bk = bk;
+    p.bn = bn;
+    p.out = out;
     p.R = A.R;
     p.N = N;
     p.V = A.V;
     p.M = A.M;
     p.nblk = A.K / A.M;
     p.mpitch = meta_pitch(A.K, A.M);
-    p.c_f32 = c_f32;
     if (A.R == 0 || N == 0) return cudaSuccess;
     if (N > 8) return cudaErrorInvalidValue;
     // splits: 1, 2, 4 or 8 (a cluster), none of them empty
@@ -377,14 +361,38 @@ cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t ld_
     return launch_stream_nb<8>(p, stream);
 }
 
-cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, void* C, int64_t ld_c,
-                                 bool c_f32, cudaStream_t stream) {
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, const OutSpec& out,
+                                 cudaStream_t stream) {
     const int64_t total = R * N;
     if (total == 0) return cudaSuccess;
     const int threads = 256;
     const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, 148 * 16);
-    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(partial, splits, R, N, C, ld_c,
-                                                                              c_f32);
+    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(partial, splits, R, N, out);
+    return cudaGetLastError();
+}
+
+// 32 x 32 tiles through shared memory (padded row: no bank conflicts).
+__global__ void transpose_f16_kernel(const __half* __restrict__ src, int64_t ld_src, int64_t R, int64_t C,
+                                     __half* __restrict__ dst, int64_t ld_dst) {
+    __shared__ __half tile[32][33];
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 32, c0 = static_cast<int64_t>(blockIdx.x) * 32;
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int64_t r = r0 + i, c = c0 + threadIdx.x;
+        if (r < R && c < C) tile[i][threadIdx.x] = src[r * ld_src + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += blockDim.y) {
+        const int64_t c = c0 + i, r = r0 + threadIdx.x;
+        if (r < R && c < C) dst[c * ld_dst + r] = tile[threadIdx.x][i];
+    }
+}
+
+cudaError_t launch_transpose_f16(const void* src, int64_t ld_src, int64_t R, int64_t C, void* dst, int64_t ld_dst,
+                                 cudaStream_t stream) {
+    if (R == 0 || C == 0) return cudaSuccess;
+    const dim3 grid(static_cast<unsigned>((C + 31) / 32), static_cast<unsigned>((R + 31) / 32));
+    transpose_f16_kernel<<<grid, dim3(32, 8), 0, stream>>>(static_cast<const __half*>(src), ld_src, R, C,
+                                                          static_cast<__half*>(dst), ld_dst);
     return cudaGetLastError();
 }
 

@@ -98,8 +98,9 @@ struct TcArgs {
     const uint8_t* meta;     // [R][mpitch] m-indices, read by the m-index warps
     int64_t mpitch;
     int64_t ld_b;
-    void* C;
-    int64_t ld_c;
+    OutSpec out;             // C (strides, type, bias, activation)
+    int plain_out;           // C row-major with no bias or activation (the vector stores below)
+    int b_kmajor;            // B K-major (tiled and lift modes): TMA boxes of 64 K x BN rows
     float* partial;          // [splits][R][N] fp32, or null
     int64_t R, N;
     int V, M;
@@ -109,7 +110,6 @@ struct TcArgs {
     int n_tiles, m_tiles;    // tile grid (see tile_geom for the order)
     int group_m;             // row tiles per group of the tile order
     int total_tiles;
-    int c_f32;
     int vec_store;           // C row starts 16-byte aligned
     int vec32;               // C row starts 32-byte aligned (32-byte stores)
     int part_vec32;          // split-K partial rows 32-byte aligned
@@ -274,8 +274,12 @@ __device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g
             } else {
                 for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u] = __uint_as_float(v[u]);
             }
-        } else if (p.c_f32) {
-            float* dst = static_cast<float*>(p.C) + row * p.ld_c + col;
+        } else if (!p.plain_out) {
+            // a bias, an activation or a transposed C: element by element (with a transposed
+            // C the lanes' rows are consecutive, so each store of the warp is coalesced)
+            for (int u = 0; u < 16 && col + u < p.N; ++u) out_store(p.out, row, col + u, __uint_as_float(v[u]));
+        } else if (p.out.f32) {
+            float* dst = static_cast<float*>(p.out.C) + row * p.out.rs + col;
             if (full && p.vec32) {
                 st_global_v8(dst, v[0], v[1], v[2], v[3], v[4], v[5], v[6], v[7]);
                 st_global_v8(dst + 8, v[8], v[9], v[10], v[11], v[12], v[13], v[14], v[15]);
@@ -287,7 +291,7 @@ __device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g
                 for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u] = __uint_as_float(v[u]);
             }
         } else {
-            __half* dst = static_cast<__half*>(p.C) + row * p.ld_c + col;
+            __half* dst = static_cast<__half*>(p.out.C) + row * p.out.rs + col;
             uint32_t h[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -473,7 +477,11 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE
                         const uint32_t sB = sB0 + slot * Cfg::kBBytes;
                         const int32_t row = (g.kt0 + k) * kTcStageK;
                         mbar_arrive_expect_tx(fb, Cfg::kBBytes);
-                        if (Cfg::kNarrow) {
+                        if (p.b_kmajor) {
+                            // two boxes of 64 K x BN rows (128-byte rows, 128B swizzle)
+                            tma_load_2d(sB, &tm_b, row, static_cast<int32_t>(g.n0), fb);
+                            tma_load_2d(sB + BN * 128, &tm_b, row + 64, static_cast<int32_t>(g.n0), fb);
+                        } else if (Cfg::kNarrow) {
                             tma_load_2d(sB, &tm_b, static_cast<int32_t>(g.n0), row, fb);
                         } else {
 #pragma unroll
@@ -497,7 +505,9 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE
         // once and advanced by adding the (16-byte unit) offsets of the stage
         // and the k-step to their start-address field.
         if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc_f16_f32(TM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/true);
+            constexpr uint32_t idesc_n = make_idesc_f16_f32(TM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/true);
+            constexpr uint32_t idesc_k = make_idesc_f16_f32(TM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/false);
+            const uint32_t idesc = p.b_kmajor ? idesc_k : idesc_n;
             // A: K-major, 128B swizzle, 128-byte rows (64 values), 8-row groups 1024 bytes apart;
             // MMA k-step s takes bytes 32s .. 32s+31 of every row
             const uint64_t adesc0 = make_smem_desc(sA0, 16, 1024, kLayoutSw128);
@@ -508,6 +518,9 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE
                 Cfg::kNarrow ? make_smem_desc(sB0, 16, 16 * BN, BN == 16 ? kLayoutSw32 : kLayoutSw64)
                              : make_smem_desc(sB0, Cfg::kAtoms > 1 ? kTcStageK * 128 : 1024, 1024, kLayoutSw128);
             constexpr uint32_t kBRowBytes = Cfg::kNarrow ? BN * 2 : 128;
+            // K-major B: BN rows of 128 bytes (64 K) per box, two boxes per stage; MMA k-step s
+            // (K = 32, 64 bytes of each row) starts 64 * (s % 2) bytes into box s / 2
+            const uint64_t bkdesc0 = make_smem_desc(sB0, 16, 1024, kLayoutSw128);
             int it = 0, ti = 0;
             bool run = true;
             for (int t = static_cast<int>(blockIdx.x); run && t < p.total_tiles;
@@ -540,8 +553,9 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE
                     const uint32_t te = tmem_e + slot * kMetaStageCols;
 #pragma unroll
                     for (int s = 0; s < kKSteps; ++s) {
-                        tc_mma_sp_f16(d, ad + 2 * s, bd + ((s * 32 * kBRowBytes) >> 4), te + s * kMetaSlotCols, idesc,
-                                      (k > 0 || s > 0) ? 1u : 0u);
+                        const uint64_t bs = p.b_kmajor ? bkdesc0 + ((slot * Cfg::kBBytes + (s >> 1) * BN * 128 + (s & 1) * 64) >> 4)
+                                                       : bd + ((s * 32 * kBRowBytes) >> 4);
+                        tc_mma_sp_f16(d, ad + 2 * s, bs, te + s * kMetaSlotCols, idesc, (k > 0 || s > 0) ? 1u : 0u);
                         if (s == 1) {
                             // test the next stage of this tile while these MMAs run
                             const int nx = it + 1;
@@ -943,12 +957,13 @@ int tc_default_stages(int tile_m, int tile_n, bool gather) {
     return tc_stages(tile_m, tile_n, tc_narrow_b(tile_n, gather));
 }
 
-cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void* B, int64_t ld_b, int64_t N, void* C,
-                           int64_t ld_c, bool c_f32, float* partial, cudaStream_t stream) {
+cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void* B, int64_t ld_b, int64_t N,
+                           const OutSpec& out, float* partial, cudaStream_t stream) {
     const bool gather = L.mode == kTcGather;
     const bool lift = L.mode == kTcLift;
     if (L.mode != kTcTiled && L.mode != kTcGather && L.mode != kTcLift) return cudaErrorInvalidValue;
     if (lift && (A.M != 8 || L.tile_m != 128)) return cudaErrorInvalidValue;
+    if (L.b_kmajor && gather) return cudaErrorInvalidValue;  // the gather copies rows of a row-major B
     if (tc_default_stages(L.tile_m, L.tile_n, gather) == 0 || L.stages != tc_default_stages(L.tile_m, L.tile_n, gather))
         return cudaErrorInvalidValue;
     TcArgs p;
@@ -957,8 +972,9 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
     p.vpr_words = values_per_row(A.K, A.M) / 2;
     p.B = static_cast<const uint16_t*>(B);
     p.ld_b = ld_b;
-    p.C = C;
-    p.ld_c = ld_c;
+    p.out = out;
+    p.plain_out = out.ns == 1 && out.bias == nullptr && out.act == VNM_ACT_NONE;
+    p.b_kmajor = L.b_kmajor ? 1 : 0;
     p.R = A.R;
     p.N = N;
     p.V = A.V;
@@ -976,10 +992,9 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
     p.num_kt = units;
     p.kt_per_split = units_per_split;
     p.partial = splits > 1 ? partial : nullptr;
-    p.c_f32 = c_f32 ? 1 : 0;
-    const int64_t esz = c_f32 ? 4 : 2;
-    p.vec_store = (reinterpret_cast<uintptr_t>(C) % 16 == 0) && ((ld_c * esz) % 16 == 0);
-    p.vec32 = (reinterpret_cast<uintptr_t>(C) % 32 == 0) && ((ld_c * esz) % 32 == 0);
+    const int64_t esz = out.f32 ? 4 : 2;
+    p.vec_store = p.plain_out && (reinterpret_cast<uintptr_t>(out.C) % 16 == 0) && ((out.rs * esz) % 16 == 0);
+    p.vec32 = p.plain_out && (reinterpret_cast<uintptr_t>(out.C) % 32 == 0) && ((out.rs * esz) % 32 == 0);
     p.part_vec32 = (reinterpret_cast<uintptr_t>(partial) % 32 == 0) && (N % 8 == 0);
     p.status = A.status;
     p.skip_stage = L.skip_stage;
@@ -1004,7 +1019,7 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
     else
         e = gather ? dispatch_bn<64, kTcGather>(L, p, stream) : dispatch_bn<64, kTcTiled>(L, p, stream);
     if (e != cudaSuccess) return e;
-    if (splits > 1) return launch_splitk_reduce(partial, splits, A.R, N, C, ld_c, c_f32, stream);
+    if (splits > 1) return launch_splitk_reduce(partial, splits, A.R, N, out, stream);
     return cudaSuccess;
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,6 +42,41 @@ __device__ __forceinline__ void record_error(int* status, int code, int where) {
     atomicAdd(status + kStatusCount, 1);
 }
 
+// Where and how an SpMM writes C: element (r, n) at C + r * rs + n * ns
+// (in elements: row-major C has rs = ld_c, ns = 1; the Linear-layer form
+// Y = X . A^T writes C transposed, rs = 1, ns = ld_y), after adding bias[r]
+// (fp16; none when null) and applying an activation (a vnm_activation).
+struct OutSpec {
+    void* C;
+    int64_t rs, ns;
+    bool f32;
+    const __half* bias;
+    int act;
+};
+
+inline OutSpec out_rowmajor(void* C, int64_t ld_c, bool f32) { return OutSpec{C, ld_c, 1, f32, nullptr, 0}; }
+
+#ifdef __CUDACC__
+// The value stored for accumulator v of row r (before the rounding to C's type).
+__device__ __forceinline__ float out_transform(const OutSpec& o, int64_t r, float v) {
+    if (o.bias != nullptr) v += __half2float(o.bias[r]);
+    if (o.act == VNM_ACT_RELU) {
+        v = fmaxf(v, 0.f);
+    } else if (o.act == VNM_ACT_GELU) {
+        v = 0.5f * v * (1.f + erff(v * 0.70710678118654752f));
+    }
+    return v;
+}
+
+__device__ __forceinline__ void out_store(const OutSpec& o, int64_t r, int64_t n, float v) {
+    v = out_transform(o, r, v);
+    if (o.f32)
+        static_cast<float*>(o.C)[r * o.rs + n * o.ns] = v;
+    else
+        static_cast<__half*>(o.C)[r * o.rs + n * o.ns] = __float2half_rn(v);
+}
+#endif
+
 // ---- launchers (each returns the launch's cudaError_t) ----
 
 cudaError_t launch_compress(const vnm_matrix_s& A, const void* W, int64_t ld_w, cudaStream_t stream);
@@ -50,13 +86,15 @@ cudaError_t launch_decompress(const vnm_matrix_s& A, void* W, int64_t ld_w, cuda
 // splits (1, 2, 4 or 8, none empty) form a thread-block cluster and reduce
 // in distributed shared memory: no workspace. `stream_chunk_blocks(V)`
 // blocks are staged per pass.
-cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
-                               int64_t ld_c, bool c_f32, int splits, cudaStream_t stream);
+// B element (k, n) at B + k * bk + n * bn (row-major B: bk = ld_b, bn = 1;
+// the Linear-layer form reads X as B: bk = 1, bn = ld_x).
+cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t bk, int64_t bn, int64_t N,
+                               const OutSpec& out, int splits, cudaStream_t stream);
 int stream_chunk_blocks(int V);
 
 // CUDA-core SpMM; writes C directly (fp16 or fp32).
-cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, void* C,
-                             int64_t ld_c, bool c_f32, cudaStream_t stream);
+cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t bk, int64_t bn, int64_t N,
+                             const OutSpec& out, cudaStream_t stream);
 
 // Shared-memory rings of the tensor-core kernel, in stages of 128 columns
 // of the MMAs' K (4 MMA k-steps). B: 64-column swizzle atoms of 128 rows x
@@ -120,9 +158,11 @@ inline int64_t tc_k_units(int64_t K, int32_t M, bool lift) { return lift ? K / k
 
 struct TcLaunch {
     CUtensorMap tm_a;   // values, box {64, tile_m}: one stage (4 MMA k-steps), 128B swizzle (not read by kTcLift)
-    CUtensorMap tm_b;   // B, box {64, 128}, 128B swizzle; {tile_n, 128}, 32B/64B swizzle when narrow
+    CUtensorMap tm_b;   // B, box {64, 128}, 128B swizzle; {tile_n, 128}, 32B/64B swizzle when narrow;
+                        // K-major: box {64, tile_n} (64 K x tile_n rows), 128B swizzle
     int tile_m, tile_n, stages, splits;
     int mode;           // a TcMode
+    bool b_kmajor;      // B given K-major (X of the Linear-layer form: tm_b boxes {64 K, tile_n}); tiled and lift
     int sm_count;       // persistent grid: at most sm_count x resident CTAs per SM
     int skip_stage;     // tests of the bounded waits only (-1: none)
 };
@@ -130,10 +170,14 @@ struct TcLaunch {
 // tcgen05 sparse SpMM; with splits > 1 it writes fp32 partials to
 // `partial` ([splits][R][N]) and a second kernel reduces them into C.
 cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void* B, int64_t ld_b, int64_t N,
-                           void* C, int64_t ld_c, bool c_f32, float* partial, cudaStream_t stream);
+                           const OutSpec& out, float* partial, cudaStream_t stream);
 
-cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, void* C,
-                                 int64_t ld_c, bool c_f32, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const float* partial, int splits, int64_t R, int64_t N, const OutSpec& out,
+                                 cudaStream_t stream);
+
+// dst[c][r] = src[r][c] for an R x C fp16 matrix (leading dimensions in elements).
+cudaError_t launch_transpose_f16(const void* src, int64_t ld_src, int64_t R, int64_t C, void* dst, int64_t ld_dst,
+                                 cudaStream_t stream);
 
 // Fused dense GEMM + prune-and-encode (W = X . Y^T compressed into A in the
 // GEMM's epilogue): tm_x / tm_y are X (R x D) and Y (K x D) as 2-D fp16

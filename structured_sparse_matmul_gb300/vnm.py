@@ -63,6 +63,8 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.vnm_decompress.argtypes = [p, p, i64, p]
     L.vnm_gemm_compress.argtypes = [p, p, i64, p, i64, i64, p, i64, p]
     L.vnm_energy.argtypes = [p, p, i64, ctypes.c_int, p, sz, p, p, p, p]
+    L.vnm_linear.argtypes = [p, p, i64, i64, p, ctypes.c_int, p, i64, ctypes.c_int, p, sz, p]
+    L.vnm_linear_workspace_size.argtypes = [p, i64, p]
     L.vnm_energy_workspace_size.argtypes = [p, p]
     L.vnm_spmm.argtypes = [p, p, i64, i64, p, i64, ctypes.c_int, p, sz, p]
     L.vnm_spmm_workspace_size.argtypes = [p, i64, p]
@@ -206,6 +208,37 @@ def vnm_gemm_compress(A: VnmMatrix, X: torch.Tensor, Y: torch.Tensor, W_out: Opt
     ld_y = _rowmajor(Y, "Y") if D > 0 else 1
     _check(lib().vnm_gemm_compress(A.handle, X.data_ptr() or None, ld_x, Y.data_ptr() or None, ld_y, D, w_ptr, ld_w,
                                    _stream_ptr(stream)), "vnm_gemm_compress")
+
+
+VNM_ACT_NONE, VNM_ACT_RELU, VNM_ACT_GELU = 0, 1, 2
+
+
+def vnm_linear_workspace_size(A: VnmMatrix, T: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().vnm_linear_workspace_size(A.handle, int(T), ctypes.byref(n)), "vnm_linear_workspace_size")
+    return int(n.value)
+
+
+def vnm_linear(A: VnmMatrix, X: torch.Tensor, Y: torch.Tensor, bias: Optional[torch.Tensor] = None,
+               act: int = VNM_ACT_NONE, workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Y = act(X . A^T + bias): X (T x K fp16), Y (T x R, fp16 or fp32), bias (R fp16) or None."""
+    if X.dtype != torch.float16 or not X.is_cuda or X.dim() != 2 or X.shape[1] != A.K:
+        raise ValueError("X must be a CUDA fp16 tensor of shape (T, K)")
+    T = int(X.shape[0])
+    if not Y.is_cuda or Y.dim() != 2 or tuple(Y.shape) != (T, A.R):
+        raise ValueError("Y must be a CUDA tensor of shape (T, R)")
+    if bias is not None and (bias.dtype != torch.float16 or not bias.is_cuda or tuple(bias.shape) != (A.R,)
+                             or not bias.is_contiguous()):
+        raise ValueError("bias must be a contiguous CUDA fp16 tensor of shape (R,)")
+    if workspace is None:
+        n = vnm_linear_workspace_size(A, T)
+        workspace = torch.empty(n, dtype=torch.uint8, device=X.device) if n else None
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    ld_x = _rowmajor(X, "X") if A.K > 0 else 1
+    _check(lib().vnm_linear(A.handle, X.data_ptr() or None, ld_x, T,
+                            bias.data_ptr() if bias is not None else None, int(act), Y.data_ptr() or None,
+                            _rowmajor(Y, "Y"), _c_type(Y), ws_ptr, ws_bytes, _stream_ptr(stream)), "vnm_linear")
 
 
 VNM_PATTERN_VNM, VNM_PATTERN_UNSTRUCTURED, VNM_PATTERN_VECTORWISE = 0, 1, 2

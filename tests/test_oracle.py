@@ -395,11 +395,34 @@ def check_energy_invariants(L):
     assert oracle.energy(W, 1, 4, oracle.PATTERN_VNM, L)[1] == round(brute * 2 ** 24)
 
 
+def check_linear_worked_row(L):
+    """The worked row 0 of the 2:4 notes as a one-output Linear layer: y =
+    0.9 x0 - 0.4 x2 + 0.7 x5 - 1.2 x7 + bias, then ReLU or GELU; GELU(y) -
+    GELU(-y) = y and GELU(0) = 0 (x * Phi(x) with Phi(-x) = 1 - Phi(x))."""
+    fx = read_fixture(os.path.join(GOLDEN, "worked_2x8.txt"))
+    W = np.array([_floats(fx["dense_row0"])], dtype=np.float16)
+    values, meta, colidx = oracle.compress(W, 1, 4, L)
+    X = np.array([[1, 2, 3, 4, 5, 6, 7, 8], [-1, 0.5, 2, 0, 0, -3, 1, 0.25]], dtype=np.float16)
+    f = lambda x: float(np.float16(x))  # noqa: E731
+    want = np.array([f(0.9) * x[0] - f(0.4) * x[2] + f(0.7) * x[5] - f(1.2) * x[7] for x in X.astype(np.float64)])
+    bias = np.array([0.5], dtype=np.float16)
+    y = oracle.linear(values, meta, colidx, 1, 8, 1, 4, X, bias)
+    assert np.allclose(y[:, 0], want + 0.5, rtol=0, atol=1e-12)
+    assert np.allclose(oracle.linear(values, meta, colidx, 1, 8, 1, 4, X, bias, oracle.ACT_RELU)[:, 0],
+                       np.maximum(want + 0.5, 0), rtol=0, atol=1e-12)
+    g = oracle.linear(values, meta, colidx, 1, 8, 1, 4, X, bias, oracle.ACT_GELU)[:, 0]
+    gneg = oracle.linear(values, meta, colidx, 1, 8, 1, 4, -X, -bias, oracle.ACT_GELU)[:, 0]
+    assert np.allclose(g - gneg, want + 0.5, rtol=0, atol=1e-12)
+    zero = oracle.linear(values, meta, colidx, 1, 8, 1, 4, np.zeros((1, 8), np.float16), None, oracle.ACT_GELU)
+    assert zero[0, 0] == 0.0
+
+
 PINS = [check_worked_example, check_worked_local_index, check_worked_product,
         check_storage_arithmetic, check_brute_force_ties, check_brute_force_subnormals,
         check_brute_force_normal, check_invariants_and_round_trip, check_spmm_against_numpy,
         check_fig3_fixture, check_gemm_compress_identity, check_gemm_compress_rank1,
-        check_gemm_compress_rounding, check_energy_worked_example, check_energy_invariants]
+        check_gemm_compress_rounding, check_energy_worked_example, check_energy_invariants,
+        check_linear_worked_row]
 
 
 # ----------------------------------------------------------------------------
