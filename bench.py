@@ -745,7 +745,9 @@ def main():
     plan = vnm.vnm_spmm_plan_query(sets[0]["A"], sets[0]["B"], c_dtype,
                                    0 if sets[0]["ws"] is None else sets[0]["ws"].numel() * 4)
     splits = plan.splits if plan.path == vnm.VNM_PATH_TC else 1
-    kernels_per_step = 1 + (1 if plan.path != vnm.VNM_PATH_NONE else 0) + (1 if splits > 1 else 0)
+    # compress, the SpMM, its split-K reduction, and for lift = 2 the kernel that writes A out as 2:4
+    kernels_per_step = (1 + (1 if plan.path != vnm.VNM_PATH_NONE else 0) + (1 if splits > 1 else 0)
+                        + (1 if plan.path == vnm.VNM_PATH_TC and plan.lift == 2 else 0))
 
     stream = torch.cuda.current_stream(dev)
 

@@ -108,9 +108,13 @@ typedef struct vnm_spmm_plan {
                           of a group of 4), zeros filling the free slots: twice the MMA work of
                           the condensed K, 128-row tiles for any V % 16 == 0, K % 128 == 0.
                           0 = the default path for M (M == 4: B in tiles; M > 4: the selected
-                          rows of B gathered, V % 64 == 0). Ignored outside the TC path. Any
-                          value but 0 or 1: VNM_ERR_INVALID_ARG; 1 where the shape does not
-                          allow it (or with tile_m != 128): VNM_ERR_UNSUPPORTED. */
+                          rows of B gathered, V % 64 == 0). 2 = the same 2:4 form written out
+                          by a first kernel into the workspace (values R x K/2, then m-indices
+                          R x K/8, each rounded up to 256 bytes; split-K partials after them),
+                          then the 2:4 path on it: chosen for M == 8 with V % 128 != 0 and
+                          N >= 512 when the workspace holds it. Ignored outside the TC path.
+                          Any value but 0, 1 or 2: VNM_ERR_INVALID_ARG; 1 or 2 where the shape
+                          does not allow it (or with tile_m != 128): VNM_ERR_UNSUPPORTED. */
     int32_t reserved[2]; /* must be 0 (vnm_spmm_with_plan rejects anything else with
                             VNM_ERR_INVALID_ARG) */
 } vnm_spmm_plan;

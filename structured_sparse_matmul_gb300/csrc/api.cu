@@ -121,7 +121,15 @@ int64_t stream_splits(const vnm_matrix_s& A, int64_t N) {
     return effective_stream_splits(A, static_cast<int>(std::min<int64_t>(s, 4)));
 }
 
-vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, size_t workspace_bytes) {
+// Workspace bytes of the written-out 2:4 form of an M = 8 matrix (lift = 2):
+// values [R][K/2] fp16, then m-indices [R][K/8], each 256-byte aligned.
+size_t expand_values_bytes(const vnm_matrix_s& A) { return (static_cast<size_t>(A.R) * A.K + 255) & ~size_t(255); }
+size_t expand_bytes(const vnm_matrix_s& A) {
+    return expand_values_bytes(A) + ((static_cast<size_t>(A.R) * (A.K / 8) + 255) & ~size_t(255));
+}
+
+vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N, size_t workspace_bytes,
+                        bool allow_expand = true) {
     vnm_spmm_plan pl;
     std::memset(&pl, 0, sizeof(pl));
     pl.splits = 1;
@@ -140,6 +148,11 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     // measured as fast or faster (the re-encoded A's shared-memory stores
     // contend with the MMAs' operand reads)
     pl.lift = !tc_geometry_ok(A) && lift_ok(A) ? 1 : 0;
+    // M == 8 whose gather would run 64-row tiles (half-rate M = 64 MMAs), with
+    // wide B and a workspace that holds it: A written out as 2:4 by a first
+    // kernel, then the 2:4 path (twice the MMA work of the gather, all at the
+    // M = 128 rate, operands by TMA)
+    if (allow_expand && lift_ok(A) && A.V % 128 != 0 && N >= 512 && workspace_bytes >= expand_bytes(A)) pl.lift = 2;
     pl.tile_m = pl.lift || tc_tile_m_ok(A, 128) ? 128 : 64;
     // 256-column tiles for wide B (measured fastest on every shape: the
     // per-stage costs are spread over the most MMA work and the fewest A
@@ -155,7 +168,8 @@ vnm_spmm_plan make_plan(const vnm_matrix_s& A, const void* B, int64_t ld_b, int6
     int64_t splits = 1;
     if (tiles < A.sm_count) splits = std::min<int64_t>(num_kt, std::max<int64_t>(1, A.sm_count / tiles));
     const int64_t per_split = A.R * N * static_cast<int64_t>(sizeof(float));
-    if (splits > 1) splits = std::min<int64_t>(splits, static_cast<int64_t>(workspace_bytes) / per_split);
+    const size_t room = pl.lift == 2 ? workspace_bytes - expand_bytes(A) : workspace_bytes;
+    if (splits > 1) splits = std::min<int64_t>(splits, static_cast<int64_t>(room) / per_split);
     splits = std::max<int64_t>(1, splits);
     pl.splits = static_cast<int32_t>(std::max<int64_t>(1, splits));
     return pl;
@@ -173,7 +187,7 @@ vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void
                       size_t workspace_bytes, const void* workspace) {
     for (int32_t r : pl.reserved)
         if (r != 0) return VNM_ERR_INVALID_ARG;
-    if (pl.lift != 0 && pl.lift != 1) return VNM_ERR_INVALID_ARG;  // read by the TC path only
+    if (pl.lift < 0 || pl.lift > 2) return VNM_ERR_INVALID_ARG;  // read by the TC path only
     if (pl.path == VNM_PATH_SIMT) return pl.splits < 1 ? VNM_ERR_INVALID_ARG : VNM_OK;  // no workspace
     if (pl.path != VNM_PATH_TC) return VNM_ERR_UNSUPPORTED;
     if (!tc_operands_ok(B, ld_b, N)) return VNM_ERR_UNSUPPORTED;
@@ -186,10 +200,9 @@ vnm_status check_plan(const vnm_matrix_s& A, const vnm_spmm_plan& pl, const void
     if (depth == 0 || (pl.stages != 0 && pl.stages != depth)) return VNM_ERR_UNSUPPORTED;
     if (pl.splits < 1) return VNM_ERR_INVALID_ARG;
     const int s = effective_splits(A, pl.splits, pl.lift != 0);
-    if (s > 1) {
-        const size_t need = static_cast<size_t>(s) * A.R * N * sizeof(float);
-        if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 16)) return VNM_ERR_INVALID_ARG;
-    }
+    const size_t need = (pl.lift == 2 ? expand_bytes(A) : 0) + (s > 1 ? static_cast<size_t>(s) * A.R * N * sizeof(float) : 0);
+    if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned(workspace, pl.lift == 2 ? 256 : 16)))
+        return VNM_ERR_INVALID_ARG;
     return VNM_OK;
 }
 
@@ -210,6 +223,17 @@ vnm_status run_product(vnm_matrix A, const vnm_spmm_plan& pl, const BOperand& B,
             e = vnm::launch_spmm_stream(*A, B.ptr, B.bk, B.bn, N, out, effective_stream_splits(*A, pl.splits), stream);
         else
             e = vnm::launch_spmm_simt(*A, B.ptr, B.bk, B.bn, N, out, stream);
+    } else if (pl.path == VNM_PATH_TC && pl.lift == 2) {
+        // A written out as a plain 2:4 matrix over the whole K, then the 2:4 path on it
+        uint8_t* ws = static_cast<uint8_t*>(workspace);
+        if (vnm::launch_lift_expand(*A, ws, ws + expand_values_bytes(*A), stream) != cudaSuccess) return VNM_ERR_CUDA;
+        vnm_matrix_s A2 = *A;
+        A2.M = 4;
+        A2.values = ws;
+        A2.meta = ws + expand_values_bytes(*A);
+        vnm_spmm_plan pl2 = pl;
+        pl2.lift = 0;
+        return run_product(&A2, pl2, B, N, out, ws + expand_bytes(*A), stream, skip_stage);
     } else if (pl.path == VNM_PATH_TC) {
         vnm::TcLaunch L;
         std::memset(&L, 0, sizeof(L));
@@ -266,6 +290,14 @@ vnm_status check_spmm_args(vnm_matrix A, const void* B, int64_t ld_b, int64_t N,
 }
 
 }  // namespace
+
+namespace vnm {
+
+vnm_spmm_plan plan_without_expansion(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N) {
+    return make_plan(A, B, ld_b, N, SIZE_MAX / 2, /*allow_expand=*/false);
+}
+
+}  // namespace vnm
 
 extern "C" {
 
@@ -382,7 +414,7 @@ LinearPlan make_linear_plan(const vnm_matrix_s& A, bool x_aligned, int64_t T, si
     lp.ldt = ((std::max<int64_t>(T, 1) + 7) / 8) * 8;
     // the plan vnm_spmm makes for a row-major B of T columns (alignment assumed)
     const void* aligned_b = reinterpret_cast<const void*>(uintptr_t(256));
-    lp.pl = make_plan(A, aligned_b, lp.ldt, T, SIZE_MAX / 2);
+    lp.pl = make_plan(A, aligned_b, lp.ldt, T, SIZE_MAX / 2, /*allow_expand=*/false);
     if (lp.pl.path == VNM_PATH_TC) {
         // K-major B is read in place by TMA where the B tiles are not gathered: M == 4, or
         // M == 8 re-encoded (lift); the gather needs X^T in the workspace, as does an X that
@@ -565,6 +597,7 @@ vnm_status vnm_spmm_workspace_size(vnm_matrix A, int64_t N, size_t* bytes) {
     int s = 1;
     if (pl.path == VNM_PATH_TC) s = effective_splits(*A, pl.splits, pl.lift != 0);
     if (s > 1) *bytes = static_cast<size_t>(s) * A->R * N * sizeof(float);
+    if (pl.path == VNM_PATH_TC && pl.lift == 2) *bytes += expand_bytes(*A);
     return VNM_OK;
 }
 

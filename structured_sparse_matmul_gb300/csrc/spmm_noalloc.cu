@@ -138,11 +138,13 @@ extern "C" vnm_status vnm_spmm_noalloc(int64_t R, int64_t K, int32_t V, int32_t 
     A.cc_minor = minor;
     A.status = status != nullptr ? status : reinterpret_cast<int*>(area);
 
-    // the plan vnm_spmm makes with unlimited workspace; its split-K partials
-    // must fit the static scratch
+    // the plan vnm_spmm makes with unlimited workspace (without the written-out
+    // 2:4 form of M = 8, which the scratch does not hold); its split-K
+    // partials must fit the static scratch
     vnm_spmm_plan plan;
-    vnm_status st = vnm_spmm_plan_query(&A, B, ld_b, N, c_type, SIZE_MAX / 2, &plan);
+    vnm_status st = vnm_spmm_plan_query(&A, B, ld_b, N, c_type, 0, &plan);  // argument checks
     if (st != VNM_OK) return st;
+    plan = vnm::plan_without_expansion(A, B, ld_b, N);
     size_t need = 0;
     if (plan.path == VNM_PATH_TC && plan.splits > 1)
         need = static_cast<size_t>(plan.splits) * static_cast<size_t>(R) * static_cast<size_t>(N) * sizeof(float);
@@ -151,5 +153,6 @@ extern "C" vnm_status vnm_spmm_noalloc(int64_t R, int64_t K, int32_t V, int32_t 
     // the internal status words must start at zero for this call
     if (status == nullptr && cudaMemsetAsync(area, 0, kStatusBytes, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return VNM_ERR_CUDA;
-    return vnm_spmm(&A, B, ld_b, N, C, ld_c, c_type, need ? area + kStatusRegionBytes : nullptr, need, stream);
+    return vnm_spmm_with_plan(&A, &plan, B, ld_b, N, C, ld_c, c_type, need ? area + kStatusRegionBytes : nullptr, need,
+                              stream);
 }

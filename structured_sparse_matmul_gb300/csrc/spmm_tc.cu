@@ -275,9 +275,36 @@ __device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g
                 for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u] = __uint_as_float(v[u]);
             }
         } else if (!p.plain_out) {
-            // a bias, an activation or a transposed C: element by element (with a transposed
-            // C the lanes' rows are consecutive, so each store of the warp is coalesced)
-            for (int u = 0; u < 16 && col + u < p.N; ++u) out_store(p.out, row, col + u, __uint_as_float(v[u]));
+            // a bias, an activation or a transposed C: the 16 values transformed, then stored one
+            // by one (with a transposed C the lanes' rows are consecutive, so each store of the
+            // warp covers 32 consecutive elements of one row of Y)
+            float t[16];
+            const float bb = p.out.bias != nullptr ? __half2float(p.out.bias[row]) : 0.f;
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                float x = __uint_as_float(v[u]) + bb;
+                if (p.out.act == VNM_ACT_RELU) x = fmaxf(x, 0.f);
+                else if (p.out.act == VNM_ACT_GELU) x = 0.5f * x * (1.f + erff(x * 0.70710678118654752f));
+                t[u] = x;
+            }
+            const int64_t ns = p.out.ns;
+            if (p.out.f32) {
+                float* dst = static_cast<float*>(p.out.C) + row * p.out.rs + col * ns;
+                if (full) {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) dst[u * ns] = t[u];
+                } else {
+                    for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u * ns] = t[u];
+                }
+            } else {
+                __half* dst = static_cast<__half*>(p.out.C) + row * p.out.rs + col * ns;
+                if (full) {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) dst[u * ns] = __float2half_rn(t[u]);
+                } else {
+                    for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u * ns] = __float2half_rn(t[u]);
+                }
+            }
         } else if (p.out.f32) {
             float* dst = static_cast<float*>(p.out.C) + row * p.out.rs + col;
             if (full && p.vec32) {
@@ -949,7 +976,61 @@ cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, cudaStream_t stream)
     }
 }
 
+// The 2:4 form of an M = 8 matrix over the whole K, written out (the
+// workspace form of the re-encoding): every row's block j becomes the two
+// 4-column groups 2j, 2j+1 of a plain 2:4 row (values2 [R][K/2], meta2
+// [R][K/8]: one byte of two 4-bit codes per block). A thread takes four
+// consecutive blocks of a row: 16 bytes of values, 16 bits of m-indices and
+// 16 bytes of column-loc in; 32 bytes of values and 4 m-index bytes out.
+__global__ void __launch_bounds__(256) lift_expand_kernel(const uint32_t* __restrict__ values,
+                                                          const uint8_t* __restrict__ meta,
+                                                          const uint32_t* __restrict__ colidx, int64_t R, int64_t nblk,
+                                                          int64_t mpitch, int V, uint32_t* __restrict__ values2,
+                                                          uint32_t* __restrict__ meta2) {
+    __shared__ uint2 tab[64];
+    if (threadIdx.x < 64) tab[threadIdx.x] = lift_entry(threadIdx.x >> 3, threadIdx.x & 7u);
+    __syncthreads();
+    const int64_t quads = nblk / 4;  // nblk = K / 8, K % 128 == 0: whole quads
+    const int64_t total = R * quads;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < total;
+         q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = q / quads, j0 = (q - r * quads) * 4;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(values + r * nblk + j0));
+        const uint32_t m = __ldg(reinterpret_cast<const uint16_t*>(meta + r * mpitch + j0 / 2));
+        const uint4 c = __ldg(reinterpret_cast<const uint4*>(colidx + (r / V) * nblk + j0));
+        const uint32_t vs[4] = {v.x, v.y, v.z, v.w}, cs[4] = {c.x, c.y, c.z, c.w};
+        uint32_t out[8], codes = 0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t nib = (m >> (4 * b)) & 15u;
+            const uint32_t d0 = (cs[b] >> ((nib & 3u) << 3)) & 7u;
+            const uint32_t d1 = (cs[b] >> ((nib >> 2) << 3)) & 7u;
+            const uint2 e = tab[8 * d0 + d1];
+            out[2 * b] = __byte_perm(vs[b], 0u, e.x);
+            out[2 * b + 1] = __byte_perm(vs[b], 0u, e.x >> 16);
+            codes |= e.y << (8 * b);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(values2 + r * (2 * nblk) + 2 * j0);
+        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+        meta2[(r * nblk + j0) / 4] = codes;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_lift_expand(const vnm_matrix_s& A, void* values2, void* meta2, cudaStream_t stream) {
+    const int64_t nblk = A.K / A.M;
+    if (A.M != 8 || A.K % kTcStageK != 0) return cudaErrorInvalidValue;
+    const int64_t total = A.R * (nblk / 4);
+    if (total == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(A.sm_count) * 8);
+    lift_expand_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const uint32_t*>(A.values), static_cast<const uint8_t*>(A.meta),
+        static_cast<const uint32_t*>(A.colidx), A.R, nblk, meta_pitch(A.K, A.M), A.V,
+        static_cast<uint32_t*>(values2), static_cast<uint32_t*>(meta2));
+    return cudaGetLastError();
+}
 
 int tc_default_stages(int tile_m, int tile_n, bool gather) {
     if (tile_m != 64 && tile_m != 128) return 0;

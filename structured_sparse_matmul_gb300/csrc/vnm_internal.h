@@ -196,6 +196,16 @@ size_t energy_workspace_bytes(int64_t R, int64_t K, int V);
 cudaError_t launch_energy(const vnm_matrix_s& A, const void* W, int64_t ld_w, int pattern, void* workspace,
                           int sm_count, int* n_total_partials, int* n_kept_partials, cudaStream_t stream);
 
+// The workspace form of the M = 8 re-encoding: writes A as a plain 2:4
+// matrix over the whole K (values2: fp16 [R][K/2], meta2: [R][K/8] bytes,
+// both 16-byte aligned), which the 2:4 tensor-core path then reads by TMA.
+cudaError_t launch_lift_expand(const vnm_matrix_s& A, void* values2, void* meta2, cudaStream_t stream);
+
+// The plan vnm_spmm makes with an unlimited workspace, but never the
+// written-out 2:4 form of M = 8 (lift = 2): what a caller whose workspace
+// holds only split-K partials can run.
+vnm_spmm_plan plan_without_expansion(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N);
+
 // Pipeline stages the tensor-core kernel is built with for a tile (0: no such tile).
 int tc_default_stages(int tile_m, int tile_n, bool gather);
 

@@ -28,8 +28,9 @@ def _product(R, K, N, V, M, seed):
 @pytest.mark.parametrize("R,K,N,V,M,skip", [(2048, 2048, 1024, 128, 4, 3),    # B by TMA
                                             (2048, 2048, 1024, 64, 16, 2),    # B gathered
                                             (4096, 2048, 2048, 64, 16, 9),    # third tile of four (4 stages each)
-                                            (4096, 2048, 2048, 32, 8, 2),     # A re-encoded as 2:4 (lift)
-                                            (4096, 2048, 2048, 32, 8, 20)])   # second tile of two (16 stages each)
+                                            (16384, 2048, 256, 32, 8, 2),     # A re-encoded as 2:4 on chip (lift)
+                                            (20480, 2048, 256, 32, 8, 20),    # second tile of two (16 stages each)
+                                            (4096, 2048, 2048, 64, 8, 3)])    # A written out as 2:4 first
 def test_bounded_wait_reports_timeout_and_device_stays_usable(R, K, N, V, M, skip):
     A, B, comp = _product(R, K, N, V, M, seed=80 + M)
     Bd = torch.from_numpy(B).to(device())

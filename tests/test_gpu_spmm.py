@@ -218,12 +218,44 @@ def test_lift_agrees_with_gather():
         check_tight_f32(got, comp, R, K, V, 8, B, what=what)
 
 
+@pytest.mark.parametrize("R,K,N,V", [(4096, 2048, 2048, 64),   # the planner's choice (wide B, 64-row gather)
+                                     (320, 1024, 600, 64),     # ragged rows and columns
+                                     (256, 1152, 136, 32)])    # a plan asking for it on a narrow product
+def test_lift_written_out(R, K, N, V):
+    """lift = 2: A written out as a plain 2:4 matrix over the whole K in the
+    workspace by a first kernel, then the 2:4 path (split K after it)."""
+    A, B, comp = _setup(R, K, N, V, 8, seed=68)
+    rows = None if R <= 512 else sample_rows(R, V, 64)
+    if N >= 512:
+        plan = vnm.vnm_spmm_plan_query(A, to_dev(B), torch.float32, vnm.vnm_spmm_workspace_size(A, N))
+        assert plan.lift == 2 and plan.tile_m == 128, plan.as_dict()
+        got, _ = run_spmm(A, B, torch.float32)  # through vnm_spmm with vnm_spmm_workspace_size bytes
+    else:
+        plan = _lift_plan(A, B, torch.float32)
+        plan.lift = 2
+        plan.splits = 3
+        ws = torch.empty((R * K + R * K // 8 + 1024) // 4 + 3 * R * N + 64, dtype=torch.float32, device=device())
+        C = torch.empty((R, N), dtype=torch.float32, device=device())
+        vnm.vnm_spmm_with_plan(A, plan, to_dev(B), C, workspace=ws)
+        assert vnm.vnm_get_status(A) == vnm.VNM_OK
+        got = C.cpu().numpy()
+    g = got if rows is None else got[rows]
+    check_close(g, _ref(comp, R, K, V, 8, B, rows=rows), f"lift 2 {R}x{K}x{N}")
+    check_tight_f32(g, comp, R, K, V, 8, B, rows=rows, what=f"lift 2 {R}x{K}x{N}")
+    # a workspace without room for the written-out form is refused for this plan
+    if N < 512:
+        with pytest.raises(vnm.VnmError) as e:
+            vnm.vnm_spmm_with_plan(A, plan, to_dev(B), C, workspace=torch.empty(1024, dtype=torch.float32,
+                                                                                  device=device()))
+        assert e.value.code == vnm.VNM_ERR_INVALID_ARG
+
+
 def test_lift_plan_checks():
     R, K, N, V = 256, 1024, 64, 128
     A, B, _ = _setup(R, K, N, V, 8, seed=66)
     plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
     assert plan.lift == 0 and plan.tile_m == 128
-    plan.lift = 2
+    plan.lift = 3
     with pytest.raises(vnm.VnmError) as e:
         run_spmm(A, B, plan=plan)
     assert e.value.code == vnm.VNM_ERR_INVALID_ARG
