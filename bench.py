@@ -61,7 +61,44 @@ def parse_args():
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload kernel table")
     ap.add_argument("--per-config-launches", type=int, default=10,
                     help="kernel launches per graph in the per-workload table (median of 7 replays)")
+    ap.add_argument("--profile-op", choices=["gemm_compress", "linear"], default=None,
+                    help="run a few launches of one of the other entry points on its first table case and exit "
+                         "(for ncu captures)")
     return ap.parse_args()
+
+
+def profile_op(op: str) -> None:
+    """A few launches of vnm_gemm_compress or vnm_linear on the first case of
+    their bench tables, checked for a clean status (for ncu captures)."""
+    import torch
+
+    from structured_sparse_matmul_gb300 import vnm
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(7)
+    if op == "gemm_compress":
+        R, K, D, V, M = GEMM_COMPRESS_CASES[1]
+        A = vnm.vnm_matrix_alloc(R, K, V, M, dev)
+        X = torch.randn(R, D, device=dev, generator=gen).half()
+        Y = torch.randn(K, D, device=dev, generator=gen).half()
+        for _ in range(3):
+            vnm.vnm_gemm_compress(A, X, Y)
+    else:
+        R, K, T, V, M = LINEAR_CASES[0]
+        A = vnm.vnm_matrix_alloc(R, K, V, M, dev)
+        vnm.vnm_compress(A, (torch.randn(R, K, device=dev, generator=gen) * 0.02).half())
+        X = torch.randn(T, K, device=dev, generator=gen).half()
+        Y = torch.empty(T, R, dtype=torch.float16, device=dev)
+        bias = torch.randn(R, device=dev, generator=gen).half()
+        for _ in range(3):
+            vnm.vnm_linear(A, X, Y, bias, vnm.VNM_ACT_GELU)
+    torch.cuda.synchronize(dev)
+    st = vnm.vnm_get_status(A)
+    if st != vnm.VNM_OK:
+        raise SystemExit(f"status {vnm.status_string(st)}")
+    print(f"{op}: 3 launches, status ok")
 
 
 def load_peaks():
@@ -698,6 +735,9 @@ def measure_per_config(dev, peaks, launches: int):
 
 def main():
     args = parse_args()
+    if args.profile_op:
+        profile_op(args.profile_op)
+        return
     from structured_sparse_matmul_gb300 import workloads
     case = workloads.workload_cases(args.workload)[args.case]
     if args.rows:

@@ -150,7 +150,147 @@ __device__ __forceinline__ float fma_f16(uint32_t a, uint32_t b, float acc) {
     return acc;
 }
 
+// The streaming kernel for row-major B and C without bias or activation
+// (vnm_spmm). Its strided form below serves the Linear-layer form.
+struct StreamArgsRM {  // the row-major, plain form (vnm_spmm)
+    const uint32_t* values;  // [R][nblk] words: the 2 fp16 values of one block
+    const uint8_t* meta;     // [R][mpitch]
+    const uint32_t* colidx;  // [R/V][nblk] words: 4 column bytes
+    const __half* B;
+    int64_t ld_b;
+    void* C;
+    int64_t ld_c;
+    int64_t R, N;
+    int V, M;
+    int64_t nblk, mpitch;
+    int splits;
+    int64_t bps;             // blocks per split
+    bool c_f32;
+};
+
 template <int NB, int RW, int U>
+__global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_rm_kernel(const StreamArgsRM p) {
+    constexpr int kChunk = 32 * U;                       // blocks per chunk
+    // staged block: [NB columns][4 slots] halves (a column's 4 slots in 8
+    // bytes), padded for NB >= 4 to spread the banks
+    constexpr int kStride = 4 * NB + (NB >= 4 ? 4 : 0);
+    __shared__ __align__(16) __half Bc[kChunk * kStride];
+    __shared__ float red[kStreamWarps * RW][NB];  // this CTA's sums of the pass's rows (split K)
+    const int64_t i = blockIdx.x / p.splits;
+    const int s = static_cast<int>(blockIdx.x % p.splits);
+    const int64_t jb = s * p.bps;
+    const int64_t je = jb + p.bps < p.nblk ? jb + p.bps : p.nblk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t* crow = p.colidx + i * p.nblk;
+
+    // the same trip count for every warp (the loop holds CTA barriers); rows
+    // past V are masked
+    for (int rbase = 0; rbase < p.V; rbase += kStreamWarps * RW) {
+        const int r0 = rbase + warp;
+        float acc[RW][NB];
+#pragma unroll
+        for (int t = 0; t < RW; ++t)
+#pragma unroll
+            for (int n = 0; n < NB; ++n) acc[t][n] = 0.f;
+        for (int64_t j0 = jb; j0 < je; j0 += kChunk) {
+            // this warp's rows of the chunk: all loads in flight at once
+            uint32_t vv[RW][U], mb[RW][U];
+#pragma unroll
+            for (int t = 0; t < RW; ++t) {
+                const int r = r0 + kStreamWarps * t;
+                const int64_t row = i * p.V + r;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t jj = j0 + lane + 32 * u;
+                    vv[t][u] = 0u;
+                    mb[t][u] = 0u;
+                    if (r < p.V && jj < je) {
+                        vv[t][u] = __ldg(p.values + row * p.nblk + jj);
+                        mb[t][u] = __ldg(p.meta + row * p.mpitch + (jj >> 1));
+                    }
+                }
+            }
+            // stage the chunk's selected rows of B (the previous chunk's reads are done)
+            __syncthreads();
+            const int nb = static_cast<int>(je - j0 < kChunk ? je - j0 : kChunk);
+            for (int q = threadIdx.x; q < nb * 4; q += blockDim.x) {
+                const int jl = q >> 2, slot = q & 3;
+                const uint32_t w = __ldg(crow + j0 + jl);
+                // column-loc byte, clamped so that a corrupt array cannot address past K
+                const uint32_t cb = min((w >> (8 * slot)) & 0xFFu, static_cast<uint32_t>(p.M - 1));
+                const __half* src = p.B + ((j0 + jl) * p.M + cb) * p.ld_b;
+                __half* dst = Bc + jl * kStride + slot;
+#pragma unroll
+                for (int n = 0; n < NB; ++n) dst[4 * n] = n < p.N ? src[n] : __float2half_rn(0.f);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int t = 0; t < RW; ++t) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int64_t jj = j0 + lane + 32 * u;
+                    if (jj >= je) continue;
+                    const uint32_t code = (mb[t][u] >> (4 * (jj & 1))) & 0xFu;
+                    // byte-permute selector of slots s0 = code & 3 (low half) and s1 = code >> 2
+                    const uint32_t sel = ((code & 3u) * 0x22u + 0x10u) | (((code >> 2) * 0x22u + 0x10u) << 8);
+                    const uint32_t a = vv[t][u];
+                    const uint2* b = reinterpret_cast<const uint2*>(Bc + (lane + 32 * u) * kStride);
+#pragma unroll
+                    for (int n = 0; n < NB; ++n) {
+                        const uint2 w = b[n];  // the 4 slots of column n
+                        const uint32_t pr = __byte_perm(w.x, w.y, sel);
+                        acc[t][n] = fma_f16(a, pr, acc[t][n]);
+                        acc[t][n] = fma_f16(a >> 16, pr >> 16, acc[t][n]);
+                    }
+                }
+            }
+        }
+        auto store = [&](int r, int n, float v) {
+            const int64_t row = i * p.V + r;
+            if (p.c_f32)
+                static_cast<float*>(p.C)[row * p.ld_c + n] = v;
+            else
+                static_cast<__half*>(p.C)[row * p.ld_c + n] = __float2half_rn(v);
+        };
+#pragma unroll
+        for (int t = 0; t < RW; ++t) {
+            const int r = r0 + kStreamWarps * t;
+            float out = 0.f;
+#pragma unroll
+            for (int n = 0; n < NB; ++n) {
+                float v = acc[t][n];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+                if (lane == n) out = v;
+            }
+            if (p.splits > 1) {
+                if (lane < NB) red[warp + kStreamWarps * t][lane] = out;
+            } else if (r < p.V && lane < p.N && lane < NB) {
+                store(r, lane, out);
+            }
+        }
+        if (p.splits > 1) {
+            // every CTA of the cluster holds its partial sums of the pass's rows
+            cluster_sync_all();
+            const uint32_t red0 = smem_u32(&red[0][0]);
+            for (int e = threadIdx.x; e < kStreamWarps * RW * NB; e += blockDim.x) {
+                const int l = e / NB, n = e % NB;  // row of the pass (warp + 16 t), column
+                const int r = rbase + l;
+                if (l % p.splits != s || r >= p.V || n >= p.N) continue;
+                float v = 0.f;
+                for (int q = 0; q < p.splits; ++q)
+                    v += dsmem_ld_f32(dsmem_map(red0 + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)));
+                store(r, n, v);
+            }
+            // no CTA reuses or leaves its partial sums while another may still read them
+            cluster_sync_all();
+        }
+    }
+}
+
+// The strided form: B element (k, n) at B + k * bk + n * bn, C written
+// through an OutSpec (PLAIN: row-major B and C, no bias or activation).
+template <int NB, int RW, int U, bool PLAIN>
 __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const StreamArgs p) {
     constexpr int kChunk = 32 * U;                       // blocks per chunk
     // staged block: [NB columns][4 slots] halves (a column's 4 slots in 8
@@ -203,7 +343,7 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
                 const __half* src = p.B + ((j0 + jl) * p.M + cb) * p.bk;
                 __half* dst = Bc + jl * kStride + slot;
 #pragma unroll
-                for (int n = 0; n < NB; ++n) dst[4 * n] = n < p.N ? src[n * p.bn] : __float2half_rn(0.f);
+                for (int n = 0; n < NB; ++n) dst[4 * n] = n < p.N ? src[PLAIN ? n : n * p.bn] : __float2half_rn(0.f);
             }
             __syncthreads();
 #pragma unroll
@@ -227,7 +367,15 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
                 }
             }
         }
-        auto store = [&](int r, int n, float v) { out_store(p.out, i * p.V + r, n, v); };
+        auto store = [&](int r, int n, float v) {
+            const int64_t row = i * p.V + r;
+            if (!PLAIN)
+                out_store(p.out, row, n, v);
+            else if (p.out.f32)
+                static_cast<float*>(p.out.C)[row * p.out.rs + n] = v;
+            else
+                static_cast<__half*>(p.out.C)[row * p.out.rs + n] = __float2half_rn(v);
+        };
 #pragma unroll
         for (int t = 0; t < RW; ++t) {
             const int r = r0 + kStreamWarps * t;
@@ -264,11 +412,11 @@ __global__ void __launch_bounds__(32 * kStreamWarps) spmm_stream_kernel(const St
     }
 }
 
-template <int NB, int RW, int U>
-cudaError_t launch_stream3(const StreamArgs& p, cudaStream_t stream) {
+template <int NB, int RW, int U, bool PLAIN>
+cudaError_t launch_stream4(const StreamArgs& p, cudaStream_t stream) {
     const int64_t ctas = (p.R / p.V) * p.splits;
     if (p.splits == 1) {
-        spmm_stream_kernel<NB, RW, U><<<static_cast<unsigned>(ctas), 32 * kStreamWarps, 0, stream>>>(p);
+        spmm_stream_kernel<NB, RW, U, PLAIN><<<static_cast<unsigned>(ctas), 32 * kStreamWarps, 0, stream>>>(p);
         return cudaGetLastError();
     }
     // the splits of a V-block row are consecutive CTAs: one cluster
@@ -284,7 +432,52 @@ cudaError_t launch_stream3(const StreamArgs& p, cudaStream_t stream) {
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, spmm_stream_kernel<NB, RW, U>, p);
+    return cudaLaunchKernelEx(&cfg, spmm_stream_kernel<NB, RW, U, PLAIN>, p);
+}
+
+template <int NB, int RW, int U>
+cudaError_t launch_stream_rm(const StreamArgs& q, cudaStream_t stream) {
+    StreamArgsRM p;
+    p.values = q.values;
+    p.meta = q.meta;
+    p.colidx = q.colidx;
+    p.B = q.B;
+    p.ld_b = q.bk;
+    p.C = q.out.C;
+    p.ld_c = q.out.rs;
+    p.R = q.R;
+    p.N = q.N;
+    p.V = q.V;
+    p.M = q.M;
+    p.nblk = q.nblk;
+    p.mpitch = q.mpitch;
+    p.splits = q.splits;
+    p.bps = q.bps;
+    p.c_f32 = q.out.f32;
+    const int64_t ctas = (p.R / p.V) * p.splits;
+    if (p.splits == 1) {
+        spmm_stream_rm_kernel<NB, RW, U><<<static_cast<unsigned>(ctas), 32 * kStreamWarps, 0, stream>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(32 * kStreamWarps);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, spmm_stream_rm_kernel<NB, RW, U>, p);
+}
+
+template <int NB, int RW, int U>
+cudaError_t launch_stream3(const StreamArgs& p, cudaStream_t stream) {
+    const bool plain = p.bn == 1 && p.out.ns == 1 && p.out.bias == nullptr && p.out.act == VNM_ACT_NONE;
+    return plain ? launch_stream_rm<NB, RW, U>(p, stream) : launch_stream4<NB, RW, U, false>(p, stream);
 }
 
 template <int NB>

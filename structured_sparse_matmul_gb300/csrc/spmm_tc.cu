@@ -254,7 +254,7 @@ __device__ __forceinline__ TileGeom tile_geom(const TcArgs& p, int t, int tm, in
 // `tacc`: the buffer's column 0 in this warp's lane quarter) -> registers ->
 // C (fp16, RNE, or fp32) or the split-K partials; `row` is this thread's row
 // of C (>= R: none). Each thread writes whole 32-byte sectors of its row.
-template <int BN>
+template <int BN, bool GEN>
 __device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g, uint32_t tacc, int64_t row, int c0,
                                               int c1) {
     // one 16-column chunk of this thread's row: fp32 partials, fp32 or fp16 C
@@ -274,7 +274,7 @@ __device__ __forceinline__ void drain_columns(const TcArgs& p, const TileGeom& g
             } else {
                 for (int u = 0; u < 16 && col + u < p.N; ++u) dst[u] = __uint_as_float(v[u]);
             }
-        } else if (!p.plain_out) {
+        } else if (GEN && !p.plain_out) {
             // a bias, an activation or a transposed C: the 16 values transformed, then stored one
             // by one (with a transposed C the lanes' rows are consecutive, so each store of the
             // warp covers 32 consecutive elements of one row of Y)
@@ -375,7 +375,9 @@ __device__ __forceinline__ void stage_next(const TcArgs& p, StageIt& x) {
 }
 
 // Persistent: CTA b takes tiles b, b + gridDim.x, ...
-template <int TM, int BN, int MODE>
+// GEN: the general output (bias, activation, transposed C) and a K-major B
+// (the Linear-layer form); without it the kernel is the plain SpMM's.
+template <int TM, int BN, int MODE, bool GEN>
 __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE>::kMinBlocks)
     spmm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const TcArgs p) {
@@ -504,7 +506,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE
                         const uint32_t sB = sB0 + slot * Cfg::kBBytes;
                         const int32_t row = (g.kt0 + k) * kTcStageK;
                         mbar_arrive_expect_tx(fb, Cfg::kBBytes);
-                        if (p.b_kmajor) {
+                        if (GEN && p.b_kmajor) {
                             // two boxes of 64 K x BN rows (128-byte rows, 128B swizzle)
                             tma_load_2d(sB, &tm_b, row, static_cast<int32_t>(g.n0), fb);
                             tma_load_2d(sB + BN * 128, &tm_b, row + 64, static_cast<int32_t>(g.n0), fb);
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE
         if (lane == 0) {
             constexpr uint32_t idesc_n = make_idesc_f16_f32(TM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/true);
             constexpr uint32_t idesc_k = make_idesc_f16_f32(TM, BN, /*sparse=*/true, /*a_mn=*/false, /*b_mn=*/false);
-            const uint32_t idesc = p.b_kmajor ? idesc_k : idesc_n;
+            const uint32_t idesc = GEN && p.b_kmajor ? idesc_k : idesc_n;
             // A: K-major, 128B swizzle, 128-byte rows (64 values), 8-row groups 1024 bytes apart;
             // MMA k-step s takes bytes 32s .. 32s+31 of every row
             const uint64_t adesc0 = make_smem_desc(sA0, 16, 1024, kLayoutSw128);
@@ -580,7 +582,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE
                     const uint32_t te = tmem_e + slot * kMetaStageCols;
 #pragma unroll
                     for (int s = 0; s < kKSteps; ++s) {
-                        const uint64_t bs = p.b_kmajor ? bkdesc0 + ((slot * Cfg::kBBytes + (s >> 1) * BN * 128 + (s & 1) * 64) >> 4)
+                        const uint64_t bs = GEN && p.b_kmajor ? bkdesc0 + ((slot * Cfg::kBBytes + (s >> 1) * BN * 128 + (s & 1) * 64) >> 4)
                                                        : bd + ((s * 32 * kBRowBytes) >> 4);
                         tc_mma_sp_f16(d, ad + 2 * s, bs, te + s * kMetaSlotCols, idesc, (k > 0 || s > 0) ? 1u : 0u);
                         if (s == 1) {
@@ -719,7 +721,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE
                             !*abort;
             if (!ok) return false;
             tc_fence_after_sync();
-            drain_columns<BN>(p, g, tmem_acc + lane_addr, trow >= 0 ? g.m0 + trow : p.R, kEpiCols, BN);
+            drain_columns<BN, GEN>(p, g, tmem_acc + lane_addr, trow >= 0 ? g.m0 + trow : p.R, kEpiCols, BN);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&acce_bar[0]));
@@ -797,7 +799,7 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE
             if (!ok) break;
             tc_fence_after_sync();
             const int64_t row = trow >= 0 ? g.m0 + trow : p.R;
-            drain_columns<BN>(p, g, tmem_acc + buf * BN + lane_addr, row, 0, kEpiCols);
+            drain_columns<BN, GEN>(p, g, tmem_acc + buf * BN + lane_addr, row, 0, kEpiCols);
             // this warp's lanes of the accumulator are in registers: release it
             tc_fence_before_sync();
             __syncwarp();
@@ -937,10 +939,10 @@ __global__ void __launch_bounds__(tc_threads<TM, BN, MODE>(), TcCfg<TM, BN, MODE
 // of the instance on each device.
 constexpr int kMaxDevices = 64;
 
-template <int TM, int BN, int MODE>
+template <int TM, int BN, int MODE, bool GEN>
 cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stream) {
     using Cfg = TcCfg<TM, BN, MODE>;
-    auto kern = spmm_tc_kernel<TM, BN, MODE>;
+    auto kern = spmm_tc_kernel<TM, BN, MODE, GEN>;
     constexpr int threads = tc_threads<TM, BN, MODE>();
     static std::atomic<int> per_sm_cache[kMaxDevices];
     int dev = 0;
@@ -963,15 +965,15 @@ cudaError_t launch_variant(const TcLaunch& L, const TcArgs& p, cudaStream_t stre
     return cudaGetLastError();
 }
 
-template <int TM, int MODE>
+template <int TM, int MODE, bool GEN>
 cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, cudaStream_t stream) {
     switch (L.tile_n) {
-        case 16: return launch_variant<TM, 16, MODE>(L, p, stream);
-        case 32: return launch_variant<TM, 32, MODE>(L, p, stream);
-        case 64: return launch_variant<TM, 64, MODE>(L, p, stream);
-        case 128: return launch_variant<TM, 128, MODE>(L, p, stream);
-        case 192: return launch_variant<TM, 192, MODE>(L, p, stream);
-        case 256: return launch_variant<TM, 256, MODE>(L, p, stream);
+        case 16: return launch_variant<TM, 16, MODE, GEN>(L, p, stream);
+        case 32: return launch_variant<TM, 32, MODE, GEN>(L, p, stream);
+        case 64: return launch_variant<TM, 64, MODE, GEN>(L, p, stream);
+        case 128: return launch_variant<TM, 128, MODE, GEN>(L, p, stream);
+        case 192: return GEN ? cudaErrorInvalidValue : launch_variant<TM, 192, MODE, false>(L, p, stream);
+        case 256: return launch_variant<TM, 256, MODE, GEN>(L, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1093,12 +1095,22 @@ cudaError_t launch_spmm_tc(const vnm_matrix_s& A, const TcLaunch& L, const void*
     if (total > INT32_MAX) return cudaErrorInvalidValue;
     p.total_tiles = static_cast<int>(total);
     cudaError_t e;
-    if (lift)
-        e = dispatch_bn<128, kTcLift>(L, p, stream);
-    else if (L.tile_m == 128)
-        e = gather ? dispatch_bn<128, kTcGather>(L, p, stream) : dispatch_bn<128, kTcTiled>(L, p, stream);
-    else
-        e = gather ? dispatch_bn<64, kTcGather>(L, p, stream) : dispatch_bn<64, kTcTiled>(L, p, stream);
+    // the plain SpMM runs kernels without the general output and K-major B
+    if (p.plain_out && !p.b_kmajor) {
+        if (lift)
+            e = dispatch_bn<128, kTcLift, false>(L, p, stream);
+        else if (L.tile_m == 128)
+            e = gather ? dispatch_bn<128, kTcGather, false>(L, p, stream) : dispatch_bn<128, kTcTiled, false>(L, p, stream);
+        else
+            e = gather ? dispatch_bn<64, kTcGather, false>(L, p, stream) : dispatch_bn<64, kTcTiled, false>(L, p, stream);
+    } else {
+        if (lift)
+            e = dispatch_bn<128, kTcLift, true>(L, p, stream);
+        else if (L.tile_m == 128)
+            e = gather ? dispatch_bn<128, kTcGather, true>(L, p, stream) : dispatch_bn<128, kTcTiled, true>(L, p, stream);
+        else
+            e = gather ? dispatch_bn<64, kTcGather, true>(L, p, stream) : dispatch_bn<64, kTcTiled, true>(L, p, stream);
+    }
     if (e != cudaSuccess) return e;
     if (splits > 1) return launch_splitk_reduce(partial, splits, A.R, N, out, stream);
     return cudaSuccess;
