@@ -588,6 +588,60 @@ def measure_linear(dev, peaks, launches: int):
             "l2_eviction": "rotating X / Y sets of more than twice the L2 in each graph", "cases": out}
 
 
+# Decode-time products with unstructured sparsity in the bitmap format
+# (Coruscant: 30-70% sparsity, Llama-style projections): R, K, sparsity.
+BITMAP_CASES = [(4096, 4096, 0.5), (11008, 4096, 0.5), (4096, 11008, 0.5), (4096, 4096, 0.3), (4096, 4096, 0.7)]
+BITMAP_N = (1, 8, 16)
+
+
+def measure_bitmap(dev, peaks, launches: int):
+    """vnm_bitmap_spmm on magnitude-pruned N(0, 0.02) weights (the smallest
+    |w| zeroed), timed like the per-workload table, against the HBM roofline
+    of its bytes (bitmaps + offsets + values + B + C) and dense torch.matmul
+    on the same shape (context)."""
+    import torch
+
+    from structured_sparse_matmul_gb300 import vnm
+
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(6161)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2 ** 20))
+    out = {}
+    for (R, K, sp) in BITMAP_CASES:
+        W = (torch.randn(R, K, device=dev, generator=gen) * 0.02).half()
+        cut = W.abs().float().flatten().kthvalue(max(1, int(sp * R * K))).values
+        W[W.abs().float() <= cut] = 0
+        A = vnm.bitmap_encode(W)
+        a_bytes = A.bitmaps.numel() * 8 + A.offsets.numel() * 4 + A.bases.numel() * 8 + A.values.numel() * 2
+        n_sets = max(2, math.ceil(2 * l2 / a_bytes) + 1)
+        mats = [A] + [vnm.bitmap_encode(W) for _ in range(n_sets - 1)]
+        for N in BITMAP_N:
+            Bs = [torch.randn(K, N, device=dev, generator=gen).half() for _ in range(n_sets)]
+            Cs = [torch.empty(R, N, dtype=torch.float16, device=dev) for _ in range(n_sets)]
+            nws = vnm.bitmap_spmm_workspace_size(R, K, N)
+            ws = torch.empty(max(1, nws // 4), dtype=torch.float32, device=dev)
+
+            def run(i, st):
+                vnm.bitmap_spmm(mats[i % n_sets], Bs[i % n_sets], Cs[i % n_sets], workspace=ws, stream=st)
+
+            def dense(i, st):
+                torch.matmul(W, Bs[i % n_sets])
+
+            t = _time_graph(dev, run, launches)
+            td = _time_graph(dev, dense, launches)
+            byts = a_bytes + 2 * K * N + 2 * R * N
+            t_roof = byts / (peaks["hbm_gbs"] * 1e9) * 1e6
+            out[f"{R}x{K}, {int(sp * 100)}% zeros, N={N}"] = {
+                "bitmap_spmm_us": t, "dense_matmul_us": td,
+                "roofline": {"bound": "hbm", "t_roof_us": t_roof, "frac": t_roof / t},
+                "format_bytes_vs_dense": a_bytes / (2.0 * R * K)}
+        del mats, W, A
+        torch.cuda.empty_cache()
+    return {"launches_per_graph": launches, "replays": 7, "statistic": "median",
+            "inputs": "torch seeded device generator, W ~ N(0, 0.02) with the smallest |w| zeroed, B ~ N(0, 1)",
+            "cases": out}
+
+
 def measure_energy(dev):
     """Energy (magnitude preservation) of the three selection policies at the
     V:N:M densities 2/M on a synthetic N(0, 0.02) weight of the 768 x 768
@@ -1060,6 +1114,7 @@ def main():
         per_config["gemm_compress"] = measure_gemm_compress(dev, peaks, max(2, args.per_config_launches))
         per_config["energy"] = measure_energy(dev)
         per_config["linear"] = measure_linear(dev, peaks, max(2, args.per_config_launches))
+        per_config["bitmap"] = measure_bitmap(dev, peaks, max(2, args.per_config_launches))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

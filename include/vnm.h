@@ -212,6 +212,54 @@ vnm_status vnm_linear(vnm_matrix A, const void* X, int64_t ld_x, int64_t T, cons
 vnm_status vnm_linear_workspace_size(vnm_matrix A, int64_t T, size_t* bytes);
 
 /*
+ * Bitmap format for unstructured sparsity (Coruscant, section 3.1, Figure 7):
+ * an R x K fp16 matrix (R % 64 == 0) in column tiles of 64 rows. Tile (i, k)
+ * covers rows 64i .. 64i+63 of column k: bit r of bitmaps[i][k] (uint64) is
+ * set when W[64i + r][k] is not +0 or -0; its values are those rows' values in
+ * row order, then +0.0 up to a multiple of 8, stored from
+ * values[bases[i] + offsets[i][k]] (offsets uint32 relative to the row
+ * block's base; bases int64 [R/64 + 1], bases[R/64] = the values' length).
+ * vnm_bitmap_sizes gives the arrays' bytes (host only); values_max_bytes is
+ * the largest values array (every tile full: R x K values).
+ * Errors: VNM_ERR_INVALID_ARG (R % 64 != 0, negative sizes).
+ */
+vnm_status vnm_bitmap_sizes(int64_t R, int64_t K, size_t* bitmaps_bytes, size_t* offsets_bytes, size_t* bases_bytes,
+                            size_t* values_max_bytes);
+
+/*
+ * Encode the dense fp16 W (R x K row-major, ld_w >= K, 2-byte aligned) into
+ * the bitmap format: bitmaps, offsets and bases as above (caller-owned device
+ * arrays of vnm_bitmap_sizes' bytes), then the values when they fit
+ * values_capacity elements. *values_len (host) gets the length the values
+ * need; the call synchronizes the stream to read it. With too small a
+ * capacity the values are not written and VNM_ERR_INVALID_ARG is returned
+ * (with *values_len set: allocate that and call again).
+ * Errors: VNM_ERR_INVALID_ARG, VNM_ERR_CUDA.
+ */
+vnm_status vnm_bitmap_encode(const void* W, int64_t ld_w, int64_t R, int64_t K, void* bitmaps, void* offsets,
+                             int64_t* bases, void* values, int64_t values_capacity, int64_t* values_len,
+                             vnm_stream_t stream);
+
+/*
+ * C = A . B for A in the bitmap format (R x K), B fp16 K x N (ld_b >= N), C
+ * fp16 or fp32 R x N (ld_c >= N), fp32 accumulation (Coruscant section 3.2:
+ * a decode-time, memory-bound product; K split over thread blocks). The
+ * arrays are as vnm_bitmap_encode wrote them, values 16-byte aligned (the
+ * padding then makes every 32 consecutive tiles' values one 16-byte aligned
+ * run, streamed into shared memory as such); the current device runs it.
+ * workspace: fp32 partial sums of the K splits, at least
+ * vnm_bitmap_spmm_workspace_size bytes, 16-byte aligned; NULL (or a smaller
+ * one) runs without splitting K.
+ * Errors: VNM_ERR_INVALID_ARG, VNM_ERR_CUDA.
+ */
+vnm_status vnm_bitmap_spmm(int64_t R, int64_t K, const void* bitmaps, const void* offsets, const int64_t* bases,
+                           const void* values, const void* B, int64_t ld_b, int64_t N, void* C, int64_t ld_c,
+                           vnm_dtype c_type, void* workspace, size_t workspace_bytes, vnm_stream_t stream);
+
+/* Bytes of workspace vnm_bitmap_spmm splits K with on the current device (host only). */
+vnm_status vnm_bitmap_spmm_workspace_size(int64_t R, int64_t K, int64_t N, size_t* bytes);
+
+/*
  * Energy (magnitude preservation) of pruning the dense fp16 matrix W (R x K,
  * leading dimension ld_w >= K; R, K, V, M are the handle's) with a selection
  * policy (VENOM section 5, Figure 11): sum of the kept |w| over the sum of

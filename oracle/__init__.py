@@ -137,6 +137,66 @@ def gemm_compress(X: np.ndarray, Y: np.ndarray, V: int, M: int, L: Optional[ctyp
     return W, compress(W, V, M, L)
 
 
+def bitmap_encode(W: np.ndarray):
+    """The bitmap format of "Coruscant" section 3.1 (Figure 7) for fp16 W
+    (R x K, R % 64 == 0): column tiles of 64 rows; tile (i, k) is rows
+    64i .. 64i+63 of column k. Returns ``(bitmaps, offsets, bases, values)``:
+    bitmaps uint64 [R/64, K] with bit r set when W[64i + r, k] is not +-0;
+    values fp16 bit patterns, per tile (row-block major, then column) its
+    non-zero values in row order followed by +0.0 up to a multiple of 8;
+    offsets uint32 [R/64, K] the start of each tile's values relative to its
+    row block's first value; bases int64 [R/64 + 1] those firsts (the last
+    is the total length)."""
+    W = np.ascontiguousarray(W, dtype=np.float16)
+    R, K = W.shape
+    assert R % 64 == 0
+    nb = R // 64
+    bits = W.view(np.uint16)
+    bitmaps = np.zeros((nb, K), dtype=np.uint64)
+    offsets = np.zeros((nb, K), dtype=np.uint32)
+    bases = np.zeros(nb + 1, dtype=np.int64)
+    chunks = []
+    total = 0
+    for i in range(nb):
+        start = total
+        for k in range(K):
+            col = bits[64 * i:64 * (i + 1), k]
+            rows = [r for r in range(64) if int(col[r]) & 0x7FFF]
+            bitmaps[i, k] = np.uint64(sum(1 << r for r in rows))
+            offsets[i, k] = total - start
+            padded = (len(rows) + 7) // 8 * 8
+            chunk = np.zeros(padded, dtype=np.uint16)
+            chunk[:len(rows)] = col[rows]
+            chunks.append(chunk)
+            total += padded
+        bases[i + 1] = total
+    values = np.concatenate(chunks) if chunks else np.zeros(0, dtype=np.uint16)
+    return bitmaps, offsets, bases, values
+
+
+def bitmap_decode(bitmaps: np.ndarray, offsets: np.ndarray, bases: np.ndarray, values: np.ndarray, R: int,
+                  K: int) -> np.ndarray:
+    """Dense fp16 R x K from the bitmap format (positions without a bit: +0.0)."""
+    W = np.zeros((R, K), dtype=np.uint16)
+    for i in range(R // 64):
+        for k in range(K):
+            bm = int(bitmaps[i, k])
+            at = int(bases[i]) + int(offsets[i, k])
+            n = 0
+            for r in range(64):
+                if (bm >> r) & 1:
+                    W[64 * i + r, k] = values[at + n]
+                    n += 1
+    return W.view(np.float16)
+
+
+def bitmap_spmm(bitmaps, offsets, bases, values, R: int, K: int, B: np.ndarray) -> np.ndarray:
+    """C = A . B in fp64 for A in the bitmap format (numpy's matmul of the
+    decoded A; fp16 products are exact in fp64)."""
+    A = bitmap_decode(bitmaps, offsets, bases, values, R, K).astype(np.float64)
+    return A @ np.asarray(B, dtype=np.float16).astype(np.float64)
+
+
 ACT_NONE, ACT_RELU, ACT_GELU = 0, 1, 2
 
 

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libvnm.so")
-SOURCES = ["api.cu", "compress.cu", "spmm_simt.cu", "spmm_tc.cu", "spmm_noalloc.cu", "gemm_compress.cu", "energy.cu"]
+SOURCES = ["api.cu", "compress.cu", "spmm_simt.cu", "spmm_tc.cu", "spmm_noalloc.cu", "gemm_compress.cu", "energy.cu", "bitmap.cu"]
 HEADERS = ["vnm_internal.h", "vnm_ptx.cuh", "vnm_select.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "-Xptxas", "-v"]

@@ -486,6 +486,82 @@ vnm_status vnm_linear(vnm_matrix A, const void* X, int64_t ld_x, int64_t T, cons
     return run_product(A, lp.pl, B, T, out, ws + lp.t_bytes, s);
 }
 
+// ---- the bitmap format (unstructured sparsity) ----
+
+vnm_status vnm_bitmap_sizes(int64_t R, int64_t K, size_t* bitmaps_bytes, size_t* offsets_bytes, size_t* bases_bytes,
+                            size_t* values_max_bytes) {
+    if (R < 0 || K < 0 || R % 64 != 0 || R > (int64_t(1) << 31) || K > (int64_t(1) << 26)) return VNM_ERR_INVALID_ARG;
+    const size_t tiles = static_cast<size_t>(R / 64) * static_cast<size_t>(K);
+    if (bitmaps_bytes) *bitmaps_bytes = tiles * 8;
+    if (offsets_bytes) *offsets_bytes = tiles * 4;
+    if (bases_bytes) *bases_bytes = (static_cast<size_t>(R / 64) + 1) * 8;
+    if (values_max_bytes) *values_max_bytes = static_cast<size_t>(R) * K * 2;
+    return VNM_OK;
+}
+
+vnm_status vnm_bitmap_encode(const void* W, int64_t ld_w, int64_t R, int64_t K, void* bitmaps, void* offsets,
+                             int64_t* bases, void* values, int64_t values_capacity, int64_t* values_len,
+                             vnm_stream_t stream) {
+    if (vnm_bitmap_sizes(R, K, nullptr, nullptr, nullptr, nullptr) != VNM_OK || values_len == nullptr)
+        return VNM_ERR_INVALID_ARG;
+    if (ld_w < std::max<int64_t>(K, 1) || bases == nullptr || !aligned(bases, 8)) return VNM_ERR_INVALID_ARG;
+    const bool work = R > 0 && K > 0;
+    if (work && (W == nullptr || !aligned(W, 2) || bitmaps == nullptr || !aligned(bitmaps, 8) || offsets == nullptr ||
+                 !aligned(offsets, 4)))
+        return VNM_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (vnm::launch_bitmap_encode_counts(W, ld_w, R, K, bitmaps, offsets, bases, s) != cudaSuccess) return VNM_ERR_CUDA;
+    int64_t len = 0;
+    if (cudaMemcpyAsync(&len, bases + R / 64, sizeof(int64_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return VNM_ERR_CUDA;
+    *values_len = len;
+    if (len > values_capacity || (len > 0 && (values == nullptr || !aligned(values, 16)))) return VNM_ERR_INVALID_ARG;
+    return vnm::launch_bitmap_encode_fill(W, ld_w, R, K, bitmaps, offsets, bases, values, s) == cudaSuccess
+               ? VNM_OK
+               : VNM_ERR_CUDA;
+}
+
+int bitmap_device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    return std::max(1, sms);
+}
+
+vnm_status vnm_bitmap_spmm_workspace_size(int64_t R, int64_t K, int64_t N, size_t* bytes) {
+    if (bytes == nullptr || N < 0 || vnm_bitmap_sizes(R, K, nullptr, nullptr, nullptr, nullptr) != VNM_OK)
+        return VNM_ERR_INVALID_ARG;
+    const int s = vnm::bitmap_spmm_splits(R, K, N, bitmap_device_sms());
+    *bytes = s > 1 ? static_cast<size_t>(s) * R * N * sizeof(float) : 0;
+    return VNM_OK;
+}
+
+vnm_status vnm_bitmap_spmm(int64_t R, int64_t K, const void* bitmaps, const void* offsets, const int64_t* bases,
+                           const void* values, const void* B, int64_t ld_b, int64_t N, void* C, int64_t ld_c,
+                           vnm_dtype c_type, void* workspace, size_t workspace_bytes, vnm_stream_t stream) {
+    if (vnm_bitmap_sizes(R, K, nullptr, nullptr, nullptr, nullptr) != VNM_OK) return VNM_ERR_INVALID_ARG;
+    if (c_type != VNM_F16 && c_type != VNM_F32) return VNM_ERR_INVALID_ARG;
+    if (N < 0 || N > (int64_t(1) << 31) || ld_b < std::max<int64_t>(N, 1) || ld_c < std::max<int64_t>(N, 1))
+        return VNM_ERR_INVALID_ARG;
+    if (R == 0 || N == 0) return VNM_OK;
+    if (C == nullptr || !aligned(C, c_type == VNM_F32 ? 4 : 2)) return VNM_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const vnm::OutSpec out = vnm::out_rowmajor(C, ld_c, c_type == VNM_F32);
+    if (K == 0) return vnm::launch_splitk_reduce(nullptr, 0, R, N, out, s) == cudaSuccess ? VNM_OK : VNM_ERR_CUDA;
+    if (bitmaps == nullptr || offsets == nullptr || bases == nullptr || values == nullptr || B == nullptr ||
+        !aligned(bitmaps, 8) || !aligned(offsets, 4) || !aligned(bases, 8) || !aligned(values, 16) || !aligned(B, 2))
+        return VNM_ERR_INVALID_ARG;
+    int splits = vnm::bitmap_spmm_splits(R, K, N, bitmap_device_sms());
+    const size_t per = static_cast<size_t>(R) * N * sizeof(float);
+    if (workspace == nullptr || !aligned(workspace, 16)) workspace_bytes = 0;
+    splits = static_cast<int>(std::max<size_t>(1, std::min<size_t>(splits, workspace_bytes / per)));
+    return vnm::launch_bitmap_spmm(R, K, bitmaps, offsets, bases, values, B, ld_b, N, out, splits,
+                                   splits > 1 ? static_cast<float*>(workspace) : nullptr, s) == cudaSuccess
+               ? VNM_OK
+               : VNM_ERR_CUDA;
+}
+
 vnm_status vnm_energy_workspace_size(vnm_matrix A, size_t* bytes) {
     if (!valid_handle(A) || bytes == nullptr) return VNM_ERR_INVALID_ARG;
     *bytes = vnm::energy_workspace_bytes(A->R, A->K, A->V);

@@ -206,6 +206,18 @@ cudaError_t launch_lift_expand(const vnm_matrix_s& A, void* values2, void* meta2
 // holds only split-K partials can run.
 vnm_spmm_plan plan_without_expansion(const vnm_matrix_s& A, const void* B, int64_t ld_b, int64_t N);
 
+// Bitmap format for unstructured sparsity (R % 64 == 0): bitmaps uint64
+// [R/64][K], offsets uint32 [R/64][K] (relative to the row block's base),
+// bases int64 [R/64 + 1], values fp16 [bases[R/64]].
+cudaError_t launch_bitmap_encode_counts(const void* W, int64_t ld_w, int64_t R, int64_t K, void* bitmaps,
+                                        void* offsets, int64_t* bases, cudaStream_t stream);
+cudaError_t launch_bitmap_encode_fill(const void* W, int64_t ld_w, int64_t R, int64_t K, const void* bitmaps,
+                                      const void* offsets, const int64_t* bases, void* values, cudaStream_t stream);
+int bitmap_spmm_splits(int64_t R, int64_t K, int64_t N, int sm_count);
+cudaError_t launch_bitmap_spmm(int64_t R, int64_t K, const void* bitmaps, const void* offsets, const int64_t* bases,
+                               const void* values, const void* B, int64_t ld_b, int64_t N, const OutSpec& out,
+                               int splits, float* partial, cudaStream_t stream);
+
 // Pipeline stages the tensor-core kernel is built with for a tile (0: no such tile).
 int tc_default_stages(int tile_m, int tile_n, bool gather);
 

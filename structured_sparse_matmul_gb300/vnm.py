@@ -65,6 +65,10 @@ def _declare(L: ctypes.CDLL) -> ctypes.CDLL:
     L.vnm_energy.argtypes = [p, p, i64, ctypes.c_int, p, sz, p, p, p, p]
     L.vnm_linear.argtypes = [p, p, i64, i64, p, ctypes.c_int, p, i64, ctypes.c_int, p, sz, p]
     L.vnm_linear_workspace_size.argtypes = [p, i64, p]
+    L.vnm_bitmap_sizes.argtypes = [i64, i64, p, p, p, p]
+    L.vnm_bitmap_encode.argtypes = [p, i64, i64, i64, p, p, p, p, i64, p, p]
+    L.vnm_bitmap_spmm.argtypes = [i64, i64, p, p, p, p, p, i64, i64, p, i64, ctypes.c_int, p, sz, p]
+    L.vnm_bitmap_spmm_workspace_size.argtypes = [i64, i64, i64, p]
     L.vnm_energy_workspace_size.argtypes = [p, p]
     L.vnm_spmm.argtypes = [p, p, i64, i64, p, i64, ctypes.c_int, p, sz, p]
     L.vnm_spmm_workspace_size.argtypes = [p, i64, p]
@@ -208,6 +212,68 @@ def vnm_gemm_compress(A: VnmMatrix, X: torch.Tensor, Y: torch.Tensor, W_out: Opt
     ld_y = _rowmajor(Y, "Y") if D > 0 else 1
     _check(lib().vnm_gemm_compress(A.handle, X.data_ptr() or None, ld_x, Y.data_ptr() or None, ld_y, D, w_ptr, ld_w,
                                    _stream_ptr(stream)), "vnm_gemm_compress")
+
+
+class BitmapMatrix:
+    """A matrix in the bitmap format (bitmaps, offsets, bases, values as torch
+    tensors on one device), made by bitmap_encode."""
+
+    def __init__(self, R: int, K: int, bitmaps, offsets, bases, values, values_storage=None):
+        self.R, self.K = R, K
+        self.bitmaps, self.offsets, self.bases, self.values = bitmaps, offsets, bases, values
+        # an allocation holding `values` (an empty slice has no address of its own)
+        self._values_storage = values if values_storage is None else values_storage
+
+    def values_ptr(self) -> int:
+        return self.values.data_ptr() if self.values.numel() else self._values_storage.data_ptr()
+
+
+def bitmap_encode(W: torch.Tensor, stream=None) -> BitmapMatrix:
+    """Encode fp16 W (R x K, R % 64 == 0) into the bitmap format (two passes:
+    the arrays of positions, then the values once their length is known)."""
+    if W.dtype != torch.float16 or not W.is_cuda or W.dim() != 2:
+        raise ValueError("W must be a CUDA fp16 matrix")
+    R, K = int(W.shape[0]), int(W.shape[1])
+    nb = ctypes.c_size_t(0); no = ctypes.c_size_t(0); nbase = ctypes.c_size_t(0); nv = ctypes.c_size_t(0)
+    _check(lib().vnm_bitmap_sizes(R, K, ctypes.byref(nb), ctypes.byref(no), ctypes.byref(nbase), ctypes.byref(nv)),
+           "vnm_bitmap_sizes")
+    dev = W.device
+    bitmaps = torch.empty(max(1, nb.value // 8), dtype=torch.int64, device=dev)
+    offsets = torch.empty(max(1, no.value // 4), dtype=torch.int32, device=dev)
+    bases = torch.empty(nbase.value // 8, dtype=torch.int64, device=dev)
+    ld = _rowmajor(W, "W") if K > 0 else 1
+    need = ctypes.c_int64(0)
+    code = lib().vnm_bitmap_encode(W.data_ptr() or None, ld, R, K, bitmaps.data_ptr(), offsets.data_ptr(),
+                                   bases.data_ptr(), None, 0, ctypes.byref(need), _stream_ptr(stream))
+    values = torch.empty(max(8, int(need.value)), dtype=torch.float16, device=dev)
+    if code == VNM_ERR_INVALID_ARG and need.value > 0:
+        code = lib().vnm_bitmap_encode(W.data_ptr() or None, ld, R, K, bitmaps.data_ptr(), offsets.data_ptr(),
+                                       bases.data_ptr(), values.data_ptr(), values.numel(), ctypes.byref(need),
+                                       _stream_ptr(stream))
+    _check(code, "vnm_bitmap_encode")
+    return BitmapMatrix(R, K, bitmaps, offsets, bases, values[:int(need.value)], values)
+
+
+def bitmap_spmm_workspace_size(R: int, K: int, N: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().vnm_bitmap_spmm_workspace_size(R, K, N, ctypes.byref(n)), "vnm_bitmap_spmm_workspace_size")
+    return int(n.value)
+
+
+def bitmap_spmm(A: BitmapMatrix, B: torch.Tensor, C: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                stream=None) -> None:
+    """C = A . B for A in the bitmap format (B fp16 K x N, C fp16 or fp32 R x N)."""
+    if B.dtype != torch.float16 or not B.is_cuda or B.dim() != 2 or B.shape[0] != A.K:
+        raise ValueError("B must be a CUDA fp16 tensor of shape (K, N)")
+    N = int(B.shape[1])
+    if not C.is_cuda or tuple(C.shape) != (A.R, N):
+        raise ValueError("C must be a CUDA tensor of shape (R, N)")
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().vnm_bitmap_spmm(A.R, A.K, A.bitmaps.data_ptr(), A.offsets.data_ptr(), A.bases.data_ptr(),
+                                 A.values_ptr() or None, B.data_ptr() or None, _rowmajor(B, "B") if N else 1, N,
+                                 C.data_ptr() or None, _rowmajor(C, "C") if N else 1, _c_type(C), ws_ptr, ws_bytes,
+                                 _stream_ptr(stream)), "vnm_bitmap_spmm")
 
 
 VNM_ACT_NONE, VNM_ACT_RELU, VNM_ACT_GELU = 0, 1, 2

@@ -39,7 +39,8 @@ def test_header_declares_the_boundary():
     for want in ("vnm_sizes", "vnm_matrix_create", "vnm_matrix_destroy", "vnm_compress", "vnm_decompress",
                  "vnm_spmm", "vnm_spmm_workspace_size", "vnm_spmm_plan_query", "vnm_spmm_with_plan",
                  "vnm_get_status", "vnm_status_string", "vnm_version", "vnm_gemm_compress", "vnm_energy", "vnm_energy_workspace_size", "vnm_linear",
-                 "vnm_linear_workspace_size"):
+                 "vnm_linear_workspace_size", "vnm_bitmap_sizes", "vnm_bitmap_encode", "vnm_bitmap_spmm",
+                 "vnm_bitmap_spmm_workspace_size"):
         assert want in names, want
 
 

@@ -417,12 +417,41 @@ def check_linear_worked_row(L):
     assert zero[0, 0] == 0.0
 
 
+def check_bitmap_format(L):
+    """The bitmap format on a hand-made 64 x 3 matrix: column 0 holds 1 at
+    row 0, -2 at row 5 and 3 at row 63 (bitmap bits 0, 5, 63; three values
+    padded to 8); column 1 only -0.0 (no bit, no values); column 2 is full
+    (all 64 bits, 64 values). Offsets 0, 8, 8; the length 72. Then random
+    matrices of 30-70% zeros decode back to themselves (-0.0 as +0.0), and the
+    product equals numpy's of the dense matrix."""
+    W = np.zeros((64, 3), dtype=np.float16)
+    W[0, 0], W[5, 0], W[63, 0] = 1, -2, 3
+    W[7, 1] = -0.0
+    W[:, 2] = np.arange(1, 65)
+    bm, off, bases, vals = oracle.bitmap_encode(W)
+    assert int(bm[0, 0]) == (1 | 1 << 5 | 1 << 63) and int(bm[0, 1]) == 0 and int(bm[0, 2]) == (1 << 64) - 1
+    assert off[0].tolist() == [0, 8, 8] and bases.tolist() == [0, 72]
+    assert vals.view(np.float16)[:8].tolist() == [1, -2, 3, 0, 0, 0, 0, 0]
+    assert vals.view(np.float16)[8:].tolist() == list(range(1, 65))
+    rng = np.random.default_rng(13)
+    for sparsity in (0.3, 0.5, 0.7):
+        D = (rng.standard_normal((128, 40)) * (rng.random((128, 40)) >= sparsity)).astype(np.float16)
+        D[3, 4] = -0.0
+        enc = oracle.bitmap_encode(D)
+        back = oracle.bitmap_decode(*enc, 128, 40)
+        assert np.array_equal(back.astype(np.float64), D.astype(np.float64))
+        assert int(enc[2][-1]) == sum((int(c) + 7) // 8 * 8 for c in (D.reshape(2, 64, 40) != 0).sum(axis=1).ravel())
+        B = rng.standard_normal((40, 5)).astype(np.float16)
+        assert np.allclose(oracle.bitmap_spmm(*enc, 128, 40, B), D.astype(np.float64) @ B.astype(np.float64),
+                           rtol=0, atol=1e-12)
+
+
 PINS = [check_worked_example, check_worked_local_index, check_worked_product,
         check_storage_arithmetic, check_brute_force_ties, check_brute_force_subnormals,
         check_brute_force_normal, check_invariants_and_round_trip, check_spmm_against_numpy,
         check_fig3_fixture, check_gemm_compress_identity, check_gemm_compress_rank1,
         check_gemm_compress_rounding, check_energy_worked_example, check_energy_invariants,
-        check_linear_worked_row]
+        check_linear_worked_row, check_bitmap_format]
 
 
 # ----------------------------------------------------------------------------
