@@ -61,15 +61,16 @@ def parse_args():
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload kernel table")
     ap.add_argument("--per-config-launches", type=int, default=10,
                     help="kernel launches per graph in the per-workload table (median of 7 replays)")
-    ap.add_argument("--profile-op", choices=["gemm_compress", "linear"], default=None,
+    ap.add_argument("--profile-op", choices=["gemm_compress", "linear", "bitmap"], default=None,
                     help="run a few launches of one of the other entry points on its first table case and exit "
                          "(for ncu captures)")
     return ap.parse_args()
 
 
 def profile_op(op: str) -> None:
-    """A few launches of vnm_gemm_compress or vnm_linear on the first case of
-    their bench tables, checked for a clean status (for ncu captures)."""
+    """A few launches of vnm_gemm_compress, vnm_linear or vnm_bitmap_spmm on
+    a case of their bench tables, checked for a clean status (for ncu
+    captures)."""
     import torch
 
     from structured_sparse_matmul_gb300 import vnm
@@ -78,6 +79,20 @@ def profile_op(op: str) -> None:
     torch.cuda.set_device(dev)
     gen = torch.Generator(device=dev)
     gen.manual_seed(7)
+    if op == "bitmap":
+        R, K, sp = BITMAP_CASES[0]
+        W = (torch.randn(R, K, device=dev, generator=gen) * 0.02).half()
+        cut = W.abs().float().flatten().kthvalue(max(1, int(sp * R * K))).values
+        W[W.abs().float() <= cut] = 0
+        Bm = vnm.bitmap_encode(W)
+        B = torch.randn(K, 1, device=dev, generator=gen).half()
+        C = torch.empty(R, 1, dtype=torch.float16, device=dev)
+        ws = torch.empty(max(1, vnm.bitmap_spmm_workspace_size(R, K, 1) // 4), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            vnm.bitmap_spmm(Bm, B, C, workspace=ws)
+        torch.cuda.synchronize(dev)
+        print(f"{op}: 3 launches, ok")
+        return
     if op == "gemm_compress":
         R, K, D, V, M = GEMM_COMPRESS_CASES[1]
         A = vnm.vnm_matrix_alloc(R, K, V, M, dev)

@@ -108,12 +108,14 @@ int effective_stream_splits(const vnm_matrix_s& A, int requested) {
     return s;
 }
 
-// K splits of the streaming CUDA-core path (N <= 8): up to four CTAs per SM,
-// at most 4 splits (8 measured slower on every decode shape), every split at
-// least one staged chunk of blocks. No workspace: the splits of a V-block
-// row reduce within their cluster.
+// K splits of the streaming CUDA-core path (N <= 8): the pipelined kernel's
+// choice where it applies; else up to four CTAs per SM, at most 4 splits (8
+// measured slower on every decode shape), every split at least one staged
+// chunk of blocks. No workspace: the splits of a V-block row reduce within
+// their cluster.
 int64_t stream_splits(const vnm_matrix_s& A, int64_t N) {
     if (N > 8 || N < 1) return 1;
+    if (const int ps = vnm::stream_pipe_splits(A, N)) return ps;
     const int64_t nblk = A.K / A.M;
     const int64_t rows_blocks = std::max<int64_t>(1, A.R / A.V);
     int64_t s = ceil_div(4 * static_cast<int64_t>(A.sm_count), rows_blocks);

@@ -11,6 +11,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "vnm_internal.h"
 #include "vnm_ptx.cuh"
@@ -435,6 +436,244 @@ cudaError_t launch_stream4(const StreamArgs& p, cudaStream_t stream) {
     return cudaLaunchKernelEx(&cfg, spmm_stream_kernel<NB, RW, U, PLAIN>, p);
 }
 
+// ---------------------------------------------------------------------------
+// Pipelined streaming path (row-major B and C, N <= 8, V a multiple of 64,
+// K/M a multiple of 32): the same CTA work as above, but a chunk is 32
+// blocks (lane = block) of 64 rows, and its values, m-indices and
+// column-loc words (each a 16-byte aligned run per row) are copied into a
+// ring of kPipeStages shared-memory stages with cp.async, up to
+// kPipeStages - 1 chunks ahead of the one being multiplied. The CTA's rows
+// of B (its K range, at most kPipeBHalves values) are loaded into shared
+// memory once; the selected rows of B for the next chunk are gathered from
+// there into the other of two staging buffers after this chunk is
+// multiplied, so that no chunk waits for a round trip to memory once the
+// ring is full.
+constexpr int kPipeWarps = 8;
+constexpr int kPipeRows = 64;    // rows per pass: 8 warps x 8
+constexpr int kPipeChunk = 32;   // blocks per chunk
+constexpr int kPipeStages = 5;        // 46 KB: three chunks in flight
+constexpr int kPipeBHalves = 12288;   // 24 KB: the CTA's rows of B
+// CTAs per SM the registers are budgeted for (shared memory allows three);
+// eight columns of B keep 64 accumulators a thread
+__host__ __device__ constexpr int pipe_resident(int nb) { return nb <= 4 ? 3 : 2; }
+constexpr int kPipeMaxDevices = 64;
+
+struct PipeStage {
+    uint32_t vals[kPipeRows][kPipeChunk];     // 8 KB: the rows' value words
+    uint8_t meta[kPipeRows][kPipeChunk / 2];  // 1 KB: their m-index bytes
+    uint32_t col[kPipeChunk];                 // the V-block row's column-loc words
+};
+
+template <int NB>
+__global__ void __launch_bounds__(32 * kPipeWarps, pipe_resident(NB)) spmm_stream_pipe_kernel(const StreamArgsRM p) {
+    constexpr int kStride = 4 * NB + (NB >= 4 ? 4 : 0);
+    constexpr int kRW = kPipeRows / kPipeWarps;
+    constexpr int kBEntries = kPipeChunk * 4 * NB;  // (block, slot, column) entries of a chunk's B
+    constexpr int kBPer = (kBEntries + 32 * kPipeWarps - 1) / (32 * kPipeWarps);
+    static_assert(kRW * kPipeWarps == kPipeRows && kPipeStages >= 3, "pipeline shape");
+    extern __shared__ __align__(16) uint8_t pipe_smem[];
+    PipeStage* st = reinterpret_cast<PipeStage*>(pipe_smem);  // [kPipeStages]
+    __half* Bs = reinterpret_cast<__half*>(pipe_smem + sizeof(PipeStage) * kPipeStages);  // [K range][NB]
+    __shared__ __align__(16) __half Bc[2][kPipeChunk * kStride];
+    __shared__ float red[kPipeRows][NB];
+    const int64_t i = blockIdx.x / p.splits;
+    const int s = static_cast<int>(blockIdx.x % p.splits);
+    const int64_t jb = s * p.bps < p.nblk ? s * p.bps : p.nblk;
+    const int64_t je = jb + p.bps < p.nblk ? jb + p.bps : p.nblk;
+    const int nch = static_cast<int>((je - jb) / kPipeChunk);  // split bounds are multiples of 32 blocks
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t* crow = p.colidx + i * p.nblk;
+
+    for (int rbase = 0; rbase < p.V; rbase += kPipeRows) {
+        const int64_t row0 = i * p.V + rbase;
+        // chunk c -> stage c % kPipeStages: values (8 granules a row), m-indices (1 a row), column-loc (8)
+        auto issue = [&](int c) {
+            PipeStage& g = st[c % kPipeStages];
+            const int64_t j0 = jb + static_cast<int64_t>(c) * kPipeChunk;
+#pragma unroll
+            for (int h = 0; h < kPipeRows * 8 / (32 * kPipeWarps); ++h) {
+                const int x = tid + 32 * kPipeWarps * h, r = x >> 3, q = x & 7;
+                cp_async_16(smem_u32(&g.vals[r][4 * q]), p.values + (row0 + r) * p.nblk + j0 + 4 * q, 16);
+            }
+            if (tid < kPipeRows)
+                cp_async_16(smem_u32(&g.meta[tid][0]), p.meta + (row0 + tid) * p.mpitch + j0 / 2, 16);
+            else if (tid < kPipeRows + 8)
+                cp_async_16(smem_u32(&g.col[4 * (tid - kPipeRows)]), crow + j0 + 4 * (tid - kPipeRows), 16);
+        };
+        // this thread's entries of chunk c's selected rows of B (stage c has landed)
+        auto load_b = [&](int c, __half (&b)[kBPer]) {
+            const PipeStage& g = st[c % kPipeStages];
+#pragma unroll
+            for (int e = 0; e < kBPer; ++e) {
+                const int q = tid + 32 * kPipeWarps * e;
+                b[e] = __float2half_rn(0.f);
+                if (q < kBEntries) {
+                    const int n = q % NB, slot = (q / NB) & 3, jl = q / (4 * NB);
+                    // column-loc byte, clamped so that a corrupt array cannot address past K
+                    const uint32_t cb = min((g.col[jl] >> (8 * slot)) & 0xFFu, static_cast<uint32_t>(p.M - 1));
+                    b[e] = Bs[((c * kPipeChunk + jl) * p.M + cb) * NB + n];
+                }
+            }
+        };
+        auto store_b = [&](int buf, const __half (&b)[kBPer]) {
+#pragma unroll
+            for (int e = 0; e < kBPer; ++e) {
+                const int q = tid + 32 * kPipeWarps * e;
+                if (q < kBEntries) {
+                    const int n = q % NB, slot = (q / NB) & 3, jl = q / (4 * NB);
+                    Bc[buf][jl * kStride + 4 * n + slot] = b[e];
+                }
+            }
+        };
+
+        float acc[kRW][NB];
+#pragma unroll
+        for (int t = 0; t < kRW; ++t)
+#pragma unroll
+            for (int n = 0; n < NB; ++n) acc[t][n] = 0.f;
+        __half breg[kBPer];
+        // fill the ring; the CTA's rows of B (zeros past N) while it fills
+#pragma unroll
+        for (int c = 0; c < kPipeStages - 1; ++c) {
+            if (c < nch) issue(c);
+            cp_async_commit();
+        }
+        if (rbase == 0) {
+            const int64_t kcols = (je - jb) * p.M;
+            for (int64_t e = tid; e < kcols * NB; e += blockDim.x) {
+                const int64_t k = e / NB;
+                const int n = static_cast<int>(e - k * NB);
+                Bs[e] = n < p.N ? p.B[(jb * p.M + k) * p.ld_b + n] : __float2half_rn(0.f);
+            }
+        }
+        if (nch > 0) {
+            cp_async_wait<kPipeStages - 2>();
+            __syncthreads();
+            load_b(0, breg);
+            store_b(0, breg);
+        }
+        for (int c = 0; c < nch; ++c) {
+            // stages c and c + 1 landed (every thread's copies), chunk c's B
+            // stored and chunk c - 1 multiplied by every thread
+            cp_async_wait<kPipeStages - 3>();
+            __syncthreads();
+            if (c + kPipeStages - 1 < nch) issue(c + kPipeStages - 1);  // over chunk c - 1's stage
+            cp_async_commit();
+            if (c + 1 < nch) load_b(c + 1, breg);
+            const PipeStage& g = st[c % kPipeStages];
+            const uint2* b = reinterpret_cast<const uint2*>(&Bc[c & 1][lane * kStride]);
+#pragma unroll
+            for (int t = 0; t < kRW; ++t) {
+                const int r = warp + kPipeWarps * t;
+                const uint32_t a = g.vals[r][lane];
+                // this block's 4 bits: slots s0 (bits 0-1, low half) and s1 (bits 2-3)
+                const uint32_t code = static_cast<uint32_t>(g.meta[r][lane >> 1]) >> (4 * (lane & 1));
+                // byte-permute selector of the two slots' halves: byte s of 0x76543210 is the
+                // selector pair (2s, 2s + 1), picked for s0 and s1 by a byte permute of its own
+                const uint32_t sel = __byte_perm(0x76543210u, 0u, (code & 3u) | ((code & 0xCu) << 2));
+#pragma unroll
+                for (int n = 0; n < NB; ++n) {
+                    const uint2 w = b[n];  // the 4 slots of column n
+                    const uint32_t pr = __byte_perm(w.x, w.y, sel);
+                    acc[t][n] = fma_f16(a, pr, acc[t][n]);
+                    acc[t][n] = fma_f16(a >> 16, pr >> 16, acc[t][n]);
+                }
+            }
+            if (c + 1 < nch) store_b((c + 1) & 1, breg);  // over chunk c - 1's B
+        }
+        cp_async_wait_all();
+
+        auto store = [&](int r, int n, float v) {
+            const int64_t row = row0 + r;
+            if (p.c_f32)
+                static_cast<float*>(p.C)[row * p.ld_c + n] = v;
+            else
+                static_cast<__half*>(p.C)[row * p.ld_c + n] = __float2half_rn(v);
+        };
+#pragma unroll
+        for (int t = 0; t < kRW; ++t) {
+            const int r = warp + kPipeWarps * t;
+            float out = 0.f;
+#pragma unroll
+            for (int n = 0; n < NB; ++n) {
+                float v = acc[t][n];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+                if (lane == n) out = v;
+            }
+            if (p.splits > 1) {
+                if (lane < NB) red[r][lane] = out;
+            } else if (lane < p.N && lane < NB) {
+                store(r, lane, out);
+            }
+        }
+        if (p.splits > 1) {
+            // every CTA of the cluster holds its partial sums of the pass's rows
+            cluster_sync_all();
+            const uint32_t red0 = smem_u32(&red[0][0]);
+            for (int e = tid; e < kPipeRows * NB; e += blockDim.x) {
+                const int r = e / NB, n = e % NB;
+                if (r % p.splits != s || n >= p.N) continue;
+                float v = 0.f;
+                for (int q = 0; q < p.splits; ++q)
+                    v += dsmem_ld_f32(dsmem_map(red0 + static_cast<uint32_t>(e) * 4u, static_cast<uint32_t>(q)));
+                store(r, n, v);
+            }
+            // no CTA reuses or leaves its partial sums while another may still read them
+            cluster_sync_all();
+        }
+        __syncthreads();  // the ring and the B buffers are free for the next pass
+    }
+}
+
+// Blocks of a split of the pipelined kernel: on chunk bounds (a split may
+// be empty: its CTA adds zeros).
+inline int64_t pipe_split_blocks(int64_t nblk, int splits) {
+    const int64_t per = (nblk + splits - 1) / splits;
+    return (per + kPipeChunk - 1) / kPipeChunk * kPipeChunk;
+}
+
+inline bool pipe_aligned(const void* x) { return (reinterpret_cast<uintptr_t>(x) & 15u) == 0; }
+
+inline int pipe_nb(int64_t N) { return N <= 1 ? 1 : N <= 2 ? 2 : N <= 4 ? 4 : 8; }
+
+template <int NB>
+cudaError_t launch_stream_pipe(const StreamArgsRM& q, cudaStream_t stream) {
+    StreamArgsRM p = q;
+    p.bps = pipe_split_blocks(p.nblk, p.splits);
+    const int64_t ctas = (p.R / p.V) * p.splits;
+    constexpr size_t smem = sizeof(PipeStage) * kPipeStages + kPipeBHalves * sizeof(__half);
+    // the shared-memory opt-in, once per device
+    static std::atomic<bool> attr_set[kPipeMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kPipeMaxDevices) return cudaErrorInvalidDevice;
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
+        e = cudaFuncSetAttribute(spmm_stream_pipe_kernel<NB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        attr_set[dev].store(true, std::memory_order_relaxed);
+    }
+    if (p.splits == 1) {
+        spmm_stream_pipe_kernel<NB><<<static_cast<unsigned>(ctas), 32 * kPipeWarps, smem, stream>>>(p);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(p.splits);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas));
+    cfg.blockDim = dim3(32 * kPipeWarps);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, spmm_stream_pipe_kernel<NB>, p);
+}
+
 template <int NB, int RW, int U>
 cudaError_t launch_stream_rm(const StreamArgs& q, cudaStream_t stream) {
     StreamArgsRM p;
@@ -454,6 +693,10 @@ cudaError_t launch_stream_rm(const StreamArgs& q, cudaStream_t stream) {
     p.splits = q.splits;
     p.bps = q.bps;
     p.c_f32 = q.out.f32;
+    // the pipelined kernel where every copy is a 16-byte aligned run
+    if (p.V % kPipeRows == 0 && p.nblk % kPipeChunk == 0 && pipe_aligned(p.values) && pipe_aligned(p.meta) &&
+        pipe_aligned(p.colidx) && pipe_split_blocks(p.nblk, p.splits) * p.M * NB <= kPipeBHalves)
+        return launch_stream_pipe<NB>(p, stream);
     const int64_t ctas = (p.R / p.V) * p.splits;
     if (p.splits == 1) {
         spmm_stream_rm_kernel<NB, RW, U><<<static_cast<unsigned>(ctas), 32 * kStreamWarps, 0, stream>>>(p);
@@ -523,6 +766,23 @@ cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t bk, i
 }
 
 int stream_chunk_blocks(int V) { return V <= 32 ? 256 : V <= 64 ? 128 : 64; }
+
+int stream_pipe_splits(const vnm_matrix_s& A, int64_t N) {
+    const int64_t nblk = A.K / A.M;
+    if (N < 1 || N > 8 || A.V % kPipeRows != 0 || nblk % kPipeChunk != 0 || !pipe_aligned(A.values) ||
+        !pipe_aligned(A.meta) || !pipe_aligned(A.colidx))
+        return 0;
+    // the CTAs that are resident at once, the fewest splits whose rows of B fit
+    const int64_t rows_blocks = std::max<int64_t>(1, A.R / A.V);
+    int need = 1;
+    while (need <= 8 && pipe_split_blocks(nblk, need) * A.M * pipe_nb(N) > kPipeBHalves) need *= 2;
+    if (need > 8) return 0;
+    int s = need;
+    while (s * 2 <= 4 && rows_blocks * s * 2 <= pipe_resident(pipe_nb(N)) * static_cast<int64_t>(A.sm_count) &&
+           nblk >= static_cast<int64_t>(s) * 2 * kPipeChunk)
+        s *= 2;
+    return s;
+}
 
 cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t bk, int64_t bn, int64_t N,
                                const OutSpec& out, int splits, cudaStream_t stream) {

@@ -91,6 +91,9 @@ cudaError_t launch_decompress(const vnm_matrix_s& A, void* W, int64_t ld_w, cuda
 cudaError_t launch_spmm_stream(const vnm_matrix_s& A, const void* B, int64_t bk, int64_t bn, int64_t N,
                                const OutSpec& out, int splits, cudaStream_t stream);
 int stream_chunk_blocks(int V);
+// Splits of the pipelined streaming kernel for this matrix and N (1, 2, 4 or
+// 8), 0 where it does not apply (then the general streaming kernel runs).
+int stream_pipe_splits(const vnm_matrix_s& A, int64_t N);
 
 // CUDA-core SpMM; writes C directly (fp16 or fp32).
 cudaError_t launch_spmm_simt(const vnm_matrix_s& A, const void* B, int64_t bk, int64_t bn, int64_t N,

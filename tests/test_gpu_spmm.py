@@ -454,11 +454,12 @@ def test_streaming_small_n(R, K, V, M, N, c_dtype):
 
 
 @pytest.mark.parametrize("splits", [1, 2, 4, 8])
-def test_streaming_split_clusters(splits):
+@pytest.mark.parametrize("R,K,N,V,M", [(192, 4096, 5, 64, 8),
+                                       (256, 256, 3, 128, 4)])  # two row passes; 64 blocks: most splits empty
+def test_streaming_split_clusters(splits, R, K, N, V, M):
     """The streaming kernel's K splits (1, 2, 4 or 8 CTAs of a V-block row in
     one cluster, reduced in split order through distributed shared memory),
     ragged N, both C types; the same C bit for bit on a second run."""
-    R, K, N, V, M = 192, 4096, 5, 64, 8
     A, B, comp = _setup(R, K, N, V, M, seed=36)
     plan = vnm.vnm_spmm_plan_query(A, to_dev(B))
     assert plan.path == vnm.VNM_PATH_SIMT, plan.as_dict()
