@@ -167,21 +167,22 @@ __device__ __forceinline__ void bm_load_meta(const uint64_t* bm_row, const uint3
     }
 }
 
-// First value and end (both multiples of 8) of a chunk of cnt >= 1 tiles.
-__device__ __forceinline__ void bm_chunk_span(uint64_t bm, uint32_t of, int cnt, uint32_t& st, uint32_t& en) {
+// First value and end (both multiples of 8) of a chunk of cnt >= 1 tiles
+// (64-bit: a row block's last tile may end at 2^32).
+__device__ __forceinline__ void bm_chunk_span(uint64_t bm, uint32_t of, int cnt, uint64_t& st, uint64_t& en) {
     st = __shfl_sync(0xFFFFFFFFu, of, 0);
     const uint32_t of_l = __shfl_sync(0xFFFFFFFFu, of, cnt - 1);
     const uint32_t lo = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(bm), cnt - 1);
     const uint32_t hi = __shfl_sync(0xFFFFFFFFu, static_cast<uint32_t>(bm >> 32), cnt - 1);
-    en = of_l + ((static_cast<uint32_t>(__popc(lo) + __popc(hi)) + 7u) & ~7u);
+    en = static_cast<uint64_t>(of_l) + ((static_cast<uint32_t>(__popc(lo) + __popc(hi)) + 7u) & ~7u);
 }
 
 // The chunk's values (a 16-byte aligned run of at most kBmSlot) -> the ring,
 // value v at ring[v mod kBmRing] (a 16-byte granule never wraps). Two
 // consecutive chunks span at most kBmRing values, so the next chunk's copy
 // never lands on the values of the chunk being decoded.
-__device__ __forceinline__ void bm_copy_values(const __half* vals, uint32_t st, uint32_t en, __half* ring, int lane) {
-    for (uint32_t v = st + 8 * lane; v < en; v += 8 * 32)
+__device__ __forceinline__ void bm_copy_values(const __half* vals, uint64_t st, uint64_t en, __half* ring, int lane) {
+    for (uint64_t v = st + 8 * lane; v < en; v += 8 * 32)
         cp_async_16(smem_u32(ring + (v & (kBmRing - 1))), vals + v, 16);
 }
 
@@ -233,7 +234,7 @@ __global__ void __launch_bounds__(32 * kBmWarps, bm_resident(NB)) bitmap_spmm_ke
                 bsh[e] = n0 + n < p.N ? __half2float(p.B[(ks + kk) * p.ld_b + n0 + n]) : 0.f;
             }
             if (nchunks > 0) {
-                uint32_t st, en;
+                uint64_t st, en;
                 bm_chunk_span(bm_c, of_c, static_cast<int>(k1 - k0 < kBmChunk ? k1 - k0 : kBmChunk), st, en);
                 bm_copy_values(vals, st, en, ring[warp], lane);
             }
@@ -248,7 +249,7 @@ __global__ void __launch_bounds__(32 * kBmWarps, bm_resident(NB)) bitmap_spmm_ke
                 bm_load_meta(bm_row, off_row, kc + 2 * kBmChunk + lane, k1, bm_n2, of_n2);
                 if (c + 1 < nchunks) {
                     const int64_t cnt_n = k1 - kc - kBmChunk;
-                    uint32_t st, en;
+                    uint64_t st, en;
                     bm_chunk_span(bm_n, of_n, static_cast<int>(cnt_n < kBmChunk ? cnt_n : kBmChunk), st, en);
                     bm_copy_values(vals, st, en, ring[warp], lane);
                 }

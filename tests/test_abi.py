@@ -6,6 +6,7 @@ import os
 import re
 import shutil
 
+import numpy as np
 import pytest
 
 import oracle
@@ -95,6 +96,25 @@ def test_handle_checks_without_gpu(libvnm):
     # arrays must be 16-byte aligned device allocations
     assert libvnm.vnm_matrix_create(16, 64, 16, 8, 8, 16, 32, ctypes.byref(ctypes.c_void_p())) == \
         vnm.VNM_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("R,K", [(64, 1), (128, 40), (4096, 11008), (0, 7), (64, 0)])
+def test_bitmap_sizes_match_oracle(libvnm, R, K):
+    """vnm_bitmap_sizes (host only) against the oracle's arrays: one 8-byte
+    bitmap and one 4-byte offset per 64-row column tile, R/64 + 1 bases, and
+    at most R*K fp16 values (every tile full)."""
+    rng = np.random.default_rng(R + K)
+    W = (rng.standard_normal((R, K)) * (rng.random((R, K)) > 0.5)).astype(np.float16)
+    bm, off, bases, _ = oracle.bitmap_encode(W)
+    out = [ctypes.c_size_t() for _ in range(4)]
+    assert libvnm.vnm_bitmap_sizes(R, K, *[ctypes.byref(o) for o in out]) == 0
+    assert [o.value for o in out] == [bm.nbytes, off.nbytes, bases.nbytes, 2 * R * K]
+
+
+@pytest.mark.parametrize("R,K", [(100, 8), (-64, 8), (64, -1), (64, 1 << 27)])
+def test_bitmap_sizes_rejected(libvnm, R, K):
+    from structured_sparse_matmul_gb300 import vnm
+    assert libvnm.vnm_bitmap_sizes(R, K, None, None, None, None) == vnm.VNM_ERR_INVALID_ARG
 
 
 def test_product_path_does_not_import_the_oracle():
