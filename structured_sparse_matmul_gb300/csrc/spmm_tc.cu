@@ -983,23 +983,29 @@ cudaError_t dispatch_bn(const TcLaunch& L, const TcArgs& p, cudaStream_t stream)
 // 4-column groups 2j, 2j+1 of a plain 2:4 row (values2 [R][K/2], meta2
 // [R][K/8]: one byte of two 4-bit codes per block). A thread takes four
 // consecutive blocks of a row: 16 bytes of values, 16 bits of m-indices and
-// 16 bytes of column-loc in; 32 bytes of values and 4 m-index bytes out.
-__global__ void __launch_bounds__(256) lift_expand_kernel(const uint32_t* __restrict__ values,
-                                                          const uint8_t* __restrict__ meta,
-                                                          const uint32_t* __restrict__ colidx, int64_t R, int64_t nblk,
-                                                          int64_t mpitch, int V, uint32_t* __restrict__ values2,
-                                                          uint32_t* __restrict__ meta2) {
+// 16 bytes of column-loc in; 32 bytes of values and 4 m-index bytes out. The
+// grid is (quads of a row, rows): the row and its V-block row come from the
+// block index, with no per-element division.
+constexpr int kLiftThreads = 128;
+
+__global__ void __launch_bounds__(kLiftThreads) lift_expand_kernel(const uint32_t* __restrict__ values,
+                                                                   const uint8_t* __restrict__ meta,
+                                                                   const uint32_t* __restrict__ colidx, int64_t R,
+                                                                   int64_t nblk, int64_t mpitch, int V,
+                                                                   uint32_t* __restrict__ values2,
+                                                                   uint32_t* __restrict__ meta2) {
     __shared__ uint2 tab[64];
     if (threadIdx.x < 64) tab[threadIdx.x] = lift_entry(threadIdx.x >> 3, threadIdx.x & 7u);
     __syncthreads();
     const int64_t quads = nblk / 4;  // nblk = K / 8, K % 128 == 0: whole quads
-    const int64_t total = R * quads;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < total;
-         q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = q / quads, j0 = (q - r * quads) * 4;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kLiftThreads + threadIdx.x;
+    if (t >= quads) return;  // no barrier follows
+    const int64_t j0 = 4 * t;
+    for (int64_t r = blockIdx.y; r < R; r += gridDim.y) {
+        const int64_t vrow = static_cast<int64_t>(static_cast<uint32_t>(r) / static_cast<uint32_t>(V));  // R < 2^31
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(values + r * nblk + j0));
         const uint32_t m = __ldg(reinterpret_cast<const uint16_t*>(meta + r * mpitch + j0 / 2));
-        const uint4 c = __ldg(reinterpret_cast<const uint4*>(colidx + (r / V) * nblk + j0));
+        const uint4 c = __ldg(reinterpret_cast<const uint4*>(colidx + vrow * nblk + j0));
         const uint32_t vs[4] = {v.x, v.y, v.z, v.w}, cs[4] = {c.x, c.y, c.z, c.w};
         uint32_t out[8], codes = 0;
 #pragma unroll
@@ -1024,10 +1030,13 @@ __global__ void __launch_bounds__(256) lift_expand_kernel(const uint32_t* __rest
 cudaError_t launch_lift_expand(const vnm_matrix_s& A, void* values2, void* meta2, cudaStream_t stream) {
     const int64_t nblk = A.K / A.M;
     if (A.M != 8 || A.K % kTcStageK != 0) return cudaErrorInvalidValue;
-    const int64_t total = A.R * (nblk / 4);
-    if (total == 0) return cudaSuccess;
-    const int64_t blocks = std::min<int64_t>((total + 255) / 256, static_cast<int64_t>(A.sm_count) * 8);
-    lift_expand_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+    const int64_t quads = nblk / 4;
+    if (A.R == 0 || quads == 0) return cudaSuccess;
+    // about 16 CTAs of 128 threads per SM, each a slice of a row's quads over a stride of rows
+    const int64_t gx = (quads + kLiftThreads - 1) / kLiftThreads;
+    const int64_t gy = std::max<int64_t>(1, std::min<int64_t>({A.R, 65535, 16 * static_cast<int64_t>(A.sm_count) / gx}));
+    if (gx > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    lift_expand_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), kLiftThreads, 0, stream>>>(
         static_cast<const uint32_t*>(A.values), static_cast<const uint8_t*>(A.meta),
         static_cast<const uint32_t*>(A.colidx), A.R, nblk, meta_pitch(A.K, A.M), A.V,
         static_cast<uint32_t*>(values2), static_cast<uint32_t*>(meta2));
