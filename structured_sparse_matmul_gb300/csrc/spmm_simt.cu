@@ -438,43 +438,38 @@ cudaError_t launch_stream4(const StreamArgs& p, cudaStream_t stream) {
 
 // ---------------------------------------------------------------------------
 // Pipelined streaming path (row-major B and C, N <= 8, V a multiple of 64,
-// K/M a multiple of 32): the same CTA work as above, but a chunk is 32
-// blocks (lane = block) of 64 rows, and its values, m-indices and
-// column-loc words (each a 16-byte aligned run per row) are copied into a
-// ring of kPipeStages shared-memory stages with cp.async, up to
-// kPipeStages - 1 chunks ahead of the one being multiplied. The CTA's rows
-// of B (its K range, at most kPipeBHalves values) are loaded into shared
-// memory once; the selected rows of B for the next chunk are gathered from
-// there into the other of two staging buffers after this chunk is
-// multiplied, so that no chunk waits for a round trip to memory once the
-// ring is full.
+// K/M a multiple of 32): the same CTA work as above, 64 rows a pass, but
+// each warp owns 8 consecutive rows and streams them on its own: a chunk is
+// 32 blocks (lane = block), and the warp's values, m-indices and the
+// V-block row's column-loc words of a chunk (16-byte aligned runs) are
+// copied into the warp's ring of kPipeStages shared-memory stages with
+// cp.async, up to kPipeStages - 1 chunks ahead of the one being multiplied.
+// The CTA's rows of B (its K range, at most kPipeBHalves values) are loaded
+// into shared memory once; each lane gathers its own block's 4 selected rows
+// of B from there. No CTA barrier sits in the chunk loop: a warp waits only
+// for its own copies.
 constexpr int kPipeWarps = 8;
-constexpr int kPipeRows = 64;    // rows per pass: 8 warps x 8
-constexpr int kPipeChunk = 32;   // blocks per chunk
-constexpr int kPipeStages = 5;        // 46 KB: three chunks in flight
+constexpr int kPipeRows = 64;         // rows per pass: 8 warps x 8
+constexpr int kPipeWarpRows = kPipeRows / kPipeWarps;
+constexpr int kPipeChunk = 32;        // blocks per chunk
+constexpr int kPipeStages = 4;        // 40 KB for the CTA: three chunks in flight per warp
 constexpr int kPipeBHalves = 12288;   // 24 KB: the CTA's rows of B
 // CTAs per SM the registers are budgeted for (shared memory allows three);
 // eight columns of B keep 64 accumulators a thread
 __host__ __device__ constexpr int pipe_resident(int nb) { return nb <= 4 ? 3 : 2; }
 constexpr int kPipeMaxDevices = 64;
 
-struct PipeStage {
-    uint32_t vals[kPipeRows][kPipeChunk];     // 8 KB: the rows' value words
-    uint8_t meta[kPipeRows][kPipeChunk / 2];  // 1 KB: their m-index bytes
-    uint32_t col[kPipeChunk];                 // the V-block row's column-loc words
+struct PipeStage {  // one warp's chunk
+    uint32_t vals[kPipeWarpRows][kPipeChunk];     // 1 KB: the rows' value words
+    uint8_t meta[kPipeWarpRows][kPipeChunk / 2];  // their m-index bytes
+    uint32_t col[kPipeChunk];                     // the V-block row's column-loc words
 };
 
 template <int NB>
 __global__ void __launch_bounds__(32 * kPipeWarps, pipe_resident(NB)) spmm_stream_pipe_kernel(const StreamArgsRM p) {
-    constexpr int kStride = 4 * NB + (NB >= 4 ? 4 : 0);
-    constexpr int kRW = kPipeRows / kPipeWarps;
-    constexpr int kBEntries = kPipeChunk * 4 * NB;  // (block, slot, column) entries of a chunk's B
-    constexpr int kBPer = (kBEntries + 32 * kPipeWarps - 1) / (32 * kPipeWarps);
-    static_assert(kRW * kPipeWarps == kPipeRows && kPipeStages >= 3, "pipeline shape");
+    static_assert(kPipeWarpRows * kPipeWarps == kPipeRows && kPipeStages >= 2, "pipeline shape");
     extern __shared__ __align__(16) uint8_t pipe_smem[];
-    PipeStage* st = reinterpret_cast<PipeStage*>(pipe_smem);  // [kPipeStages]
-    __half* Bs = reinterpret_cast<__half*>(pipe_smem + sizeof(PipeStage) * kPipeStages);  // [K range][NB]
-    __shared__ __align__(16) __half Bc[2][kPipeChunk * kStride];
+    __half* Bs = reinterpret_cast<__half*>(pipe_smem);  // [K range][NB]
     __shared__ float red[kPipeRows][NB];
     const int64_t i = blockIdx.x / p.splits;
     const int s = static_cast<int>(blockIdx.x % p.splits);
@@ -482,117 +477,99 @@ __global__ void __launch_bounds__(32 * kPipeWarps, pipe_resident(NB)) spmm_strea
     const int64_t je = jb + p.bps < p.nblk ? jb + p.bps : p.nblk;
     const int nch = static_cast<int>((je - jb) / kPipeChunk);  // split bounds are multiples of 32 blocks
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    PipeStage* ring = reinterpret_cast<PipeStage*>(pipe_smem + kPipeBHalves * sizeof(__half)) + warp * kPipeStages;
     const uint32_t* crow = p.colidx + i * p.nblk;
 
+    // the CTA's rows of B (zeros past N), once for every pass
+    const int64_t kcols = (je - jb) * p.M;
+    for (int64_t e = tid; e < kcols * NB; e += blockDim.x) {
+        const int64_t k = e / NB;
+        const int n = static_cast<int>(e - k * NB);
+        Bs[e] = n < p.N ? p.B[(jb * p.M + k) * p.ld_b + n] : __float2half_rn(0.f);
+    }
+    __syncthreads();
+
     for (int rbase = 0; rbase < p.V; rbase += kPipeRows) {
-        const int64_t row0 = i * p.V + rbase;
-        // chunk c -> stage c % kPipeStages: values (8 granules a row), m-indices (1 a row), column-loc (8)
+        const int64_t row0 = i * p.V + rbase + kPipeWarpRows * warp;  // this warp's first row
+        // chunk c -> stage c % kPipeStages of this warp: values (8 granules a row),
+        // m-indices (1 a row), column-loc (8)
         auto issue = [&](int c) {
-            PipeStage& g = st[c % kPipeStages];
+            PipeStage& g = ring[c % kPipeStages];
             const int64_t j0 = jb + static_cast<int64_t>(c) * kPipeChunk;
 #pragma unroll
-            for (int h = 0; h < kPipeRows * 8 / (32 * kPipeWarps); ++h) {
-                const int x = tid + 32 * kPipeWarps * h, r = x >> 3, q = x & 7;
+            for (int h = 0; h < kPipeWarpRows * 8 / 32; ++h) {
+                const int x = lane + 32 * h, r = x >> 3, q = x & 7;
                 cp_async_16(smem_u32(&g.vals[r][4 * q]), p.values + (row0 + r) * p.nblk + j0 + 4 * q, 16);
             }
-            if (tid < kPipeRows)
-                cp_async_16(smem_u32(&g.meta[tid][0]), p.meta + (row0 + tid) * p.mpitch + j0 / 2, 16);
-            else if (tid < kPipeRows + 8)
-                cp_async_16(smem_u32(&g.col[4 * (tid - kPipeRows)]), crow + j0 + 4 * (tid - kPipeRows), 16);
-        };
-        // this thread's entries of chunk c's selected rows of B (stage c has landed)
-        auto load_b = [&](int c, __half (&b)[kBPer]) {
-            const PipeStage& g = st[c % kPipeStages];
-#pragma unroll
-            for (int e = 0; e < kBPer; ++e) {
-                const int q = tid + 32 * kPipeWarps * e;
-                b[e] = __float2half_rn(0.f);
-                if (q < kBEntries) {
-                    const int n = q % NB, slot = (q / NB) & 3, jl = q / (4 * NB);
-                    // column-loc byte, clamped so that a corrupt array cannot address past K
-                    const uint32_t cb = min((g.col[jl] >> (8 * slot)) & 0xFFu, static_cast<uint32_t>(p.M - 1));
-                    b[e] = Bs[((c * kPipeChunk + jl) * p.M + cb) * NB + n];
-                }
-            }
-        };
-        auto store_b = [&](int buf, const __half (&b)[kBPer]) {
-#pragma unroll
-            for (int e = 0; e < kBPer; ++e) {
-                const int q = tid + 32 * kPipeWarps * e;
-                if (q < kBEntries) {
-                    const int n = q % NB, slot = (q / NB) & 3, jl = q / (4 * NB);
-                    Bc[buf][jl * kStride + 4 * n + slot] = b[e];
-                }
-            }
+            if (lane < kPipeWarpRows)
+                cp_async_16(smem_u32(&g.meta[lane][0]), p.meta + (row0 + lane) * p.mpitch + j0 / 2, 16);
+            else if (lane < kPipeWarpRows + 8)
+                cp_async_16(smem_u32(&g.col[4 * (lane - kPipeWarpRows)]), crow + j0 + 4 * (lane - kPipeWarpRows), 16);
         };
 
-        float acc[kRW][NB];
+        float acc[kPipeWarpRows][NB];
 #pragma unroll
-        for (int t = 0; t < kRW; ++t)
+        for (int t = 0; t < kPipeWarpRows; ++t)
 #pragma unroll
             for (int n = 0; n < NB; ++n) acc[t][n] = 0.f;
-        __half breg[kBPer];
-        // fill the ring; the CTA's rows of B (zeros past N) while it fills
 #pragma unroll
         for (int c = 0; c < kPipeStages - 1; ++c) {
             if (c < nch) issue(c);
             cp_async_commit();
         }
-        if (rbase == 0) {
-            const int64_t kcols = (je - jb) * p.M;
-            for (int64_t e = tid; e < kcols * NB; e += blockDim.x) {
-                const int64_t k = e / NB;
-                const int n = static_cast<int>(e - k * NB);
-                Bs[e] = n < p.N ? p.B[(jb * p.M + k) * p.ld_b + n] : __float2half_rn(0.f);
-            }
-        }
-        if (nch > 0) {
-            cp_async_wait<kPipeStages - 2>();
-            __syncthreads();
-            load_b(0, breg);
-            store_b(0, breg);
-        }
         for (int c = 0; c < nch; ++c) {
-            // stages c and c + 1 landed (every thread's copies), chunk c's B
-            // stored and chunk c - 1 multiplied by every thread
-            cp_async_wait<kPipeStages - 3>();
-            __syncthreads();
+            cp_async_wait<kPipeStages - 2>();  // chunk c (this lane's copies)
+            __syncwarp();                      // ... every lane's; chunk c - 1 read by every lane
             if (c + kPipeStages - 1 < nch) issue(c + kPipeStages - 1);  // over chunk c - 1's stage
             cp_async_commit();
-            if (c + 1 < nch) load_b(c + 1, breg);
-            const PipeStage& g = st[c % kPipeStages];
-            const uint2* b = reinterpret_cast<const uint2*>(&Bc[c & 1][lane * kStride]);
+            const PipeStage& g = ring[c % kPipeStages];
+            // this lane's block: its 4 selected rows of B, column n's 4 slots as one uint2
+            const uint32_t w = g.col[lane];
+            const int64_t kb = (static_cast<int64_t>(c) * kPipeChunk + lane) * p.M;  // in the CTA's K range
+            uint2 bq[NB];
+            {
+                uint32_t h[4][NB];
 #pragma unroll
-            for (int t = 0; t < kRW; ++t) {
-                const int r = warp + kPipeWarps * t;
-                const uint32_t a = g.vals[r][lane];
+                for (int slot = 0; slot < 4; ++slot) {
+                    // column-loc byte, clamped so that a corrupt array cannot address past K
+                    const uint32_t cb = min((w >> (8 * slot)) & 0xFFu, static_cast<uint32_t>(p.M - 1));
+                    const __half* src = Bs + (kb + cb) * NB;
+#pragma unroll
+                    for (int n = 0; n < NB; ++n) h[slot][n] = __half_as_ushort(src[n]);
+                }
+#pragma unroll
+                for (int n = 0; n < NB; ++n)
+                    bq[n] = make_uint2(h[0][n] | (h[1][n] << 16), h[2][n] | (h[3][n] << 16));
+            }
+#pragma unroll
+            for (int t = 0; t < kPipeWarpRows; ++t) {
+                const uint32_t a = g.vals[t][lane];
                 // this block's 4 bits: slots s0 (bits 0-1, low half) and s1 (bits 2-3)
-                const uint32_t code = static_cast<uint32_t>(g.meta[r][lane >> 1]) >> (4 * (lane & 1));
+                const uint32_t code = static_cast<uint32_t>(g.meta[t][lane >> 1]) >> (4 * (lane & 1));
                 // byte-permute selector of the two slots' halves: byte s of 0x76543210 is the
                 // selector pair (2s, 2s + 1), picked for s0 and s1 by a byte permute of its own
                 const uint32_t sel = __byte_perm(0x76543210u, 0u, (code & 3u) | ((code & 0xCu) << 2));
 #pragma unroll
                 for (int n = 0; n < NB; ++n) {
-                    const uint2 w = b[n];  // the 4 slots of column n
-                    const uint32_t pr = __byte_perm(w.x, w.y, sel);
+                    const uint32_t pr = __byte_perm(bq[n].x, bq[n].y, sel);
                     acc[t][n] = fma_f16(a, pr, acc[t][n]);
                     acc[t][n] = fma_f16(a >> 16, pr >> 16, acc[t][n]);
                 }
             }
-            if (c + 1 < nch) store_b((c + 1) & 1, breg);  // over chunk c - 1's B
         }
         cp_async_wait_all();
+        __syncwarp();  // the warp's ring is free for the next pass
 
-        auto store = [&](int r, int n, float v) {
-            const int64_t row = row0 + r;
+        auto store = [&](int r, int n, float v) {  // r: row of the pass
+            const int64_t row = i * p.V + rbase + r;
             if (p.c_f32)
                 static_cast<float*>(p.C)[row * p.ld_c + n] = v;
             else
                 static_cast<__half*>(p.C)[row * p.ld_c + n] = __float2half_rn(v);
         };
 #pragma unroll
-        for (int t = 0; t < kRW; ++t) {
-            const int r = warp + kPipeWarps * t;
+        for (int t = 0; t < kPipeWarpRows; ++t) {
+            const int r = kPipeWarpRows * warp + t;
             float out = 0.f;
 #pragma unroll
             for (int n = 0; n < NB; ++n) {
@@ -622,7 +599,6 @@ __global__ void __launch_bounds__(32 * kPipeWarps, pipe_resident(NB)) spmm_strea
             // no CTA reuses or leaves its partial sums while another may still read them
             cluster_sync_all();
         }
-        __syncthreads();  // the ring and the B buffers are free for the next pass
     }
 }
 
@@ -642,7 +618,7 @@ cudaError_t launch_stream_pipe(const StreamArgsRM& q, cudaStream_t stream) {
     StreamArgsRM p = q;
     p.bps = pipe_split_blocks(p.nblk, p.splits);
     const int64_t ctas = (p.R / p.V) * p.splits;
-    constexpr size_t smem = sizeof(PipeStage) * kPipeStages + kPipeBHalves * sizeof(__half);
+    constexpr size_t smem = kPipeBHalves * sizeof(__half) + sizeof(PipeStage) * kPipeStages * kPipeWarps;
     // the shared-memory opt-in, once per device
     static std::atomic<bool> attr_set[kPipeMaxDevices];
     int dev = 0;
