@@ -659,26 +659,27 @@ def measure_bitmap(dev, peaks, launches: int):
 
 def measure_energy(dev):
     """Energy (magnitude preservation) of the three selection policies at the
-    V:N:M densities 2/M on a synthetic N(0, 0.02) weight of the 768 x 768
-    shape of the pages' Figure 11 study (VENOM section 5), and the time of one
-    vnm_energy call (its host read-back included) on a 4096 x 4096 weight."""
+    V:N:M densities 2/4 .. 2/40 on a synthetic N(0, 0.02) weight of the
+    768 x 768 shape of the pages' Figure 11 study (VENOM section 5; 768 x 960
+    for 2:40, which 768 columns do not divide), and the time of one vnm_energy
+    call (its host read-back included) on a 4096 x 4096 weight."""
     import torch
 
     from structured_sparse_matmul_gb300 import inputs, vnm
 
-    W_h = inputs.normal_f16((768, 768), 1011, 0, 0.02)
-    W = torch.from_numpy(W_h).to(dev)
     table = {}
-    for M in (4, 8, 16, 32):
-        row = {}
-        A1 = vnm.vnm_matrix_alloc(768, 768, 16, M, dev)
+    # 768 x 768 for M dividing 768; 768 x 960 for M = 40 (the densest the study goes to)
+    for M, K, seed in ((4, 768, 1011), (8, 768, 1011), (16, 768, 1011), (32, 768, 1011), (40, 960, 1013)):
+        W = torch.from_numpy(inputs.normal_f16((768, K), seed, 0, 0.02)).to(dev)
+        row = {"weight": f"768x{K}"}
+        A1 = vnm.vnm_matrix_alloc(768, K, 16, M, dev)
         row["unstructured"] = vnm.vnm_energy(A1, W, vnm.VNM_PATTERN_UNSTRUCTURED)[0]
         for V in (1, 16, 32, 64, 128):
-            A = vnm.vnm_matrix_alloc(768, 768, V, M, dev)
+            A = vnm.vnm_matrix_alloc(768, K, V, M, dev)
             vnm.vnm_compress(A, W)
             row[f"{V}:2:{M}"] = vnm.vnm_energy(A, W, vnm.VNM_PATTERN_VNM)[0]
         for l in (4, 8, 16, 32):
-            A = vnm.vnm_matrix_alloc(768, 768, l, M, dev)
+            A = vnm.vnm_matrix_alloc(768, K, l, M, dev)
             row[f"vw_{l}"] = vnm.vnm_energy(A, W, vnm.VNM_PATTERN_VECTORWISE)[0]
         table[f"density 2/{M}"] = row
     big = torch.from_numpy(inputs.normal_f16((4096, 4096), 1012, 0, 0.02)).to(dev)
@@ -695,7 +696,7 @@ def measure_energy(dev):
             vnm.vnm_energy(A, big, pat, workspace=ws)
             ts.append((time.perf_counter() - t0) * 1e6)
         times[name] = statistics.median(ts)
-    return {"weight": "768x768 N(0, 0.02), synthetic (the shape of the pages' Figure 11 study)",
+    return {"weight": "768x768 N(0, 0.02), synthetic (the shape of the pages' Figure 11 study); 768x960 for 2:40",
             "energy": table,
             "call_us_4096x4096_v64m8": times}
 

@@ -29,7 +29,7 @@ def _check(W, V, M, ld=None):
 
 
 @pytest.mark.parametrize("R,K,V,M", [(768, 768, 16, 4), (768, 768, 64, 8), (768, 768, 128, 16), (768, 768, 1, 32),
-                                     (272, 520, 16, 8), (4096, 4096, 64, 8)])
+                                     (768, 960, 32, 40), (768, 960, 128, 20), (272, 520, 16, 8), (4096, 4096, 64, 8)])
 def test_normal_weights(R, K, V, M):
     _check(inputs.normal_f16((R, K), 51, 0, 0.02), V, M)
 
