@@ -60,7 +60,7 @@ def parse_args():
                     help="streams that carry a step's host-to-device copies (row chunks of W, then B)")
     ap.add_argument("--no-per-config", action="store_true", help="skip the per-workload kernel table")
     ap.add_argument("--per-config-launches", type=int, default=10,
-                    help="kernel launches per graph in the per-workload table (median of 7 replays)")
+                    help="kernel launches per graph in the per-workload table (median of 10 replays)")
     ap.add_argument("--profile-op", choices=["gemm_compress", "linear", "bitmap"], default=None,
                     help="run a few launches of one of the other entry points on its first table case and exit "
                          "(for ncu captures)")
@@ -363,6 +363,8 @@ def run_reference(args, case):
 
 # Sources of each profiled kernel: a summary's DRAM traffic is used only
 # while these files are unchanged since the capture.
+REPLAYS = 10  # replays of a timed graph whose median is reported (per kernel and per workload case)
+
 KERNEL_SOURCES = {
     "spmm_tc_kernel": ["spmm_tc.cu", "vnm_ptx.cuh", "vnm_internal.h", "api.cu"],  # api.cu: the tile plan
     "compress": ["compress.cu", "vnm_internal.h"],
@@ -429,7 +431,7 @@ def roofline_of(case, peaks, spmm_us, a_bytes):
 
 
 def _time_graph(dev, fn, launches: int) -> float:
-    """Median of 7 replays of a CUDA graph of `launches` calls fn(i, stream),
+    """Median of REPLAYS replays of a CUDA graph of `launches` calls fn(i, stream),
     in microseconds per call (events on the replaying stream)."""
     import torch
     cur = torch.cuda.current_stream(dev)
@@ -446,7 +448,7 @@ def _time_graph(dev, fn, launches: int) -> float:
     g.replay()
     torch.cuda.synchronize(dev)
     ts = []
-    for _ in range(7):
+    for _ in range(REPLAYS):
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(cur)
@@ -517,7 +519,7 @@ def measure_gemm_compress(dev, peaks, launches: int):
             "sets": n_sets}
         del sets, W
         torch.cuda.empty_cache()
-    return {"launches_per_graph": launches, "replays": 7, "statistic": "median",
+    return {"launches_per_graph": launches, "replays": REPLAYS, "statistic": "median",
             "inputs": "torch seeded device generator, X, Y ~ N(0, 1)",
             "l2_eviction": "rotating input sets of more than twice the L2 in each graph", "cases": out}
 
@@ -598,7 +600,7 @@ def measure_linear(dev, peaks, launches: int):
             "roofline": {"t_roof_us": t_roof, "frac": t_roof / t_plain}, "sets": n_sets}
         del sets, Wd, Wp, Xt, Ct, ws
         torch.cuda.empty_cache()
-    return {"launches_per_graph": launches, "replays": 7, "statistic": "median",
+    return {"launches_per_graph": launches, "replays": REPLAYS, "statistic": "median",
             "inputs": "torch seeded device generator, W ~ N(0, 0.02), X ~ N(0, 1), bias ~ N(0, 0.25)",
             "l2_eviction": "rotating X / Y sets of more than twice the L2 in each graph", "cases": out}
 
@@ -652,7 +654,7 @@ def measure_bitmap(dev, peaks, launches: int):
                 "format_bytes_vs_dense": a_bytes / (2.0 * R * K)}
         del mats, W, A
         torch.cuda.empty_cache()
-    return {"launches_per_graph": launches, "replays": 7, "statistic": "median",
+    return {"launches_per_graph": launches, "replays": REPLAYS, "statistic": "median",
             "inputs": "torch seeded device generator, W ~ N(0, 0.02) with the smallest |w| zeroed, B ~ N(0, 1)",
             "cases": out}
 
@@ -690,7 +692,7 @@ def measure_energy(dev):
     for name, pat in (("vnm", vnm.VNM_PATTERN_VNM), ("unstructured", vnm.VNM_PATTERN_UNSTRUCTURED),
                       ("vectorwise", vnm.VNM_PATTERN_VECTORWISE)):
         ts = []
-        for _ in range(7):
+        for _ in range(REPLAYS):
             torch.cuda.synchronize(dev)
             t0 = time.perf_counter()
             vnm.vnm_energy(A, big, pat, workspace=ws)
@@ -703,7 +705,7 @@ def measure_energy(dev):
 
 def measure_per_config(dev, peaks, launches: int):
     """Every case of workloads 1-5: SpMM and compress launch times (median of
-    7 replays of a graph of `launches` launches over rotating input sets that
+    REPLAYS replays of a graph of `launches` launches over rotating input sets that
     together exceed twice the L2), the SpMM roofline, the plan, and dense
     torch.matmul on the same shape (context). Inputs come from torch's seeded
     device generator with the workloads' distributions (A ~ N(0, 0.02),
@@ -731,7 +733,7 @@ def measure_per_config(dev, peaks, launches: int):
         g.replay()
         torch.cuda.synchronize(dev)
         ts = []
-        for _ in range(7):
+        for _ in range(REPLAYS):
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(cur)
@@ -796,7 +798,7 @@ def measure_per_config(dev, peaks, launches: int):
             }
             del sets
             torch.cuda.empty_cache()
-    return {"launches_per_graph": launches, "replays": 7, "statistic": "median",
+    return {"launches_per_graph": launches, "replays": REPLAYS, "statistic": "median",
             "inputs": "torch seeded device generator, A ~ N(0, 0.02), B ~ N(0, 1)",
             "l2_eviction": "rotating input sets of more than twice the L2 in each graph", "cases": table}
 
@@ -961,9 +963,9 @@ def main():
     elapsed_ms = timed(graph)
     dist_barrier(world, dev)
     serial_ms = timed(graph_serial) / steps
-    # each kernel's average launch duration: median of 5 replays of its graph
-    spmm_ms = statistics.median(timed(graph_spmm) for _ in range(5)) / steps
-    comp_ms = statistics.median(timed(graph_comp) for _ in range(5)) / steps
+    # each kernel's average launch duration: median of REPLAYS replays of its graph
+    spmm_ms = statistics.median(timed(graph_spmm) for _ in range(REPLAYS)) / steps
+    comp_ms = statistics.median(timed(graph_comp) for _ in range(REPLAYS)) / steps
     # launch floor: K empty kernels (a sleep of zero cycles), captured and
     # timed the same way
     empty_ms = None
