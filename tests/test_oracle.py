@@ -415,15 +415,20 @@ def check_linear_worked_row(L):
     assert np.allclose(g - gneg, want + 0.5, rtol=0, atol=1e-12)
     zero = oracle.linear(values, meta, colidx, 1, 8, 1, 4, np.zeros((1, 8), np.float16), None, oracle.ACT_GELU)
     assert zero[0, 0] == 0.0
+    # GELU(1) = Phi(1), the standard normal distribution function at 1 (erf form, not the tanh approximation)
+    one = oracle.linear(values, meta, colidx, 1, 8, 1, 4, np.zeros((1, 8), np.float16), np.ones(1, np.float16),
+                        oracle.ACT_GELU)
+    assert abs(one[0, 0] - 0.8413447460685429) < 1e-12
 
 
 def check_bitmap_format(L):
     """The bitmap format on a hand-made 64 x 3 matrix: column 0 holds 1 at
     row 0, -2 at row 5 and 3 at row 63 (bitmap bits 0, 5, 63; three values
     padded to 8); column 1 only -0.0 (no bit, no values); column 2 is full
-    (all 64 bits, 64 values). Offsets 0, 8, 8; the length 72. Then random
-    matrices of 30-70% zeros decode back to themselves (-0.0 as +0.0), and the
-    product equals numpy's of the dense matrix."""
+    (all 64 bits, 64 values). Offsets 0, 8, 8; the length 72. An all-zero
+    matrix has no values; a matrix without zeros has full tiles and no
+    padding. Then random matrices of 30-70% zeros decode back to themselves
+    (-0.0 as +0.0), and the product equals numpy's of the dense matrix."""
     W = np.zeros((64, 3), dtype=np.float16)
     W[0, 0], W[5, 0], W[63, 0] = 1, -2, 3
     W[7, 1] = -0.0
@@ -433,6 +438,13 @@ def check_bitmap_format(L):
     assert off[0].tolist() == [0, 8, 8] and bases.tolist() == [0, 72]
     assert vals.view(np.float16)[:8].tolist() == [1, -2, 3, 0, 0, 0, 0, 0]
     assert vals.view(np.float16)[8:].tolist() == list(range(1, 65))
+    # no non-zero at all: empty values, every offset and base 0; no zero at all: full tiles, no padding
+    bm, off, bases, vals = oracle.bitmap_encode(np.zeros((128, 5), np.float16))
+    assert not bm.any() and not off.any() and bases.tolist() == [0, 0, 0] and vals.size == 0
+    full = np.arange(1, 64 * 3 + 1, dtype=np.float16).reshape(64, 3)
+    bm, off, bases, vals = oracle.bitmap_encode(full)
+    assert all(int(b) == (1 << 64) - 1 for b in bm[0]) and off[0].tolist() == [0, 64, 128]
+    assert bases.tolist() == [0, 192] and vals.view(np.float16)[64:128].tolist() == full[:, 1].tolist()
     rng = np.random.default_rng(13)
     for sparsity in (0.3, 0.5, 0.7):
         D = (rng.standard_normal((128, 40)) * (rng.random((128, 40)) >= sparsity)).astype(np.float16)
@@ -552,4 +564,49 @@ def test_mutants_are_caught(tmp_path):
                 pin(L)
             except (AssertionError, oracle.OracleError, IndexError, ValueError):
                 failed.append(pin.__name__)
+        assert failed, f"no pin caught the planted mistake: {what}"
+
+
+# Planted mistakes in the oracle's Python functions (the Linear form, the
+# energy and the bitmap format): (what, pattern in oracle/__init__.py,
+# replacement, the function it lands in).
+PY_MUTANTS = [
+    ("bitmap bits MSB-first", r"np\.uint64\(sum\(1 << r for r in rows\)\)",
+     "np.uint64(sum(1 << (63 - r) for r in rows))", "bitmap_encode"),
+    ("bitmap values not padded", r"padded = \(len\(rows\) \+ 7\) // 8 \* 8", "padded = len(rows)", "bitmap_encode"),
+    ("bitmap counts -0.0 as a non-zero", r"if int\(col\[r\]\) & 0x7FFF\]", "if int(col[r])]", "bitmap_encode"),
+    ("bitmap decode ignores the row block's base", r"at = int\(bases\[i\]\) \+ int\(offsets\[i, k\]\)",
+     "at = int(offsets[i, k])", "bitmap_decode"),
+    ("unstructured keeps the smallest", r"flat = np\.sort\(u\.ravel\(\)\)\[::-1\]", "flat = np.sort(u.ravel())",
+     "energy"),
+    ("vector-wise ranks columns by their largest |w|",
+     r"col = u\[i \* V:\(i \+ 1\) \* V\]\.sum\(axis=0, dtype=np\.uint64\)",
+     "col = u[i * V:(i + 1) * V].max(axis=0)", "energy"),
+    ("GELU by the tanh approximation",
+     r"Y = Y \* \(1\.0 \+ np\.vectorize\(math\.erf\)\(Y / math\.sqrt\(2\.0\)\)\) / 2\.0",
+     "Y = 0.5 * Y * (1.0 + np.tanh(math.sqrt(2.0 / math.pi) * (Y + 0.044715 * Y ** 3)))", "linear"),
+    ("bias dropped", r"Y \+= np\.asarray\(bias, dtype=np\.float16\)", "Y += 0 * np.asarray(bias, dtype=np.float16)",
+     "linear"),
+]
+
+
+def test_python_mutants_are_caught(monkeypatch):
+    """Every planted mistake in the oracle's Python functions fails at least
+    one pin (the mutated function replaces the oracle's for the run)."""
+    path = os.path.join(os.path.dirname(oracle.__file__), "__init__.py")
+    src = open(path).read()
+    L = oracle.lib()
+    for what, pat, rep, fn in PY_MUTANTS:
+        new, n = re.subn(pat, rep, src, count=1)
+        assert n == 1, f"mutant pattern not found: {what}"
+        ns = {"__name__": "oracle_mutant", "__file__": path}
+        exec(compile(new, path, "exec"), ns)
+        failed = []
+        with monkeypatch.context() as m:
+            m.setattr(oracle, fn, ns[fn])
+            for pin in PINS:
+                try:
+                    pin(L)
+                except (AssertionError, oracle.OracleError, IndexError, ValueError):
+                    failed.append(pin.__name__)
         assert failed, f"no pin caught the planted mistake: {what}"
